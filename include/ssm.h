@@ -1,0 +1,142 @@
+/*
+ * ssm.h -- C ABI of the B300 (sm_103a) selective-scan library (libssm_b300.so).
+ *
+ * Two operations of the Mamba selective state-space layer, both hand-written CUDA:
+ *
+ *   ssm_selective_scan_fwd   the fused forward pass over a whole sequence
+ *   ssm_state_update         the single-token recurrent update used in decoding
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are described by ssm_tensor_t: a DEVICE pointer, an element type and a
+ *    shape. Storage is dense row-major (last index fastest); there are no strides.
+ *  - Ownership: the caller owns every buffer. The library allocates nothing, frees
+ *    nothing and never synchronises; work is enqueued on the caller's stream
+ *    (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *  - Errors: all arguments are validated on the host before anything is enqueued.
+ *    Any status other than SSM_OK means nothing was launched and no output was
+ *    written. A failed launch returns SSM_ERR_CUDA (from cudaGetLastError).
+ *  - Pointers must be 16-byte aligned (a PyTorch allocation always is).
+ *  - Outputs must not overlap any input (SSM_ERR_LAYOUT), except where an entry point
+ *    says it updates a tensor in place.
+ *  - Every I/O tensor (u, delta, z, B, C, x) of one call has the same element type,
+ *    SSM_BF16 or SSM_F32. A, D, delta_bias and the states are always SSM_F32.
+ *    The output y has the I/O type or SSM_F32 (full-precision output of a bf16 call).
+ *  - Arithmetic: fp32 throughout (state, discretisation, contraction); bf16 outputs
+ *    are rounded to nearest-even from fp32.
+ *  - N (state size) must be 4, 8 or 16, else SSM_ERR_UNSUPPORTED.
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+typedef struct {
+  void* data;          /* device pointer; may be NULL only when the tensor is empty */
+  ssm_dtype_t dtype;
+  int32_t ndim;        /* number of valid entries in shape[] */
+  int64_t shape[3];
+} ssm_tensor_t;
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_NULL = 1,            /* a required descriptor or data pointer is NULL */
+  SSM_ERR_SHAPE = 2,           /* ndim or a dimension does not match the contract */
+  SSM_ERR_DTYPE = 3,           /* element type not allowed, or I/O types differ */
+  SSM_ERR_LAYOUT = 4,          /* misaligned pointer, or an output overlaps an input */
+  SSM_ERR_UNSUPPORTED = 5,     /* a valid request this build does not implement (e.g. N) */
+  SSM_ERR_CUDA = 6,            /* the CUDA runtime reported an error at launch */
+  SSM_ERR_DEVICE_TIMEOUT = 7   /* a kernel gave up a bounded wait (see ssm_device_error) */
+} ssm_status_t;
+
+/*
+ * ssm_selective_scan_fwd -- fused selective-scan forward pass.
+ *
+ * For each batch row b and channel d, from h = 0 ("8.7 State Space Models (Mamba)",
+ * section 2.1, h(0) = 0), for t = 0 .. L-1:
+ *   dt        = delta_softplus ? softplus(delta[b,t,d] + bias[d]) : delta[b,t,d] + bias[d]
+ *   h[n]      = exp(dt * A[d,n]) * h[n] + dt * B[b,t,n] * u[b,t,d]      (n = 0 .. N-1)
+ *   v         = sum_n C[b,t,n] * h[n] + D[d] * u[b,t,d]
+ *   y[b,t,d]  = z ? v * silu(z[b,t,d]) : v
+ * and finally last_state[b,d,:] = h.
+ * Sources: "Mamba and State Space Models" (placement-prep chapter), sections
+ * "Selective scan pseudo-code" (the recurrence and read-out) and "Discretization and
+ * initialization details" (A-bar = exp(Delta A), B-bar = Delta B, Delta = softplus(Wx + b));
+ * "Arch 02: Mamba SSM" deck, continuous form y = Cx + Du (the D skip) and the selective
+ * SSM block (per-token B, C of shape (B, L, N)); "8.7 State Space Models (Mamba)",
+ * section 6 (the SiLU(z) gate on the SSM output).
+ *
+ *   u          (batch, L, D)  I/O type        input sequence
+ *   delta      (batch, L, D)  I/O type        raw step size (before bias and softplus)
+ *   A          (D, N)         f32             diagonal state matrix (any values; normally < 0)
+ *   B, C       (batch, L, N)  I/O type        per-token input / output projections
+ *   D          (D)            f32, nullable   skip weight (NULL = no skip)
+ *   z          (batch, L, D)  I/O type, nullable   gate input (NULL = no gate)
+ *   delta_bias (D)            f32, nullable   added to delta before softplus (NULL = 0)
+ *   delta_softplus            0 or 1
+ *   y          (batch, L, D)  I/O type or f32   output, written
+ *   last_state (batch, D, N)  f32, nullable   final state, written (NULL = not written)
+ *   stream                    cudaStream_t
+ * batch == 0 or L == 0 is a valid no-op; with L == 0 a non-NULL last_state is zeroed.
+ * The per-step state never reaches global memory.
+ */
+ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                    const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                    const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                    int delta_softplus, ssm_tensor_t* y,
+                                    ssm_tensor_t* last_state, void* stream);
+
+/*
+ * ssm_state_update -- one recurrent decode step, state updated in place.
+ *
+ * For each batch row b and channel d:
+ *   state[b,d,n] = exp(delta[b,d] * A[d,n]) * state[b,d,n] + delta[b,d] * B[b,n] * x[b,d]
+ *   v            = sum_n C[b,n] * state[b,d,n] + D[d] * x[b,d]
+ *   y[b,d]       = z ? v * silu(z[b,d]) : v
+ * delta is the final step size: no bias and no softplus are applied.
+ * Sources: "8.7 State Space Models (Mamba)", section 5 (O(1) work and a fixed d*n state
+ * per generated token); "Mamba and State Space Models", "Selective scan pseudo-code"
+ * (one step of the loop body) and "Common Pitfalls" (the state after a prefix is
+ * reusable: last_state of ssm_selective_scan_fwd continues here).
+ *
+ *   state  (batch, D, N)  f32             read and overwritten in place
+ *   x      (batch, D)     I/O type        token input
+ *   delta  (batch, D)     I/O type        step size
+ *   A      (D, N)         f32
+ *   B, C   (batch, N)     I/O type
+ *   D      (D)            f32, nullable
+ *   z      (batch, D)     I/O type, nullable
+ *   y      (batch, D)     I/O type or f32   output, written
+ *   stream                cudaStream_t
+ * batch == 0 is a valid no-op. Only state may alias itself; y must not overlap any input.
+ */
+ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x,
+                              const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                              const ssm_tensor_t* B, const ssm_tensor_t* C,
+                              const ssm_tensor_t* D, const ssm_tensor_t* z,
+                              ssm_tensor_t* y, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ssm_status_string(ssm_status_t status);
+
+/*
+ * ssm_device_error -- diagnostic read of the library's device-side error word on the
+ * current device. It SYNCHRONISES the given stream, returns the word in *code (0 = no
+ * error; otherwise a kernel gave up a bounded wait) and clears it. Returns SSM_OK,
+ * SSM_ERR_NULL (code == NULL) or SSM_ERR_CUDA. Kernels never trap: a wait that runs out
+ * sets this word and returns.
+ */
+ssm_status_t ssm_device_error(void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

@@ -1,0 +1,148 @@
+"""fp64 CPU oracle for the Mamba selective scan and the recurrent state update.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package. It shares
+no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, fp64, sequential); this module
+only marshals numpy arrays into it. Definitions and their sources (page title and
+section) are in the C header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libssm_oracle.so"
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(out_dir: str | None = None, plant: int = 0, force: bool = False) -> str:
+    """Compile ssm_oracle.c into a shared library; returns its path.
+
+    ``plant`` > 0 compiles a deliberately wrong variant (see ssm_oracle.c) used only by
+    the pin tests to show that each planted mistake is caught.
+    """
+    out_dir = out_dir or _HERE
+    name = LIB_NAME if plant == 0 else f"libssm_oracle_plant{plant}.so"
+    out = os.path.join(out_dir, name)
+    src = os.path.join(_HERE, "ssm_oracle.c")
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= max(
+        os.path.getmtime(src), os.path.getmtime(os.path.join(_HERE, "ssm_oracle.h"))
+    ):
+        return out
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           f"-DSSM_ORACLE_PLANT={plant}", "-o", out, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True, cwd=_HERE)
+    return out
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def _f64(a, shape=None):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor -> numpy (CPU), exact widening to fp64
+        a = a.detach().to("cpu").double().numpy()
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if shape is not None and tuple(a.shape) != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {tuple(a.shape)}")
+    return a
+
+
+class Oracle:
+    """ctypes front end over one build of the oracle library."""
+
+    def __init__(self, lib_path: str | None = None):
+        self.path = lib_path or build()
+        lib = ctypes.CDLL(self.path)
+        lib.ssm_oracle_softplus.restype = ctypes.c_double
+        lib.ssm_oracle_softplus.argtypes = [ctypes.c_double]
+        lib.ssm_oracle_silu.restype = ctypes.c_double
+        lib.ssm_oracle_silu.argtypes = [ctypes.c_double]
+        lib.ssm_oracle_fwd.restype = ctypes.c_int
+        lib.ssm_oracle_fwd.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int, _dp, _dp, _dp,
+                                                                               ctypes.c_int]
+        lib.ssm_oracle_state_update.restype = ctypes.c_int
+        lib.ssm_oracle_state_update.argtypes = [_i64, _i64, _i64] + [_dp] * 9
+        self.lib = lib
+
+    def softplus(self, r: float) -> float:
+        return self.lib.ssm_oracle_softplus(float(r))
+
+    def silu(self, z: float) -> float:
+        return self.lib.ssm_oracle_silu(float(z))
+
+    def selective_scan_fwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           delta_softplus=True, h0=None, nthreads=0):
+        """Returns (y, last_state) as fp64 numpy arrays.
+
+        u, delta, z: (batch, L, D); A: (D, N); B, C: (batch, L, N); D, delta_bias: (D);
+        h0: (batch, D, N) initial state (zeros if None).
+        """
+        u = _f64(u)
+        batch, L, Dm = u.shape
+        A = _f64(A)
+        N = A.shape[1]
+        delta = _f64(delta, (batch, L, Dm))
+        B = _f64(B, (batch, L, N))
+        C = _f64(C, (batch, L, N))
+        A = _f64(A, (Dm, N))
+        D = _f64(D, (Dm,))
+        z = _f64(z, (batch, L, Dm))
+        delta_bias = _f64(delta_bias, (Dm,))
+        h0 = _f64(h0, (batch, Dm, N))
+        y = np.empty((batch, L, Dm), np.float64)
+        last = np.empty((batch, Dm, N), np.float64)
+        rc = self.lib.ssm_oracle_fwd(batch, L, Dm, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                     _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                     _ptr(h0), _ptr(y), _ptr(last), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("ssm_oracle_fwd rejected its arguments")
+        return y, last
+
+    def state_update(self, state, x, delta, A, B, C, D=None, z=None):
+        """One decode step. Returns (y, new_state); the input state is not modified.
+
+        state: (batch, D, N); x, delta, z: (batch, D); A: (D, N); B, C: (batch, N); D: (D).
+        """
+        st = _f64(state).copy()
+        batch, Dm, N = st.shape
+        x = _f64(x, (batch, Dm))
+        delta = _f64(delta, (batch, Dm))
+        A = _f64(A, (Dm, N))
+        B = _f64(B, (batch, N))
+        C = _f64(C, (batch, N))
+        D = _f64(D, (Dm,))
+        z = _f64(z, (batch, Dm))
+        y = np.empty((batch, Dm), np.float64)
+        rc = self.lib.ssm_oracle_state_update(batch, Dm, N, _ptr(st), _ptr(x), _ptr(delta), _ptr(A),
+                                              _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y))
+        if rc != 0:
+            raise RuntimeError("ssm_oracle_state_update rejected its arguments")
+        return y, st
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def selective_scan_fwd(*args, **kwargs):
+    return default().selective_scan_fwd(*args, **kwargs)
+
+
+def state_update(*args, **kwargs):
+    return default().state_update(*args, **kwargs)

@@ -1,0 +1,199 @@
+/*
+ * ssm_oracle.c -- the fp64 sequential oracle declared in ssm_oracle.h.
+ *
+ * TEST INFRASTRUCTURE ONLY (tests, smoke check, CPU-baseline leg of the bench).
+ * Written from the definition, step by step in the pages' order, with no blocking,
+ * fusion or reordering: one (batch, channel) recurrence at a time, t ascending,
+ * states n ascending. Threads only split independent (batch, channel) recurrences.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -o libssm_oracle.so ssm_oracle.c -lm -lpthread
+ *
+ * SSM_ORACLE_PLANT=k (compile-time, tests only) plants one deliberate mistake so the
+ * pin tests can show that each kind of mistake is caught; the default build plants none.
+ */
+#include "ssm_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <unistd.h>
+
+#ifndef SSM_ORACLE_PLANT
+#define SSM_ORACLE_PLANT 0
+#endif
+
+/* Softplus: log(1 + exp(r)), the positivity map for the step size ("Mamba and State
+ * Space Models", "Discretization and initialization details"). Written in the
+ * overflow-free form; both branches equal log(1 + exp(r)) exactly in real arithmetic. */
+double ssm_oracle_softplus(double r) {
+  if (r > 0.0) return r + log1p(exp(-r));
+  return log1p(exp(r));
+}
+
+/* SiLU / swish gate z * sigmoid(z) ("8.7 State Space Models (Mamba)", section 6;
+ * "Mamba and State Space Models", "The Mamba Block": multiply by SiLU of the z branch). */
+double ssm_oracle_silu(double z) {
+#if SSM_ORACLE_PLANT == 5
+  return 1.0 / (1.0 + exp(-z)); /* planted: sigmoid instead of SiLU */
+#else
+  return z / (1.0 + exp(-z));
+#endif
+}
+
+typedef struct {
+  int64_t batch, L, D, N;
+  const double *u, *delta, *A, *B, *C, *Dskip, *z, *delta_bias, *h0;
+  int delta_softplus;
+  double *y, *last_state;
+  int64_t ch_begin, ch_end; /* flattened channel range b*D + d */
+} fwd_job_t;
+
+/* One channel's recurrence, exactly the sequential definition:
+ *   "Mamba and State Space Models", "Selective scan pseudo-code" (loop over t:
+ *   dA = exp(delta*A); dB = delta*B; h = dA*h + dB*x; y = sum_n h*C), plus the
+ *   D skip of the continuous form y = Cx + Du ("Arch 02: Mamba SSM") and the
+ *   SiLU(z) output gate ("8.7 State Space Models (Mamba)", section 6). */
+static void fwd_channel(const fwd_job_t* j, int64_t b, int64_t d, double* h) {
+  const int64_t L = j->L, D = j->D, N = j->N;
+  for (int64_t n = 0; n < N; ++n) h[n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0; /* h(0) = 0 */
+  for (int64_t t = 0; t < L; ++t) {
+    const int64_t ix = (b * L + t) * D + d;  /* (batch, L, D) */
+    const int64_t ixn = (b * L + t) * N;     /* (batch, L, N) */
+    double r = j->delta[ix];
+#if SSM_ORACLE_PLANT == 4
+    double dt = j->delta_softplus ? ssm_oracle_softplus(r) : r; /* planted: bias after softplus */
+    if (j->delta_bias) dt += j->delta_bias[d];
+#else
+    if (j->delta_bias) r += j->delta_bias[d];
+#if SSM_ORACLE_PLANT == 9
+    double dt = r; /* planted: softplus skipped */
+#else
+    double dt = j->delta_softplus ? ssm_oracle_softplus(r) : r;
+#endif
+#endif
+    const double x = j->u[ix];
+    double acc = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+#if SSM_ORACLE_PLANT == 8
+      const double An = j->A[n * D + d]; /* planted: A indexed (n, d) instead of (d, n) */
+#else
+      const double An = j->A[d * N + n];
+#endif
+#if SSM_ORACLE_PLANT == 2
+      const double dA = exp(-dt * An);              /* planted: wrong sign in the exponent */
+#else
+      const double dA = exp(dt * An);               /* A-bar = exp(Delta * A) */
+#endif
+#if SSM_ORACLE_PLANT == 6
+      const double dB = j->B[ixn + n];              /* planted: B-bar = B (Delta dropped) */
+#elif SSM_ORACLE_PLANT == 3
+      const double dB = dt * j->C[ixn + n];         /* planted: B and C swapped */
+#else
+      const double dB = dt * j->B[ixn + n];         /* B-bar = Delta * B */
+#endif
+#if SSM_ORACLE_PLANT == 7
+      acc += j->C[ixn + n] * h[n];                  /* planted: read out before the update */
+      h[n] = dA * h[n] + dB * x;
+#elif SSM_ORACLE_PLANT == 3
+      h[n] = dA * h[n] + dB * x;
+      acc += j->B[ixn + n] * h[n];
+#else
+      h[n] = dA * h[n] + dB * x;                    /* h_t = A-bar h_{t-1} + B-bar u_t */
+      acc += j->C[ixn + n] * h[n];                  /* y_t = C_t . h_t */
+#endif
+    }
+#if SSM_ORACLE_PLANT == 1
+    double v = acc;                                 /* planted: D skip dropped */
+#else
+    double v = acc + (j->Dskip ? j->Dskip[d] * x : 0.0);
+#endif
+    j->y[ix] = j->z ? v * ssm_oracle_silu(j->z[ix]) : v;
+  }
+  if (j->last_state)
+    for (int64_t n = 0; n < N; ++n) j->last_state[(b * D + d) * N + n] = h[n];
+}
+
+static void* fwd_worker(void* arg) {
+  const fwd_job_t* j = (const fwd_job_t*)arg;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+  if (!h) return (void*)1;
+  for (int64_t c = j->ch_begin; c < j->ch_end; ++c) fwd_channel(j, c / j->D, c % j->D, h);
+  free(h);
+  return NULL;
+}
+
+static int resolve_threads(int nthreads, int64_t work) {
+  if (nthreads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = n > 0 ? (int)n : 1;
+  }
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > work) nthreads = work > 0 ? (int)work : 1;
+  return nthreads;
+}
+
+int ssm_oracle_fwd(int64_t batch, int64_t L, int64_t D, int64_t N,
+                   const double* u, const double* delta, const double* A,
+                   const double* B, const double* C, const double* Dskip,
+                   const double* z, const double* delta_bias, int delta_softplus,
+                   const double* h0, double* y, double* last_state, int nthreads) {
+  if (batch < 0 || L < 0 || D < 0 || N <= 0) return -1;
+  const int64_t nch = batch * D;
+  if (nch == 0) return 0;
+  if ((L > 0 && (!u || !delta || !B || !C || !y)) || !A) return -1;
+  fwd_job_t base = {batch, L, D, N, u, delta, A, B, C, Dskip, z, delta_bias, h0,
+                    delta_softplus, y, last_state, 0, 0};
+  int nt = resolve_threads(nthreads, nch);
+  if (nt == 1) {
+    base.ch_begin = 0;
+    base.ch_end = nch;
+    return fwd_worker(&base) ? -1 : 0;
+  }
+  pthread_t tid[256];
+  fwd_job_t jobs[256];
+  int started = 0, rc = 0;
+  for (int i = 0; i < nt; ++i) {
+    jobs[i] = base;
+    jobs[i].ch_begin = nch * i / nt;
+    jobs[i].ch_end = nch * (i + 1) / nt;
+    if (pthread_create(&tid[i], NULL, fwd_worker, &jobs[i]) != 0) {
+      rc = -1;
+      break;
+    }
+    ++started;
+  }
+  for (int i = 0; i < started; ++i) {
+    void* ret = NULL;
+    pthread_join(tid[i], &ret);
+    if (ret) rc = -1;
+  }
+  return rc;
+}
+
+/* One recurrent step per (batch, channel): the O(1)-per-token inference update
+ * ("8.7 State Space Models (Mamba)", section 5; "Mamba and State Space Models",
+ * "Selective scan pseudo-code" body for a single t), continuing from a given state. */
+int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* Dskip,
+                            const double* z, double* y) {
+  if (batch < 0 || D < 0 || N <= 0) return -1;
+  if (batch * D == 0) return 0;
+  if (!state || !x || !delta || !A || !B || !C || !y) return -1;
+  for (int64_t b = 0; b < batch; ++b) {
+    for (int64_t d = 0; d < D; ++d) {
+      const double dt = delta[b * D + d];
+      const double xv = x[b * D + d];
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) {
+        double* s = &state[(b * D + d) * N + n];
+        const double dA = exp(dt * A[d * N + n]);
+        *s = dA * (*s) + dt * B[b * N + n] * xv;
+        acc += C[b * N + n] * (*s);
+      }
+      double v = acc + (Dskip ? Dskip[d] * xv : 0.0);
+      y[b * D + d] = z ? v * ssm_oracle_silu(z[b * D + d]) : v;
+    }
+  }
+  return 0;
+}

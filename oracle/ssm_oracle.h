@@ -1,0 +1,74 @@
+/*
+ * ssm_oracle.h -- plain, slow, sequential fp64 CPU oracle for the Mamba selective
+ * scan (forward) and the single-token recurrent state update.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link, load or
+ * call this code: only the tests, the smoke check and the bench's CPU-baseline leg
+ * use it. It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (all arrays fp64, dense, row-major, channel index fastest):
+ *
+ *   for every batch row b and channel d, starting from h = h0 (or 0):
+ *     for t = 0 .. L-1:
+ *       r     = delta[b,t,d] + delta_bias[d]                  (bias 0 if absent)
+ *       dt    = delta_softplus ? log(1 + exp(r)) : r
+ *       for n: h[n] = exp(dt * A[d,n]) * h[n] + dt * B[b,t,n] * u[b,t,d]
+ *       v     = sum_n C[b,t,n] * h[n] + Dskip[d] * u[b,t,d]   (skip 0 if absent)
+ *       y     = z present ? v * z / (1 + exp(-z[b,t,d])) : v
+ *     last_state[b,d,:] = h
+ *
+ * Sources (page title, section):
+ *  - "Mamba and State Space Models" (vanos001 placement-prep chapter), section
+ *    "Selective scan pseudo-code": the sequential loop over t with
+ *    dA = exp(delta*A), dB = delta*B, h = dA*h + dB*x, y = (h*C).sum over N.
+ *  - same chapter, "Discretization and initialization details": A-bar = exp(Delta*A)
+ *    with B-bar simplified to Delta*B; Delta = softplus(W x + b_Delta), the bias
+ *    added before the softplus.
+ *  - "Arch 02: Mamba SSM" deck, continuous form y = Cx + Du (the D skip) and the
+ *    selective-SSM block (B, C per token (B,L,N); Delta per token and channel).
+ *  - "8.7 State Space Models (Mamba)", section 6 "The block": the SSM output is
+ *    multiplied elementwise by SiLU of the other half (the z gate); section 2.1: h(0)=0.
+ *  - "Mamba and State Space Models", "Common Pitfalls": the state after a prefix is
+ *    reusable (h0 argument / last_state output; decode continues from it).
+ */
+#ifndef SSM_ORACLE_H
+#define SSM_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Softplus in a numerically stable form: r + log1p(exp(-r)) for r > 0, else log1p(exp(r)). */
+double ssm_oracle_softplus(double r);
+/* SiLU (swish): z * sigmoid(z) = z / (1 + exp(-z)). */
+double ssm_oracle_silu(double z);
+
+/*
+ * Forward selective scan.
+ *   u, delta, z, y : (batch, L, D)      B, C : (batch, L, N)
+ *   A : (D, N)     Dskip, delta_bias : (D)     h0, last_state : (batch, D, N)
+ * Nullable: Dskip, z, delta_bias, h0, last_state. y must not alias an input.
+ * nthreads <= 0 uses every online CPU. Returns 0 on success, -1 on bad arguments.
+ */
+int ssm_oracle_fwd(int64_t batch, int64_t L, int64_t D, int64_t N,
+                   const double* u, const double* delta, const double* A,
+                   const double* B, const double* C, const double* Dskip,
+                   const double* z, const double* delta_bias, int delta_softplus,
+                   const double* h0, double* y, double* last_state, int nthreads);
+
+/*
+ * One recurrent decode step, in place on state (batch, D, N):
+ *   x, delta, z, y : (batch, D)   B, C : (batch, N)   A : (D, N)   Dskip : (D)
+ * delta is the final step size (no bias, no softplus). Nullable: Dskip, z.
+ * Returns 0 on success, -1 on bad arguments.
+ */
+int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* Dskip,
+                            const double* z, double* y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

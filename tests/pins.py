@@ -1,0 +1,282 @@
+"""Pins for the fp64 oracle: checks against facts the pages and the mathematics fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError if the oracle
+disagrees. None of them re-types the oracle's loop: each uses a different route to
+the same number (a printed worked example, a closed form, a convolution, explicit
+products, a limit, an invariant). ``test_oracle_pins.py`` runs them on the real
+oracle; ``test_oracle_mutants.py`` runs them on builds with one planted mistake each
+and requires every mutant to fail at least one pin.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+from scipy.special import expit
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _silu(z):
+    return z * expit(z)
+
+
+def _softplus(r):
+    return np.logaddexp(0.0, r)
+
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    scale = max(np.max(np.abs(b)), 1e-300)
+    return float(np.max(np.abs(a - b)) / scale)
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            vals[k] = [float(x) for x in v]
+    return vals
+
+
+def pin_worked_example(o):
+    """'Mamba and State Space Models', 'A worked numerical pass': A = -1, step sizes
+    0.1, 5.0, 0.1 give A-bar 0.905, 0.007, 0.905, and token 2 dominates the state."""
+    g = _read_golden("worked_example.txt")
+    A = np.array([[g["A"][0]]])
+    delta = np.array(g["delta"]).reshape(1, 3, 1)
+    # Decay only: start from h0 = 1 with zero input, so y_t = prod_{s<=t} A-bar_s.
+    y, _ = o.selective_scan_fwd(np.zeros((1, 3, 1)), delta, A, np.ones((1, 3, 1)), np.ones((1, 3, 1)),
+                                delta_softplus=False, h0=np.ones((1, 1, 1)))
+    y = y.ravel()
+    abar = [y[0], y[1] / y[0], y[2] / y[1]]
+    assert [round(a, 3) for a in abar] == g["abar"], abar
+    # Write-dominance: unit inputs at every token; token 2's share of h_3 exceeds 90%.
+    y1, _ = o.selective_scan_fwd(np.ones((1, 3, 1)), delta, A, np.ones((1, 3, 1)), np.ones((1, 3, 1)),
+                                 delta_softplus=False)
+    share2 = abar[2] * g["delta"][1] / y1.ravel()[2]
+    assert share2 > 0.9, share2
+
+
+def pin_lti_convolution(o, seed=1):
+    """Constant delta, B, C: y = K * u + D u with K_j = sum_n C_n exp(j dt A_n) dt B_n
+    ("Arch 02: Mamba SSM" kernel K = (C B-bar, C A-bar B-bar, ...); "State Space Model
+    (SSM)" glossary; "8.7 State Space Models (Mamba)" section 2.1), by brute force."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 2, 37, 3, 5
+    raw = rng.normal(-1.0, 0.7, (b, 1, D))
+    bias = rng.normal(0.0, 0.3, D)
+    A = -rng.uniform(0.2, 3.0, (D, N))
+    B0 = rng.standard_normal((b, 1, N))
+    C0 = rng.standard_normal((b, 1, N))
+    u = rng.standard_normal((b, L, D))
+    z = rng.standard_normal((b, L, D))
+    Dk = rng.standard_normal(D)
+    y, _ = o.selective_scan_fwd(u, np.repeat(raw, L, 1), A, np.repeat(B0, L, 1), np.repeat(C0, L, 1),
+                                D=Dk, z=z, delta_bias=bias, delta_softplus=True)
+    ref = np.zeros_like(y)
+    for bi in range(b):
+        for d in range(D):
+            dt = _softplus(raw[bi, 0, d] + bias[d])
+            j = np.arange(L)[:, None]
+            K = (C0[bi, 0] * np.exp(j * dt * A[d]) * dt * B0[bi, 0]).sum(-1)  # (L,)
+            for t in range(L):
+                conv = np.dot(K[: t + 1][::-1], u[bi, : t + 1, d])
+                ref[bi, t, d] = (conv + Dk[d] * u[bi, t, d]) * _silu(z[bi, t, d])
+    assert _rel(y, ref) < 1e-11, _rel(y, ref)
+
+
+def pin_delta_zero_holds_state(o, seed=2):
+    """Delta -> 0 leaves the state untouched ("Arch 02: Mamba SSM": small Delta ~ pure
+    copy; "Mamba and State Space Models": small Delta leaves the state untouched)."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 2, 9, 4, 8
+    u = rng.standard_normal((b, L, D))
+    z = rng.standard_normal((b, L, D))
+    Dk = rng.standard_normal(D)
+    A = -rng.uniform(0.5, 8, (D, N))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    h0 = rng.standard_normal((b, D, N))
+    y, last = o.selective_scan_fwd(u, np.zeros((b, L, D)), A, B, C, D=Dk, z=z, delta_softplus=False, h0=h0)
+    assert np.array_equal(last, h0)
+    ref = np.einsum("bln,bdn->bld", C, h0) + Dk * u
+    assert _rel(y, ref * _silu(z)) < 1e-13
+    y0, last0 = o.selective_scan_fwd(u, np.zeros((b, L, D)), A, B, C, D=Dk, z=z, delta_softplus=False)
+    assert np.all(last0 == 0.0)
+    assert _rel(y0, Dk * u * _silu(z)) < 1e-14
+    ys, st = o.state_update(h0, u[:, 0], np.zeros((b, D)), A, B[:, 0], C[:, 0], D=Dk, z=z[:, 0])
+    assert np.array_equal(st, h0)
+
+
+def pin_scalar_closed_form(o):
+    """Constant input to a single active state: h_t = b (1 - a^t) / (1 - a), the
+    geometric sum of the recurrence h_t = a h_{t-1} + b ("Arch 02: Mamba SSM")."""
+    L, D, N = 50, 3, 4
+    A = -np.array([[0.7, 2, 3, 4], [1.3, 2, 3, 4], [0.05, 1, 1, 1]])
+    dts = np.array([0.3, 0.11, 0.9])
+    u0, B0, C0 = 1.7, -0.6, 1.9
+    Dk = np.array([0.5, -1.0, 2.0])
+    Bm = np.zeros((1, L, N))
+    Bm[..., 0] = B0
+    Cm = np.full((1, L, N), 5.0)  # C on the inactive states multiplies zeros
+    Cm[..., 0] = C0
+    y, last = o.selective_scan_fwd(np.full((1, L, D), u0), np.broadcast_to(dts, (1, L, D)), A, Bm, Cm,
+                                   D=Dk, delta_softplus=False)
+    t = np.arange(1, L + 1)[:, None]
+    a = np.exp(dts * A[:, 0])
+    bb = dts * B0 * u0
+    h = bb * (1 - a ** t) / (1 - a)
+    assert _rel(y[0], C0 * h + Dk * u0) < 1e-12
+    assert _rel(last[0, :, 0], h[-1]) < 1e-12
+    assert np.all(last[0, :, 1:] == 0.0)
+
+
+def pin_bruteforce_unrolling(o, seed=3):
+    """Tiny L: h_t = sum_{s<=t} (prod_{r=s+1..t} A-bar_r) B-bar_s u_s with explicit
+    products ("Arch 02: Mamba SSM" recurrence; "8.7 State Space Models (Mamba)" 2.1)."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 2, 6, 3, 4
+    u = rng.standard_normal((b, L, D))
+    raw = rng.normal(-1, 1, (b, L, D))
+    bias = rng.normal(0, 0.5, D)
+    z = rng.standard_normal((b, L, D))
+    A = -rng.uniform(0.1, 4, (D, N))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    Dk = rng.standard_normal(D)
+    y, last = o.selective_scan_fwd(u, raw, A, B, C, D=Dk, z=z, delta_bias=bias, delta_softplus=True)
+    ref = np.zeros((b, L, D))
+    hL = np.zeros((b, D, N))
+    for bi in range(b):
+        for d in range(D):
+            dt = _softplus(raw[bi, :, d] + bias[d])
+            for t in range(L):
+                h = np.zeros(N)
+                for s in range(t + 1):
+                    prod = np.ones(N)
+                    for r in range(s + 1, t + 1):
+                        prod = prod * np.exp(dt[r] * A[d])
+                    h += prod * dt[s] * B[bi, s] * u[bi, s, d]
+                ref[bi, t, d] = (np.dot(C[bi, t], h) + Dk[d] * u[bi, t, d]) * _silu(z[bi, t, d])
+                if t == L - 1:
+                    hL[bi, d] = h
+    assert _rel(y, ref) < 1e-12, _rel(y, ref)
+    assert _rel(last, hL) < 1e-12
+
+
+def pin_large_delta_reset(o, seed=4):
+    """Large Delta replaces the state by the current write ("Arch 02: Mamba SSM": large
+    Delta ~ full state replacement; "Mamba and State Space Models", worked pass)."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 1, 7, 3, 4
+    u = rng.standard_normal((b, L, D))
+    A = -rng.uniform(1, 3, (D, N))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    big = 50.0
+    y, last = o.selective_scan_fwd(u, np.full((b, L, D), big), A, B, C, delta_softplus=False)
+    h = big * B[:, :, None, :] * u[:, :, :, None]  # (b, L, D, N)
+    ref = np.einsum("bln,bldn->bld", C, h)
+    assert _rel(y, ref) < 1e-15 + 1e-20
+    assert _rel(last, h[:, -1]) < 1e-15
+
+
+def pin_stability_bound(o, seed=5):
+    """Delta > 0 and A < 0 give 0 < A-bar < 1 and a bounded state:
+    |h_t[n]| <= max|B-bar u| / (1 - max A-bar) ("Mamba and State Space Models",
+    "Discretization and initialization details": exp(Delta A) in (0,1), stable)."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 1, 40, 3, 4
+    u = rng.standard_normal((b, L, D)) * 3
+    raw = rng.normal(-1, 1, (b, L, D))
+    A = -rng.uniform(0.3, 2, (D, N))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    dt = _softplus(raw)
+    abar = np.exp(dt[..., None] * A[None, None])           # (b, L, D, N)
+    assert np.all((abar > 0) & (abar < 1))
+    bmax = np.max(np.abs(dt[..., None] * B[:, :, None, :] * u[..., None]), axis=1)  # (b, D, N)
+    bound = bmax / (1 - np.max(abar, axis=1))
+    for Lp in range(1, L + 1):
+        _, last = o.selective_scan_fwd(u[:, :Lp], raw[:, :Lp], A, B[:, :Lp], C[:, :Lp], delta_softplus=True)
+        assert np.all(np.abs(last) <= bound * (1 + 1e-12))
+
+
+def pin_decode_matches_forward(o, seed=6):
+    """T single-token updates from zero == forward over T steps; and the state after a
+    prefix continues the sequence ("Mamba and State Space Models", "Common Pitfalls":
+    the state after a shared prefix is reusable; "8.7 State Space Models (Mamba)" s.5)."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 2, 12, 3, 8
+    u = rng.standard_normal((b, L, D))
+    dt = _softplus(rng.standard_normal((b, L, D)))
+    z = rng.standard_normal((b, L, D))
+    A = -rng.uniform(0.1, 4, (D, N))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    Dk = rng.standard_normal(D)
+    y, last = o.selective_scan_fwd(u, dt, A, B, C, D=Dk, z=z, delta_softplus=False)
+    st = np.zeros((b, D, N))
+    for t in range(L):
+        yt, st = o.state_update(st, u[:, t], dt[:, t], A, B[:, t], C[:, t], D=Dk, z=z[:, t])
+        assert _rel(yt, y[:, t]) < 1e-14
+    assert _rel(st, last) < 1e-14
+    P = 5
+    _, mid = o.selective_scan_fwd(u[:, :P], dt[:, :P], A, B[:, :P], C[:, :P], D=Dk, z=z[:, :P],
+                                  delta_softplus=False)
+    y2, last2 = o.selective_scan_fwd(u[:, P:], dt[:, P:], A, B[:, P:], C[:, P:], D=Dk, z=z[:, P:],
+                                     delta_softplus=False, h0=mid)
+    assert _rel(y2, y[:, P:]) < 1e-14 and _rel(last2, last) < 1e-14
+
+
+def pin_softplus_silu(o):
+    """Softplus = log(1 + e^r) and SiLU = z sigmoid(z), against library routines and
+    exact values (softplus(0) = ln 2; silu(0) = 0)."""
+    assert abs(o.softplus(0.0) - np.log(2.0)) < 1e-16
+    for r in np.linspace(-60, 60, 241):
+        ref = _softplus(r)
+        assert abs(o.softplus(r) - ref) <= 1e-15 * max(abs(ref), 1e-300), r
+    assert o.silu(0.0) == 0.0
+    for zz in np.linspace(-40, 40, 161):
+        ref = _silu(zz)
+        assert abs(o.silu(zz) - ref) <= 1e-15 * max(abs(ref), 1e-300) + 1e-300, zz
+
+
+def combine(p, q):
+    """The scan operator on (a, b) pairs: applying (a1, b1) then (a2, b2) to a state h
+    gives a2 (a1 h + b1) + b2 = (a1 a2) h + (a2 b1 + b2)."""
+    return p[0] * q[0], q[0] * p[1] + q[1]
+
+
+def pin_scan_operator(o, seed=7):
+    """The recurrence h_t = a_t h_{t-1} + b_t is a fold of an associative operator
+    ("8.7 State Space Models (Mamba)", section 4.1; "Mamba and State Space Models",
+    "Hardware-Aware Parallel Scan"), and the fold reproduces the oracle's state."""
+    rng = np.random.default_rng(seed)
+    for _ in range(200):
+        p, q, r = [(rng.uniform(0, 1), rng.standard_normal()) for _ in range(3)]
+        lhs = combine(combine(p, q), r)
+        rhs = combine(p, combine(q, r))
+        assert abs(lhs[0] - rhs[0]) <= 1e-15 and abs(lhs[1] - rhs[1]) <= 1e-14 * (1 + abs(lhs[1]))
+    L, N = 33, 4
+    u = rng.standard_normal((1, L, 1))
+    dt = _softplus(rng.standard_normal((1, L, 1)))
+    A = -rng.uniform(0.1, 2, (1, N))
+    B = rng.standard_normal((1, L, N))
+    C = rng.standard_normal((1, L, N))
+    _, last = o.selective_scan_fwd(u, dt, A, B, C, delta_softplus=False)
+    acc = (np.ones(N), np.zeros(N))
+    for t in range(L):
+        acc = combine(acc, (np.exp(dt[0, t, 0] * A[0]), dt[0, t, 0] * B[0, t] * u[0, t, 0]))
+    assert _rel(last[0, 0], acc[1]) < 1e-13
+
+
+ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_delta_zero_holds_state, pin_scalar_closed_form,
+            pin_bruteforce_unrolling, pin_large_delta_reset, pin_stability_bound, pin_decode_matches_forward,
+            pin_softplus_silu, pin_scan_operator]
