@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused selective-scan forward pass on one B300 (plus the decode step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one fused forward pass (discretise, recurrence, read-out, D skip, SiLU gate,
+last_state) over the Mamba-1.4B-shaped layer workload: batch 4, L 4096, D 4096, N 16,
+bf16 I/O, fp32 state. Inputs (539 MB) are larger than L2 (126 MB), so no flush is
+needed between steps. Prints one JSON line (rank 0).
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
+workload shards by batch/channel with no exchange; replicas give weak scaling).
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"] if os.path.exists(
+    os.path.join(ROOT, "BASELINE.json")) else "selective-scan fwd GB/s & elem/s (B·L·D) on 1 B300; % of roofline"
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "sm_max_mhz": 2032.0, "source": "fallback"}
+SM_COUNT = 148
+EX2_PER_CLK_SM = 32       # measured on B300: MUFU.EX2 32 lanes/clk/SM
+FP32_PER_CLK_SM = 128     # FFMA lanes/clk/SM
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def alu_peak_elem_steps(sm_mhz, sms=SM_COUNT):
+    """Element-steps/s at the ALU roofline: one ex2 (32/clk/SM) and 4 fp32 ops
+    (128/clk/SM) per (b, t, d, n): both pipes give the same bound on B300."""
+    return min(sms * EX2_PER_CLK_SM, sms * FP32_PER_CLK_SM / 4) * sm_mhz * 1e6
+
+
+# ---- clocks ------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        which = "timed region"
+        if len(inside) < 3:  # short timed region: fall back to all samples under this run
+            inside = [p for (t, p) in self.samples]
+            which = "whole run (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        reasons = set()
+        for p in inside:
+            for name, v in zip(self.NAMES, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][2]),
+                "reasons": sorted(reasons), "samples": len(inside), "sampled_over": which,
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+# ---- distributed plumbing (replicas; timing barrier and max only) -------------------------
+def dist_init():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- CPU oracle timing -----------------------------------------------------------------
+def oracle_sample(w, seconds, seed=0):
+    """Time the oracle on whole-sequence channels of batch row 0, sized to ~``seconds``.
+    Returns (elements (B*L*D units) processed, wall seconds, channels, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from selective_state_space_141_b300 import inputs
+
+    threads = os.cpu_count() or 1
+    g = torch.Generator().manual_seed(seed)
+    L, N = w.L, w.N
+
+    def make(k):
+        io = w.dtype
+        return dict(u=torch.randn(1, L, k, generator=g).to(io), delta=(torch.randn(1, L, k, generator=g) * 0.5 - 2).to(io),
+                    z=torch.randn(1, L, k, generator=g).to(io), B=torch.randn(1, L, N, generator=g).to(io),
+                    C=torch.randn(1, L, N, generator=g).to(io), D=torch.randn(k, generator=g),
+                    delta_bias=(torch.rand(k, generator=g) * (inputs.BIAS_HI - inputs.BIAS_LO) + inputs.BIAS_LO)
+                    if w.has_bias else None, A=inputs.s4d_real_A(k, N))
+
+    def run(d):
+        arr = {k: (v.double().numpy() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        t0 = time.perf_counter()
+        oracle.selective_scan_fwd(arr["u"], arr["delta"], arr["A"], arr["B"], arr["C"], D=arr["D"], z=arr["z"],
+                                  delta_bias=arr["delta_bias"], delta_softplus=True, nthreads=threads)
+        return time.perf_counter() - t0
+
+    k0 = min(w.D * w.batch, threads * 32)
+    t_cal = run(make(k0))
+    k = int(max(k0, min(w.D * w.batch, k0 * seconds / max(t_cal, 1e-3))))
+    k = max(threads, (k // threads) * threads)
+    t = run(make(k))
+    return k * L, t, k, threads
+
+
+def cpu_baseline_obj(w, seconds):
+    elems, t, k, threads = oracle_sample(w, seconds)
+    frac = elems / w.elems
+    gbs = w.compulsory_bytes() * frac / t / 1e9
+    return {"value": gbs, "unit": "GB/s", "elem_per_s": elems / t, "cores": threads, "kind": "oracle",
+            "sample": f"{k} whole-sequence channels (L={w.L}, N={w.N}) of batch row 0, fp64, "
+                      f"{threads} threads, {t:.1f} s; GB/s scaled by the sample's share of compulsory bytes"}
+
+
+# ---- the reference arm: the oracle as it stands -------------------------------------------
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step)
+    times, elems = [], 0
+    ks = []
+    for _ in range(args.steps):
+        e, t, k, threads = oracle_sample(w, per_step)
+        times.append(t)
+        elems += e
+        ks.append(k)
+    total = sum(times)
+    frac = elems / w.elems
+    gbs = w.compulsory_bytes() * frac / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N, "io": "bf16",
+                       "sample_per_step": f"~{statistics.median(ks)} whole-sequence channels"},
+            "elem_per_s": elems / total,
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: whole-sequence channels of one batch row, ~{per_step:.1f} s"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm --------------------------------------------------------------------------
+def run_ours(args, w, ws, rank, local):
+    import torch
+
+    from selective_state_space_141_b300 import inputs, ssm
+
+    ssm.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    peaks = load_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2032.0))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alu_peak = alu_peak_elem_steps(sm_max, props.multi_processor_count)
+
+    d = inputs.fwd_inputs(w, dev)
+    y = torch.empty_like(d["u"])
+    last = torch.empty(w.batch, w.D, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                               delta_bias=d["delta_bias"], delta_softplus=True, y=y, last_state=last,
+                               stream=stream)
+
+    uid = str(getattr(props, "uuid", ""))
+    gpu_id = (uid if uid.startswith("GPU-") else "GPU-" + uid) if uid else str(local)
+    sampler = ClockSampler(gpu_id)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    h0 = time.time()
+    e0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    barrier(ws)
+    total_ms = e0.elapsed_time(e1)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    total_ms = max_over_ranks(total_ms, ws)
+    if ssm.device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    # the clocks are read over the timed region; extend briefly so short runs still get samples
+    if h1 - h0 < 0.5:
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            step()
+        torch.cuda.synchronize()
+        h1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(h0, h1)
+
+    sec = total_ms / 1e3
+    gbs = ws * K * w.compulsory_bytes() / sec / 1e9
+    elem_s = ws * K * w.elems / sec
+    achieved = w.element_steps / (launch_ms / 1e3)
+    result = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N, "io": "bf16",
+                   "state": "fp32", "l2": "inputs (539 MB) larger than L2 (126 MB); no flush between steps",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "elem_per_s": elem_s,
+        "roofline": {
+            "bound": "alu", "achieved": achieved / 1e12, "peak": alu_peak / 1e12,
+            "unit": "T element-steps/s (1 ex2 + 4 fp32 ops each)", "frac": achieved / alu_peak,
+            "traffic": args.traffic,
+            "peak_basis": f"{props.multi_processor_count} SMs x 32 ex2/clk (= 128 fp32 lanes / 4 ops) x "
+                          f"{sm_max:.0f} MHz max SM clock",
+            "launch_ms": launch_ms,
+            "hbm": {"achieved_gbs": w.compulsory_bytes() / (launch_ms / 1e3) / 1e9, "peak_gbs": hbm_peak,
+                    "frac": w.compulsory_bytes() / (launch_ms / 1e3) / 1e9 / hbm_peak,
+                    "peak_source": peaks.get("source")},
+        },
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        result["e2e"] = e2e(w, d, args, ssm, torch, stream)
+    if not args.no_decode:
+        result["decode"] = decode_bench(args, ssm, torch, inputs, dev, hbm_peak)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def e2e(w, d, args, ssm, torch, stream):
+    """Same metric through the public call with HOST inputs: every step copies the
+    inputs from pinned host memory, runs the scan and copies y + last_state back."""
+    names = [k for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias") if d.get(k) is not None]
+    host = {k: d[k].cpu().pin_memory() for k in names}
+    dev_in = {k: torch.empty_like(d[k]) for k in names}
+    y_h = torch.empty(d["u"].shape, dtype=d["u"].dtype).pin_memory()
+    last_h = torch.empty(w.batch, w.D, w.N, dtype=torch.float32).pin_memory()
+    y = torch.empty_like(d["u"])
+    last = torch.empty(w.batch, w.D, w.N, dtype=torch.float32, device=d["u"].device)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = y_h.numel() * y_h.element_size() + last_h.numel() * 4
+
+    def step():
+        for k in names:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        ssm.selective_scan_fwd(dev_in["u"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"],
+                               D=dev_in.get("D"), z=dev_in.get("z"), delta_bias=dev_in.get("delta_bias"), y=y,
+                               last_state=last, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        last_h.copy_(last, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, args.e2e_steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    return {"value": w.compulsory_bytes() / sec / 1e9, "unit": "GB/s", "ms_per_step": sec * 1e3,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def decode_bench(args, ssm, torch, inputs, dev, hbm_peak):
+    """The decode workload: 1024 single-token steps captured in one CUDA graph."""
+    w = inputs.DECODE
+    T = args.decode_steps
+    d = inputs.decode_inputs(w, dev, steps=T)
+    ys = torch.empty(T, w.batch, w.D, dtype=w.dtype, device=dev)
+    state = d["state"]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        for t in range(2):
+            ssm.state_update(state, d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t], D=d["D"], z=d["z"][t],
+                             y=ys[t])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(T):
+            ssm.state_update(state, d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t], D=d["D"], z=d["z"][t],
+                             y=ys[t])
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if ssm.device_error() != 0:
+        raise RuntimeError("device error word set during decode")
+    per_step = e0.elapsed_time(e1) / 1e3 / (reps * T)
+    bps = w.bytes_per_step()
+    return {"workload": w.name, "us_per_step": per_step * 1e6, "GB/s": bps / per_step / 1e9,
+            "hbm_frac": bps / per_step / 1e9 / hbm_peak, "bytes_per_step": bps, "steps_per_graph": T,
+            "elem_per_s": w.batch * w.D / per_step,
+            "note": "state (84 MB) fits in L2 (126 MB) across steps; GB/s counts compulsory bytes per step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="m1p4b")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from selective_state_space_141_b300 import inputs
+    w = inputs.FWD_WORKLOADS[args.workload]
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, w, ws, rank)
+    else:
+        run_ours(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

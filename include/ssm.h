@@ -16,7 +16,9 @@
  *  - Errors: all arguments are validated on the host before anything is enqueued.
  *    Any status other than SSM_OK means nothing was launched and no output was
  *    written. A failed launch returns SSM_ERR_CUDA (from cudaGetLastError).
- *  - Pointers must be 16-byte aligned (a PyTorch allocation always is).
+ *  - Pointers must be aligned to their element size; ssm_state_update also needs
+ *    state and A 16-byte aligned. Faster kernel variants are chosen when every
+ *    pointer is 16-byte aligned (a fresh PyTorch allocation always is).
  *  - Outputs must not overlap any input (SSM_ERR_LAYOUT), except where an entry point
  *    says it updates a tensor in place.
  *  - Every I/O tensor (u, delta, z, B, C, x) of one call has the same element type,
@@ -30,6 +32,12 @@
 #define SSM_B300_H
 
 #include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -86,7 +94,7 @@ typedef enum {
  * batch == 0 or L == 0 is a valid no-op; with L == 0 a non-NULL last_state is zeroed.
  * The per-step state never reaches global memory.
  */
-ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+SSM_API ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta,
                                     const ssm_tensor_t* A, const ssm_tensor_t* B,
                                     const ssm_tensor_t* C, const ssm_tensor_t* D,
                                     const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
@@ -117,14 +125,14 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
  *   stream                cudaStream_t
  * batch == 0 is a valid no-op. Only state may alias itself; y must not overlap any input.
  */
-ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x,
+SSM_API ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x,
                               const ssm_tensor_t* delta, const ssm_tensor_t* A,
                               const ssm_tensor_t* B, const ssm_tensor_t* C,
                               const ssm_tensor_t* D, const ssm_tensor_t* z,
                               ssm_tensor_t* y, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* ssm_status_string(ssm_status_t status);
+SSM_API const char* ssm_status_string(ssm_status_t status);
 
 /*
  * ssm_device_error -- diagnostic read of the library's device-side error word on the
@@ -133,7 +141,7 @@ const char* ssm_status_string(ssm_status_t status);
  * SSM_ERR_NULL (code == NULL) or SSM_ERR_CUDA. Kernels never trap: a wait that runs out
  * sets this word and returns.
  */
-ssm_status_t ssm_device_error(void* stream, int32_t* code);
+SSM_API ssm_status_t ssm_device_error(void* stream, int32_t* code);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,145 @@
+// scan_fwd.cuh -- fused selective-scan forward kernels.
+//
+// Per (batch b, channel d), from h = 0, for t = 0 .. L-1:
+//   dt   = softplus(delta + bias)           (or delta + bias)
+//   h[n] = exp(dt * A[d,n]) * h[n] + dt * u * B[t,n]
+//   y    = (sum_n C[t,n] h[n] + D[d] u) * silu(z)
+// ("Mamba and State Space Models", "Selective scan pseudo-code" and
+//  "Discretization and initialization details"; "Arch 02: Mamba SSM", y = Cx + Du;
+//  "8.7 State Space Models (Mamba)", section 6, the SiLU(z) gate.)
+//
+// The state h lives in fp32 registers for the whole sequence and never reaches
+// global memory; only y and the final state are written ("Mamba and State Space
+// Models", "Hardware-Aware Parallel Scan": kernel fusion, no intermediate h in HBM).
+#pragma once
+
+#include "common.cuh"
+
+namespace ssm {
+
+struct FwdParams {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* Dskip;       // nullable
+  const void* z;            // nullable
+  const float* delta_bias;  // nullable
+  int delta_softplus;
+  void* y;
+  float* last_state;        // nullable
+  int64_t batch, L, D;
+};
+
+// ------------------------------------------------------------------------------------
+// Generic kernel: any D, any L, fp32 or bf16 I/O. Channel-parallel: a group of
+// LPC = N / SPL adjacent lanes owns one channel, SPL states each, and walks the
+// sequence in chunks of TC steps staged through shared memory:
+//   stage  : u, z, (dt, dt*u) per (t, d) and B, C per (t, n) -> smem (fp32)
+//   scan   : each lane updates its SPL states for every t, writes its partial C.h
+//   finish : y = sum of partials + D u, gated, stored
+// ------------------------------------------------------------------------------------
+template <typename T, typename TY, int N, int SPL, int DT, int TC>
+__global__ void __launch_bounds__(DT*(N / SPL))
+scan_fwd_generic(const FwdParams p) {
+  constexpr int LPC = N / SPL;
+  constexpr int NT = DT * LPC;
+  __shared__ float sU[TC][DT];
+  __shared__ float sZ[TC][DT];
+  __shared__ float2 sDD[TC][DT];
+  __shared__ float sB[TC][N];
+  __shared__ float sC[TC][N];
+  __shared__ float sP[TC][NT];
+
+  const int tid = threadIdx.x;
+  const int64_t b = blockIdx.y;
+  const int64_t L = p.L, D = p.D;
+  const int64_t d0 = (int64_t)blockIdx.x * DT;
+  const int j = tid / LPC, g = tid % LPC;
+  const int64_t dj = d0 + j;
+  const bool vj = dj < D;
+
+  const T* __restrict__ u = static_cast<const T*>(p.u) + b * L * D;
+  const T* __restrict__ dl = static_cast<const T*>(p.delta) + b * L * D;
+  const T* __restrict__ zp = p.z ? static_cast<const T*>(p.z) + b * L * D : nullptr;
+  const T* __restrict__ Bp = static_cast<const T*>(p.B) + b * L * N;
+  const T* __restrict__ Cp = static_cast<const T*>(p.C) + b * L * N;
+  TY* __restrict__ y = static_cast<TY*>(p.y) + b * L * D;
+
+  constexpr bool kAccurate = sizeof(T) == 4;  // fp32 I/O: near-correctly-rounded decay
+  float Av[SPL], A2[SPL], h[SPL];
+#pragma unroll
+  for (int k = 0; k < SPL; ++k) {
+    Av[k] = vj ? p.A[dj * N + g * SPL + k] : 0.f;
+    A2[k] = Av[k] * kLog2e;
+    h[k] = 0.f;
+  }
+
+  for (int64_t t0 = 0; t0 < L; t0 += TC) {
+    const int tc = (int)((L - t0) < TC ? (L - t0) : TC);
+    for (int i = tid; i < TC * DT; i += NT) {
+      const int t = i / DT, jj = i % DT;
+      const int64_t d = d0 + jj;
+      float uu = 0.f, zz = 0.f, dt = 0.f;
+      if (t < tc && d < D) {
+        const int64_t ix = (t0 + t) * D + d;
+        uu = to_f32(u[ix]);
+        float r = to_f32(dl[ix]);
+        if (p.delta_bias) r += p.delta_bias[d];
+        dt = p.delta_softplus ? softplus_precise(r) : r;
+        if (zp) zz = to_f32(zp[ix]);
+      }
+      sU[t][jj] = uu;
+      sZ[t][jj] = zz;
+      sDD[t][jj] = make_float2(dt, dt * uu);
+    }
+    for (int i = tid; i < TC * N; i += NT) {
+      const int t = i / N, n = i % N;
+      float bb = 0.f, cc = 0.f;
+      if (t < tc) {
+        const int64_t ix = (t0 + t) * N + n;
+        bb = to_f32(Bp[ix]);
+        cc = to_f32(Cp[ix]);
+      }
+      sB[t][n] = bb;
+      sC[t][n] = cc;
+    }
+    __syncthreads();
+
+    for (int t = 0; t < tc; ++t) {
+      const float2 dd = sDD[t][j];
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < SPL; ++k) {
+        const int n = g * SPL + k;
+        const float a = decay<kAccurate>(dd.x, Av[k], A2[k]);  // A-bar = exp(dt * A)
+        h[k] = fmaf(a, h[k], dd.y * sB[t][n]);             // h = A-bar h + (dt u) B
+        acc = fmaf(sC[t][n], h[k], acc);                   // C . h (this lane's states)
+      }
+      sP[t][tid] = acc;
+    }
+    __syncthreads();
+
+    for (int i = tid; i < TC * DT; i += NT) {
+      const int t = i / DT, jj = i % DT;
+      const int64_t d = d0 + jj;
+      if (t < tc && d < D) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < LPC; ++q) v += sP[t][jj * LPC + q];
+        if (p.Dskip) v = fmaf(p.Dskip[d], sU[t][jj], v);
+        if (zp) v *= silu_precise(sZ[t][jj]);
+        y[(t0 + t) * D + d] = from_f32<TY>(v);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (vj && p.last_state) {
+#pragma unroll
+    for (int k = 0; k < SPL; ++k) p.last_state[(b * D + dj) * N + g * SPL + k] = h[k];
+  }
+}
+
+}  // namespace ssm

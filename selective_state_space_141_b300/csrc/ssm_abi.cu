@@ -1,0 +1,264 @@
+// ssm_abi.cu -- the extern "C" boundary of libssm_b300.so (declared in include/ssm.h).
+//
+// Host side only: validate every descriptor, pick a kernel variant, enqueue it on the
+// caller's stream. Nothing here allocates, frees or synchronises (except the explicit
+// diagnostic ssm_device_error).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "../../include/ssm.h"
+#include "common.cuh"
+#include "scan_fwd.cuh"
+#include "state_update.cuh"
+
+namespace {
+
+using ssm::DecodeParams;
+using ssm::FwdParams;
+
+bool dtype_ok(ssm_dtype_t t) { return t == SSM_F32 || t == SSM_BF16; }
+int64_t elem_size(ssm_dtype_t t) { return t == SSM_F32 ? 4 : 2; }
+
+int64_t numel(const ssm_tensor_t* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// Shape, non-null data and alignment of one descriptor: natural element alignment
+// always, 16 bytes where a kernel reads the tensor with 16-byte vectors (align16).
+ssm_status_t check_tensor(const ssm_tensor_t* t, std::initializer_list<int64_t> shape, bool align16 = false) {
+  if (!t) return SSM_ERR_NULL;
+  if (t->ndim != (int32_t)shape.size() || t->ndim < 1 || t->ndim > 3) return SSM_ERR_SHAPE;
+  int i = 0;
+  for (int64_t s : shape) {
+    if (t->shape[i] != s || s < 0) return SSM_ERR_SHAPE;
+    ++i;
+  }
+  if (!dtype_ok(t->dtype)) return SSM_ERR_DTYPE;
+  if (numel(t) > 0) {
+    if (!t->data) return SSM_ERR_NULL;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(t->data);
+    if (a % (uintptr_t)elem_size(t->dtype) != 0 || (align16 && a % 16 != 0)) return SSM_ERR_LAYOUT;
+  }
+  return SSM_OK;
+}
+
+struct Span {
+  uintptr_t lo = 0, hi = 0;  // [lo, hi)
+};
+Span span_of(const ssm_tensor_t* t) {
+  Span s;
+  if (t && t->data && numel(t) > 0) {
+    s.lo = reinterpret_cast<uintptr_t>(t->data);
+    s.hi = s.lo + (uintptr_t)(numel(t) * elem_size(t->dtype));
+  }
+  return s;
+}
+bool overlaps(const ssm_tensor_t* a, const ssm_tensor_t* b) {
+  Span x = span_of(a), y = span_of(b);
+  if (x.lo == x.hi || y.lo == y.hi) return false;
+  return x.lo < y.hi && y.lo < x.hi;
+}
+
+bool n_supported(int64_t n) { return n == 4 || n == 8 || n == 16; }
+
+// ---- forward launch ------------------------------------------------------------------
+template <typename T, typename TY, int N>
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t st) {
+  constexpr int SPL = 4, DT = 32, TC = 32;
+  dim3 grid((unsigned)((p.D + DT - 1) / DT), (unsigned)p.batch);
+  dim3 block(DT * (N / SPL));
+  void* args[] = {const_cast<FwdParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC>), grid,
+                          block, args, 0, st);
+}
+
+template <typename T, typename TY>
+cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
+  switch (N) {
+    case 4: return launch_fwd<T, TY, 4>(p, st);
+    case 8: return launch_fwd<T, TY, 8>(p, st);
+    default: return launch_fwd<T, TY, 16>(p, st);
+  }
+}
+
+// ---- decode launch -------------------------------------------------------------------
+template <typename T, typename TY, int N>
+cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
+  const int64_t threads = p.batch * p.D * (N / 4);
+  dim3 grid((unsigned)((threads + 255) / 256)), block(256);
+  void* args[] = {const_cast<DecodeParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::state_update_kernel<T, TY, N>), grid, block, args,
+                          0, st);
+}
+
+template <typename T, typename TY>
+cudaError_t launch_dec_n(int64_t N, const DecodeParams& p, cudaStream_t st) {
+  switch (N) {
+    case 4: return launch_dec<T, TY, 4>(p, st);
+    case 8: return launch_dec<T, TY, 8>(p, st);
+    default: return launch_dec<T, TY, 16>(p, st);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_status_string(ssm_status_t s) {
+  switch (s) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_NULL: return "SSM_ERR_NULL: a required descriptor or data pointer is NULL";
+    case SSM_ERR_SHAPE: return "SSM_ERR_SHAPE: ndim or a dimension does not match the contract";
+    case SSM_ERR_DTYPE: return "SSM_ERR_DTYPE: element type not allowed or I/O types differ";
+    case SSM_ERR_LAYOUT: return "SSM_ERR_LAYOUT: misaligned pointer or an output overlaps an input";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: request not implemented by this build";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA: the CUDA runtime reported an error";
+    case SSM_ERR_DEVICE_TIMEOUT: return "SSM_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
+  }
+  return "SSM_ERR_UNKNOWN";
+}
+
+ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                    ssm_tensor_t* y, ssm_tensor_t* last_state, void* stream) {
+  if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+  if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
+  const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
+  if (batch < 0 || L < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
+  ssm_status_t s;
+  if ((s = check_tensor(u, {batch, L, Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(delta, {batch, L, Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(A, {Dm, N})) != SSM_OK) return s;
+  if ((s = check_tensor(B, {batch, L, N})) != SSM_OK) return s;
+  if ((s = check_tensor(C, {batch, L, N})) != SSM_OK) return s;
+  if (D && (s = check_tensor(D, {Dm})) != SSM_OK) return s;
+  if (z && (s = check_tensor(z, {batch, L, Dm})) != SSM_OK) return s;
+  if (delta_bias && (s = check_tensor(delta_bias, {Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(y, {batch, L, Dm})) != SSM_OK) return s;
+  if (last_state && (s = check_tensor(last_state, {batch, Dm, N})) != SSM_OK) return s;
+
+  const ssm_dtype_t io = u->dtype;
+  if (delta->dtype != io || B->dtype != io || C->dtype != io || (z && z->dtype != io)) return SSM_ERR_DTYPE;
+  if (y->dtype != io && y->dtype != SSM_F32) return SSM_ERR_DTYPE;
+  if (A->dtype != SSM_F32 || (D && D->dtype != SSM_F32) || (delta_bias && delta_bias->dtype != SSM_F32) ||
+      (last_state && last_state->dtype != SSM_F32))
+    return SSM_ERR_DTYPE;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_UNSUPPORTED;
+  if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
+  if (batch > 65535) return SSM_ERR_UNSUPPORTED;
+
+  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias};
+  for (const ssm_tensor_t* in : ins) {
+    if (overlaps(y, in)) return SSM_ERR_LAYOUT;
+    if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
+  }
+  if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (batch == 0 || Dm == 0) return SSM_OK;
+  if (L == 0) {
+    if (last_state && cudaMemsetAsync(last_state->data, 0, (size_t)(numel(last_state) * 4), st) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+
+  FwdParams p;
+  p.u = u->data;
+  p.delta = delta->data;
+  p.A = static_cast<const float*>(A->data);
+  p.B = B->data;
+  p.C = C->data;
+  p.Dskip = D ? static_cast<const float*>(D->data) : nullptr;
+  p.z = z ? z->data : nullptr;
+  p.delta_bias = delta_bias ? static_cast<const float*>(delta_bias->data) : nullptr;
+  p.delta_softplus = delta_softplus;
+  p.y = y->data;
+  p.last_state = last_state ? static_cast<float*>(last_state->data) : nullptr;
+  p.batch = batch;
+  p.L = L;
+  p.D = Dm;
+
+  cudaError_t e;
+  if (io == SSM_F32)
+    e = launch_fwd_n<float, float>(N, p, st);
+  else if (y->dtype == SSM_BF16)
+    e = launch_fwd_n<__nv_bfloat16, __nv_bfloat16>(N, p, st);
+  else
+    e = launch_fwd_n<__nv_bfloat16, float>(N, p, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta,
+                              const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
+                              const ssm_tensor_t* D, const ssm_tensor_t* z, ssm_tensor_t* y, void* stream) {
+  if (!state || !x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+  if (state->ndim != 3) return SSM_ERR_SHAPE;
+  const int64_t batch = state->shape[0], Dm = state->shape[1], N = state->shape[2];
+  if (batch < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
+  ssm_status_t s;
+  if ((s = check_tensor(state, {batch, Dm, N}, true)) != SSM_OK) return s;
+  if ((s = check_tensor(x, {batch, Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(delta, {batch, Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(A, {Dm, N}, true)) != SSM_OK) return s;
+  if ((s = check_tensor(B, {batch, N})) != SSM_OK) return s;
+  if ((s = check_tensor(C, {batch, N})) != SSM_OK) return s;
+  if (D && (s = check_tensor(D, {Dm})) != SSM_OK) return s;
+  if (z && (s = check_tensor(z, {batch, Dm})) != SSM_OK) return s;
+  if ((s = check_tensor(y, {batch, Dm})) != SSM_OK) return s;
+
+  const ssm_dtype_t io = x->dtype;
+  if (delta->dtype != io || B->dtype != io || C->dtype != io || (z && z->dtype != io)) return SSM_ERR_DTYPE;
+  if (y->dtype != io && y->dtype != SSM_F32) return SSM_ERR_DTYPE;
+  if (state->dtype != SSM_F32 || A->dtype != SSM_F32 || (D && D->dtype != SSM_F32)) return SSM_ERR_DTYPE;
+  if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
+
+  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, z};
+  for (const ssm_tensor_t* in : ins) {
+    if (overlaps(y, in)) return SSM_ERR_LAYOUT;
+    if (overlaps(state, in)) return SSM_ERR_LAYOUT;
+  }
+  if (overlaps(state, y)) return SSM_ERR_LAYOUT;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (batch == 0 || Dm == 0) return SSM_OK;
+
+  DecodeParams p;
+  p.state = static_cast<float*>(state->data);
+  p.x = x->data;
+  p.delta = delta->data;
+  p.A = static_cast<const float*>(A->data);
+  p.B = B->data;
+  p.C = C->data;
+  p.Dskip = D ? static_cast<const float*>(D->data) : nullptr;
+  p.z = z ? z->data : nullptr;
+  p.y = y->data;
+  p.batch = batch;
+  p.D = Dm;
+
+  cudaError_t e;
+  if (io == SSM_F32)
+    e = launch_dec_n<float, float>(N, p, st);
+  else if (y->dtype == SSM_BF16)
+    e = launch_dec_n<__nv_bfloat16, __nv_bfloat16>(N, p, st);
+  else
+    e = launch_dec_n<__nv_bfloat16, float>(N, p, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status_t ssm_device_error(void* stream, int32_t* code) {
+  if (!code) return SSM_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, ssm::g_ssm_error, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+  if (cudaMemcpyToSymbol(ssm::g_ssm_error, &zero, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+  *code = v;
+  return SSM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// state_update.cuh -- single-token recurrent decode step, fp32 state updated in place.
+//
+// For each (b, d):  state[n] = exp(dt A[d,n]) state[n] + dt B[b,n] x
+//                   y = (sum_n C[b,n] state[n] + D[d] x) * silu(z)
+// ("8.7 State Space Models (Mamba)", section 5: O(1) work per generated token on a
+//  fixed d*n state; "Mamba and State Space Models", "Selective scan pseudo-code",
+//  one iteration of the loop body.)
+//
+// The step streams the whole state once (read + write, 16-byte vectors); it is bound
+// by memory bandwidth, not arithmetic.
+#pragma once
+
+#include "common.cuh"
+
+namespace ssm {
+
+struct DecodeParams {
+  float* state;
+  const void* x;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* Dskip;  // nullable
+  const void* z;       // nullable
+  void* y;
+  int64_t batch, D;
+};
+
+// One thread per (b, d, group of 4 states); the N/4 lanes of a channel are adjacent
+// in the warp and combine their partial C.h with xor-shuffles.
+template <typename T, typename TY, int N>
+__global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p) {
+  constexpr int LPC = N / 4;
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bd = gt / LPC;
+  const int g = (int)(gt % LPC);
+  const int64_t nbd = p.batch * p.D;
+  const bool v = bd < nbd;
+  const int64_t b = v ? bd / p.D : 0, d = v ? bd % p.D : 0;
+
+  float acc = 0.f, x = 0.f;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (v) {
+    const T* xp = static_cast<const T*>(p.x);
+    const T* dp = static_cast<const T*>(p.delta);
+    const T* Bp = static_cast<const T*>(p.B) + b * N + g * 4;
+    const T* Cp = static_cast<const T*>(p.C) + b * N + g * 4;
+    x = to_f32(xp[bd]);
+    const float dt = to_f32(dp[bd]);
+    const float dx = dt * x;
+    float4* sp = reinterpret_cast<float4*>(p.state + bd * N + g * 4);
+    s = *sp;
+    const float4 a4 = *reinterpret_cast<const float4*>(p.A + d * N + g * 4);
+    float sv[4] = {s.x, s.y, s.z, s.w};
+    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = decay<sizeof(T) == 4>(dt, av[k], av[k] * kLog2e);
+      sv[k] = fmaf(a, sv[k], dx * to_f32(Bp[k]));
+      acc = fmaf(to_f32(Cp[k]), sv[k], acc);
+    }
+    *sp = make_float4(sv[0], sv[1], sv[2], sv[3]);
+  }
+#pragma unroll
+  for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (v && g == 0) {
+    float out = acc;
+    if (p.Dskip) out = fmaf(p.Dskip[d], x, out);
+    if (p.z) out *= silu_precise(to_f32(static_cast<const T*>(p.z)[bd]));
+    static_cast<TY*>(p.y)[bd] = from_f32<TY>(out);
+  }
+}
+
+}  // namespace ssm

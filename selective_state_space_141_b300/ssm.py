@@ -1,0 +1,137 @@
+"""ctypes binding over libssm_b300.so (the C ABI in include/ssm.h).
+
+Argument marshalling only: torch tensors become ssm_tensor_t descriptors (device
+pointer, element type, shape) and the current torch stream is passed through. Every
+step of the computation runs in the library's CUDA kernels. There is no fallback: if
+the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssm_b300.so")
+
+SSM_F32, SSM_BF16 = 0, 1
+_BAD_DTYPE = 99  # forwarded for any other torch dtype so the library reports SSM_ERR_DTYPE
+_DTYPES = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
+
+STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_DTYPE", 4: "SSM_ERR_LAYOUT",
+          5: "SSM_ERR_UNSUPPORTED", 6: "SSM_ERR_CUDA", 7: "SSM_ERR_DEVICE_TIMEOUT"}
+
+
+class SsmTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 3)]
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+_lib = None
+_P = ctypes.POINTER(SsmTensor)
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of the CUDA library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise SsmError(6, f"CUDA library not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    lib.ssm_selective_scan_fwd.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P, ctypes.c_void_p]
+    lib.ssm_state_update.restype = ctypes.c_int
+    lib.ssm_state_update.argtypes = [_P] * 9 + [ctypes.c_void_p]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [ctypes.c_int]
+    lib.ssm_device_error.restype = ctypes.c_int
+    lib.ssm_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    _lib = lib
+    return lib
+
+
+def describe(t: torch.Tensor | None):
+    """ssm_tensor_t for a dense tensor (None -> NULL). Non-contiguous tensors are refused
+    here because the descriptor carries no strides."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise SsmError(4, "tensor is not contiguous")
+    if t.dim() > 3:
+        raise SsmError(2, "tensor has more than 3 dimensions")
+    d = SsmTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES.get(t.dtype, _BAD_DTYPE)
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = s
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, y=None,
+                       last_state=None, return_last_state=True, y_dtype=None, stream=None):
+    """Fused selective-scan forward pass (``ssm_selective_scan_fwd``).
+
+    u, delta, z: (batch, L, D); A: (D, N) fp32; B, C: (batch, L, N); D, delta_bias: (D) fp32.
+    Outputs are allocated with torch on u's device unless given. Returns (y, last_state);
+    last_state is None when ``return_last_state`` is False and none was passed.
+    """
+    lib = load_library()
+    if y is None:
+        y = torch.empty(u.shape, dtype=y_dtype or u.dtype, device=u.device)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((u.shape[0], u.shape[2], A.shape[-1]), dtype=torch.float32, device=u.device)
+    ds = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias, y, last_state)]
+    st = lib.ssm_selective_scan_fwd(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
+                                    _ref(ds[9]), _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_selective_scan_fwd")
+    return y, last_state
+
+
+def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, y_dtype=None, stream=None):
+    """One decode step (``ssm_state_update``); ``state`` (batch, D, N) fp32 is updated in
+    place. x, delta, z: (batch, D); B, C: (batch, N). Returns y (batch, D)."""
+    lib = load_library()
+    if y is None:
+        y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
+    ds = [describe(t) for t in (state, x, delta, A, B, C, D, z, y)]
+    st = lib.ssm_state_update(*[_ref(d) for d in ds], _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_state_update")
+    return y
+
+
+def device_error(stream=None) -> int:
+    """Synchronise and read/clear the library's device error word (0 = none)."""
+    lib = load_library()
+    code = ctypes.c_int32(0)
+    st = lib.ssm_device_error(_stream(stream), ctypes.byref(code))
+    if st != 0:
+        raise SsmError(st, "ssm_device_error")
+    return int(code.value)

@@ -1,0 +1,169 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry point
+include/ssm.h declares, and rejects bad arguments on the host before any CUDA call.
+Only argument-validation paths run here (fake, never-dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_141_b300 import ssm
+from selective_state_space_141_b300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return ssm.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ssm.h")).read()
+    return sorted(set(re.findall(r"SSM_API\s+[\w\s\*]+?\b(ssm_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert {"ssm_selective_scan_fwd", "ssm_state_update", "ssm_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in ssm.STATUS.items():
+        assert lib.ssm_status_string(code).decode().startswith(name)
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails before any launch
+
+
+def T(shape, dtype=ssm.SSM_BF16, addr=None):
+    t = ssm.SsmTensor()
+    n = 1
+    for s in shape:
+        n *= s
+    global FAKE
+    if addr is None:
+        addr = FAKE
+        FAKE += ((n * 4 + 255) // 256 + 1) * 256
+    t.data = addr if n > 0 else None
+    t.dtype = dtype
+    t.ndim = len(shape)
+    for i, s in enumerate(shape):
+        t.shape[i] = s
+    return t
+
+
+def fwd_args(b=2, L=5, D=8, N=16, io=ssm.SSM_BF16):
+    return dict(u=T((b, L, D), io), delta=T((b, L, D), io), A=T((D, N), ssm.SSM_F32), B=T((b, L, N), io),
+                C=T((b, L, N), io), D=T((D,), ssm.SSM_F32), z=T((b, L, D), io), bias=T((D,), ssm.SSM_F32),
+                y=T((b, L, D), io), last=T((b, D, N), ssm.SSM_F32))
+
+
+def call_fwd(lib, a, softplus=1):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    return lib.ssm_selective_scan_fwd(r("u"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("bias"),
+                                      softplus, r("y"), r("last"), None)
+
+
+def test_fwd_null(lib):
+    for k in ("u", "delta", "A", "B", "C", "y"):
+        a = fwd_args()
+        a[k] = None
+        assert call_fwd(lib, a) == 1, k
+    a = fwd_args()
+    a["u"].data = None
+    assert call_fwd(lib, a) == 1
+
+
+def test_fwd_shape(lib):
+    a = fwd_args()
+    a["delta"] = T((2, 5, 9))
+    assert call_fwd(lib, a) == 2
+    a = fwd_args()
+    a["B"] = T((2, 4, 16))
+    assert call_fwd(lib, a) == 2
+    a = fwd_args()
+    a["last"] = T((2, 8, 8), ssm.SSM_F32)
+    assert call_fwd(lib, a) == 2
+    a = fwd_args()
+    a["u"].ndim = 2
+    assert call_fwd(lib, a) == 2
+
+
+def test_fwd_dtype(lib):
+    a = fwd_args()
+    a["z"].dtype = ssm.SSM_F32
+    assert call_fwd(lib, a) == 3
+    a = fwd_args()
+    a["A"].dtype = ssm.SSM_BF16
+    assert call_fwd(lib, a) == 3
+    a = fwd_args(io=ssm.SSM_F32)
+    a["y"].dtype = ssm.SSM_BF16  # f32 call cannot write bf16 y
+    assert call_fwd(lib, a) == 3
+    a = fwd_args()
+    a["u"].dtype = 7
+    assert call_fwd(lib, a) == 3
+
+
+def test_fwd_layout(lib):
+    a = fwd_args()
+    a["u"].data = a["u"].data + 1  # not aligned to its 2-byte elements
+    assert call_fwd(lib, a) == 4
+    a = fwd_args()
+    a["y"].data = a["u"].data  # y aliases u
+    assert call_fwd(lib, a) == 4
+    a = fwd_args()
+    a["last"].data = a["z"].data + 16  # last_state overlaps z
+    assert call_fwd(lib, a) == 4
+
+
+def test_fwd_unsupported(lib):
+    a = fwd_args(N=5)
+    assert call_fwd(lib, a) == 5
+    a = fwd_args(N=32)
+    assert call_fwd(lib, a) == 5
+    assert call_fwd(lib, fwd_args(), softplus=2) == 5
+
+
+def test_fwd_empty_batch_is_noop(lib):
+    assert call_fwd(lib, fwd_args(b=0)) == 0
+    assert call_fwd(lib, fwd_args(D=0)) == 0
+
+
+def dec_args(b=3, D=8, N=16, io=ssm.SSM_BF16):
+    return dict(state=T((b, D, N), ssm.SSM_F32), x=T((b, D), io), delta=T((b, D), io), A=T((D, N), ssm.SSM_F32),
+                B=T((b, N), io), C=T((b, N), io), D=T((D,), ssm.SSM_F32), z=T((b, D), io), y=T((b, D), io))
+
+
+def call_dec(lib, a):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    return lib.ssm_state_update(r("state"), r("x"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("y"),
+                                None)
+
+
+def test_decode_validation(lib):
+    for k in ("state", "x", "delta", "A", "B", "C", "y"):
+        a = dec_args()
+        a[k] = None
+        assert call_dec(lib, a) == 1, k
+    a = dec_args()
+    a["x"] = T((3, 9))
+    assert call_dec(lib, a) == 2
+    a = dec_args()
+    a["state"].dtype = ssm.SSM_BF16
+    assert call_dec(lib, a) == 3
+    a = dec_args()
+    a["y"].data = a["state"].data
+    assert call_dec(lib, a) == 4
+    assert call_dec(lib, dec_args(N=12)) == 5
+    assert call_dec(lib, dec_args(b=0)) == 0
+
+
+def test_binding_refuses_noncontiguous():
+    import torch
+    t = torch.zeros(4, 6)[:, ::2]
+    with pytest.raises(ssm.SsmError):
+        ssm.describe(t)

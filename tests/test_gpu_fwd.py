@@ -1,0 +1,197 @@
+"""GPU forward scan vs the fp64 oracle, called through the C ABI.
+
+Small shapes are compared element by element over whole tensors (several tiles plus
+ragged tails in L and D). The full-size workloads run the exact launch the bench
+times and are compared on seeded samples of channels (each channel is an independent
+recurrence, so the oracle computes exactly those channels over the whole sequence).
+"""
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+from parity import TOL_BF16, TOL_F32, check, to64
+from selective_state_space_141_b300 import inputs, ssm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def gpu_fwd(d, y_dtype=None):
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], delta_softplus=d["delta_softplus"],
+                                     y_dtype=y_dtype)
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    return y, last
+
+
+def oracle_fwd(d):
+    return oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], delta_softplus=d["delta_softplus"])
+
+
+def to_dev(d):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def sample_channels(d, per_row, rows, seed):
+    """Oracle on a seeded sample of channels: {b: (ds, y_ref (L, k), state_ref (k, N))}."""
+    rng = np.random.default_rng(seed)
+    batch, L, D = d["u"].shape
+    out = {}
+    for b in sorted(rng.choice(batch, size=min(rows, batch), replace=False).tolist()):
+        ds = np.sort(rng.choice(D, size=min(per_row, D), replace=False))
+        idx = torch.as_tensor(ds, device=d["u"].device)
+        sub = dict(
+            u=d["u"][b:b + 1].index_select(2, idx), delta=d["delta"][b:b + 1].index_select(2, idx),
+            z=None if d["z"] is None else d["z"][b:b + 1].index_select(2, idx),
+            B=d["B"][b:b + 1], C=d["C"][b:b + 1], A=d["A"].index_select(0, idx),
+            D=None if d["D"] is None else d["D"].index_select(0, idx),
+            delta_bias=None if d["delta_bias"] is None else d["delta_bias"].index_select(0, idx),
+            delta_softplus=d["delta_softplus"])
+        y, last = oracle_fwd(sub)
+        out[b] = (ds, y[0], last[0])
+    return out
+
+
+def check_sampled(y, last, ref, tol, bf16_out, what):
+    for b, (ds, yr, sr) in ref.items():
+        idx = torch.as_tensor(ds, device=y.device)
+        check(y[b].index_select(1, idx), yr, tol, bf16_out, f"{what} y b={b}")
+        check(last[b].index_select(0, idx), sr, tol, False, f"{what} last_state b={b}")
+
+
+# ---- the five workloads (four forward) -----------------------------------------------
+
+def test_tiny_fp32_full():
+    d = to_dev(inputs.fwd_inputs(inputs.TINY))
+    y, last = gpu_fwd(d)
+    yr, sr = oracle_fwd(d)
+    check(y, yr, TOL_F32, False, "y")
+    check(last, sr, TOL_F32, False, "last_state")
+
+
+@pytest.mark.parametrize("key", ["m130m", "m1p4b"])
+def test_layer_workloads_sampled(key):
+    w = inputs.FWD_WORKLOADS[key]
+    d = inputs.fwd_inputs(w, DEV)
+    ref = sample_channels(d, per_row=24, rows=3, seed=11)
+    y, last = gpu_fwd(d)
+    check_sampled(y, last, ref, TOL_BF16, True, key)
+    y32, last32 = gpu_fwd(d, y_dtype=torch.float32)
+    check_sampled(y32, last32, ref, TOL_BF16, False, key + " (fp32 out)")
+    # The bf16 output is the fp32 output rounded to nearest-even.
+    assert torch.equal(y, y32.to(torch.bfloat16))
+
+
+def test_long_sequence_sampled():
+    d = inputs.fwd_inputs(inputs.LONG, DEV)
+    ref = sample_channels(d, per_row=6, rows=1, seed=12)
+    y, last = gpu_fwd(d)
+    check_sampled(y, last, ref, TOL_BF16, True, "long")
+
+
+def test_long_sequence_lti_vs_convolution():
+    """Time-invariant sub-case: the first 4096 outputs equal the convolution with
+    K_j = sum_n C_n exp(j dt A_n) dt B_n (brute force, independent of the oracle)."""
+    d = inputs.fwd_inputs(inputs.LONG, DEV, lti=True)
+    y, _ = gpu_fwd(d, y_dtype=torch.float32)
+    T = 4096
+    rng = np.random.default_rng(13)
+    ds = rng.choice(inputs.LONG.D, size=8, replace=False)
+    A, B0, C0 = to64(d["A"]), to64(d["B"][0, 0]), to64(d["C"][0, 0])
+    bias, Dk = to64(d["delta_bias"]), to64(d["D"])
+    u, z, raw = to64(d["u"][0, :T]), to64(d["z"][0, :T]), to64(d["delta"][0, 0])
+    yg = to64(y[0, :T])
+    for dd in ds:
+        dt = np.logaddexp(0.0, raw[dd] + bias[dd])
+        K = (C0 * np.exp(np.arange(T)[:, None] * dt * A[dd]) * dt * B0).sum(-1)
+        conv = np.convolve(u[:, dd], K)[:T]
+        ref = (conv + Dk[dd] * u[:, dd]) * z[:, dd] * expit(z[:, dd])
+        check(yg[:, dd], ref, TOL_BF16, False, f"lti channel {dd}")
+
+
+# ---- small shapes, whole tensors --------------------------------------------------------
+
+SHAPES = [  # batch, L, D, N
+    (1, 1, 1, 16), (2, 2, 3, 16), (1, 31, 33, 16), (3, 32, 64, 16), (2, 33, 65, 8), (1, 100, 96, 4),
+    (2, 257, 130, 16), (1, 1000, 40, 16), (4, 64, 512, 16),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_random_shapes(shape, dtype):
+    b, L, D, N = shape
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=dtype, seed=sum(shape)))
+    yr, sr = oracle_fwd(d)
+    if dtype == torch.float32:
+        y, last = gpu_fwd(d)
+        check(y, yr, TOL_F32, False, "y")
+        check(last, sr, TOL_F32, False, "last")
+    else:
+        y, last = gpu_fwd(d)
+        check(y, yr, TOL_BF16, True, "y bf16")
+        y32, _ = gpu_fwd(d, y_dtype=torch.float32)
+        check(y32, yr, TOL_BF16, False, "y fp32-out")
+        check(last, sr, TOL_BF16, False, "last")
+
+
+@pytest.mark.parametrize("flags", [(0, 0, 0, 1), (1, 0, 0, 1), (0, 1, 0, 1), (0, 0, 1, 1), (1, 1, 1, 0),
+                                   (0, 0, 0, 0)], ids=lambda f: "D%dz%dbias%dsp%d" % f)
+def test_optional_inputs(flags):
+    has_D, has_z, has_bias, sp = flags
+    d = to_dev(inputs.random_fwd(2, 70, 48, 16, dtype=torch.float32, seed=5, has_bias=bool(has_bias),
+                                 has_D=bool(has_D), has_z=bool(has_z), delta_softplus=bool(sp)))
+    if not sp:  # positive step sizes without softplus (the default bias is negative)
+        d["delta"] = d["delta"].abs() * 0.05
+        if d["delta_bias"] is not None:
+            d["delta_bias"] = d["delta_bias"].abs() * 0.01
+    yr, sr = oracle_fwd(d)
+    y, last = gpu_fwd(d)
+    check(y, yr, TOL_F32, False, "y")
+    check(last, sr, TOL_F32, False, "last")
+
+
+def test_zero_length_zeroes_last_state():
+    d = to_dev(inputs.random_fwd(2, 0, 16, 16, dtype=torch.bfloat16))
+    last = torch.full((2, 16, 16), 7.0, device=DEV)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], last_state=last)
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and torch.all(last == 0)
+
+
+def test_empty_batch_noop():
+    d = to_dev(inputs.random_fwd(0, 5, 16, 16, dtype=torch.bfloat16))
+    y, last = gpu_fwd(d)
+    assert y.numel() == 0 and last.numel() == 0
+
+
+def test_delta_zero_holds_state():
+    d = to_dev(inputs.random_fwd(1, 50, 32, 16, dtype=torch.float32, has_bias=False, delta_softplus=False))
+    d["delta"].zero_()
+    y, last = gpu_fwd(d)
+    assert torch.all(last == 0)
+    ref = to64(d["D"]) * to64(d["u"]) * to64(d["z"]) * expit(to64(d["z"]))
+    check(y, ref, TOL_F32, False, "y = D u silu(z)")
+
+
+def test_large_delta_resets_state():
+    d = to_dev(inputs.random_fwd(1, 40, 32, 16, dtype=torch.float32, has_bias=False, has_D=False, has_z=False,
+                                 delta_softplus=False))
+    d["delta"].fill_(50.0)
+    y, last = gpu_fwd(d)
+    h = 50.0 * to64(d["B"])[0][:, None, :] * to64(d["u"])[0][:, :, None]  # (L, D, N)
+    ref = np.einsum("ln,ldn->ld", to64(d["C"])[0], h)
+    check(y[0], ref, TOL_F32, False, "y")
+    check(last[0], h[-1], TOL_F32, False, "last")
+
+
+def test_rerun_is_deterministic():
+    d = to_dev(inputs.random_fwd(2, 300, 96, 16, dtype=torch.bfloat16, seed=3))
+    y1, s1 = gpu_fwd(d)
+    y2, s2 = gpu_fwd(d)
+    assert torch.equal(y1, y2) and torch.equal(s1, s2)
