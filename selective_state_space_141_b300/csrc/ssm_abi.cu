@@ -3,14 +3,19 @@
 // Host side only: validate every descriptor, pick a kernel variant, enqueue it on the
 // caller's stream. Nothing here allocates, frees or synchronises (except the explicit
 // diagnostic ssm_device_error).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <initializer_list>
 
 #include "../../include/ssm.h"
 #include "common.cuh"
 #include "scan_fwd.cuh"
+#include "scan_fwd_chan.cuh"
 #include "state_update.cuh"
 
 namespace {
@@ -65,7 +70,90 @@ bool overlaps(const ssm_tensor_t* a, const ssm_tensor_t* b) {
 
 bool n_supported(int64_t n) { return n == 4 || n == 8 || n == 16; }
 
-// ---- forward launch ------------------------------------------------------------------
+// ---- kernel-variant selection ------------------------------------------------------
+// SSM_B300_FORWARD_KERNEL = auto (default) | generic | chan. Both variants compute the
+// same result; the override exists so each can be checked on its own.
+enum class FwdVariant { kAuto, kGeneric, kChan };
+FwdVariant forward_variant() {
+  const char* e = getenv("SSM_B300_FORWARD_KERNEL");
+  if (e && strcmp(e, "generic") == 0) return FwdVariant::kGeneric;
+  if (e && strcmp(e, "chan") == 0) return FwdVariant::kChan;
+  return FwdVariant::kAuto;
+}
+
+// ---- TMA descriptors -------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Row-major bf16 matrix (outer x inner), box (box_outer x box_inner), zero fill outside.
+bool encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+// ---- channel-parallel TMA kernel (bf16 I/O) ----------------------------------------------
+constexpr int kChanTC = 64, kChanStages = 3;
+
+bool chan_eligible(const FwdParams& p, int64_t N) {
+  // TMA needs 16-byte aligned bases and row pitches (D % 8 == 0 for bf16) and int32 row
+  // coordinates; last_state is written with 16-byte vector stores.
+  return (N == 8 || N == 16) && p.D % 8 == 0 && p.batch * p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
+         aligned16(p.delta) && aligned16(p.z) && aligned16(p.B) && aligned16(p.C) &&
+         aligned16(p.last_state) && encode_fn() != nullptr;
+}
+
+template <typename TY, int N>
+cudaError_t launch_chan(const FwdParams& p, cudaStream_t st, bool* launched) {
+  *launched = false;
+  const uint64_t rows = (uint64_t)(p.batch * p.L);
+  CUtensorMap mu, md, mz, mb, mc;
+  if (!encode_bf16_2d(&mu, p.u, p.D, rows, ssm::kChanCTA, kChanTC) ||
+      !encode_bf16_2d(&md, p.delta, p.D, rows, ssm::kChanCTA, kChanTC) ||
+      !encode_bf16_2d(&mb, p.B, N, rows, N, kChanTC) || !encode_bf16_2d(&mc, p.C, N, rows, N, kChanTC))
+    return cudaSuccess;
+  if (p.z) {
+    if (!encode_bf16_2d(&mz, p.z, p.D, rows, ssm::kChanCTA, kChanTC)) return cudaSuccess;
+  } else {
+    mz = mu;  // never read when z is absent
+  }
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages>;
+  constexpr int smem = ssm::chan_smem_bytes<N, kChanTC, kChanStages>();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  dim3 grid((unsigned)((p.D + ssm::kChanCTA - 1) / ssm::kChanCTA), (unsigned)p.batch);
+  void* args[] = {&mu, &md, &mz, &mb, &mc, const_cast<FwdParams*>(&p)};
+  *launched = true;
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(ssm::kChanThreads), args, smem, st);
+}
+
+template <typename TY>
+cudaError_t launch_chan_n(int64_t N, const FwdParams& p, cudaStream_t st, bool* launched) {
+  if (N == 8) return launch_chan<TY, 8>(p, st, launched);
+  return launch_chan<TY, 16>(p, st, launched);
+}
+
+// ---- generic forward launch ------------------------------------------------------------
 template <typename T, typename TY, int N>
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t st) {
   constexpr int SPL = 4, DT = 32, TC = 32;
@@ -184,6 +272,13 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   p.D = Dm;
 
   cudaError_t e;
+  const FwdVariant var = forward_variant();
+  if (io == SSM_BF16 && var != FwdVariant::kGeneric && chan_eligible(p, N)) {
+    bool launched = false;
+    e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, st, &launched)
+                             : launch_chan_n<float>(N, p, st, &launched);
+    if (launched || e != cudaSuccess) return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  }
   if (io == SSM_F32)
     e = launch_fwd_n<float, float>(N, p, st);
   else if (y->dtype == SSM_BF16)

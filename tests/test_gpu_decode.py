@@ -84,8 +84,15 @@ def test_decode_iterated_equals_forward():
                                    z=d["z"][:, t].contiguous(), y_dtype=torch.float32))
     torch.cuda.synchronize()
     y_d = torch.stack(ys, 1)
-    check(y_d, y_f, TOL_F32, False, "decode vs forward y")
-    check(state, last_f, TOL_F32, False, "decode vs forward state")
+    # bf16 inputs: the two kernels may use different fast SFU forms, so they agree to
+    # the bf16 tolerance, and each matches the oracle.
+    yr, sr = oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                       delta_softplus=False)
+    check(y_d, y_f, TOL_BF16, False, "decode vs forward y")
+    check(state, last_f, TOL_BF16, False, "decode vs forward state")
+    check(y_d, yr, TOL_BF16, False, "decode vs oracle y")
+    check(y_f, yr, TOL_BF16, False, "forward vs oracle y")
+    check(state, sr, TOL_BF16, False, "decode vs oracle state")
 
 
 def test_prefix_state_then_decode():

@@ -195,3 +195,39 @@ def test_rerun_is_deterministic():
     y1, s1 = gpu_fwd(d)
     y2, s2 = gpu_fwd(d)
     assert torch.equal(y1, y2) and torch.equal(s1, s2)
+
+
+# ---- each forward kernel variant on its own ---------------------------------------------
+
+CHAN_SHAPES = [  # shapes the TMA channel kernel accepts (bf16, D % 8 == 0, N in {8, 16})
+    (1, 1, 8, 16), (2, 63, 136, 16), (2, 64, 128, 16), (3, 65, 256, 8), (1, 200, 1000, 16), (1, 1000, 264, 16),
+    (2, 130, 384, 16),
+]
+
+
+@pytest.mark.parametrize("variant", ["generic", "chan"])
+@pytest.mark.parametrize("shape", CHAN_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_variants_vs_oracle(shape, variant, monkeypatch):
+    monkeypatch.setenv("SSM_B300_FORWARD_KERNEL", variant)
+    b, L, D, N = shape
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=torch.bfloat16, seed=100 + sum(shape)))
+    yr, sr = oracle_fwd(d)
+    y, last = gpu_fwd(d)
+    check(y, yr, TOL_BF16, True, f"{variant} y")
+    check(last, sr, TOL_BF16, False, f"{variant} last")
+    y32, _ = gpu_fwd(d, y_dtype=torch.float32)
+    check(y32, yr, TOL_BF16, False, f"{variant} y fp32-out")
+
+
+@pytest.mark.parametrize("flags", [(0, 0, 0, 1), (1, 1, 0, 0)], ids=["bare", "D_z_nosoftplus"])
+def test_chan_optional_inputs(flags, monkeypatch):
+    monkeypatch.setenv("SSM_B300_FORWARD_KERNEL", "chan")
+    has_D, has_z, has_bias, sp = flags
+    d = to_dev(inputs.random_fwd(2, 150, 256, 16, dtype=torch.bfloat16, seed=7, has_bias=bool(has_bias),
+                                 has_D=bool(has_D), has_z=bool(has_z), delta_softplus=bool(sp)))
+    if not sp:
+        d["delta"] = (d["delta"].float().abs() * 0.05).to(torch.bfloat16)
+    yr, sr = oracle_fwd(d)
+    y, last = gpu_fwd(d, y_dtype=torch.float32)
+    check(y, yr, TOL_BF16, False, "y")
+    check(last, sr, TOL_BF16, False, "last")
