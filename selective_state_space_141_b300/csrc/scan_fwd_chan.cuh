@@ -10,12 +10,16 @@
 //    at the same rate.
 //  * A CTA covers 128 consecutive channels of one batch row and walks the sequence
 //    in chunks of TC steps. Tiles of u, delta, z (TC x 128 bf16) and B, C (TC x N)
-//    arrive by TMA into an S-stage shared-memory ring guarded by mbarriers:
+//    arrive by TMA (3-D maps over (D, L, batch), zero fill past L) into an S-stage
+//    shared-memory ring guarded by mbarriers:
 //      warp 4 (one lane)  issues the TMA loads            full[s]  (tx bytes)
 //      warp 5             converts B, C to fp32 in smem   ready[s] (32 arrivals)
 //      warps 0..3         run the recurrence              empty[s] (4 arrivals)
-//  * The state h never leaves registers; y goes straight to global memory, the final
-//    state once at the end.
+//  * y of each chunk goes to a per-warp shared tile (double-buffered) and leaves by
+//    one TMA store per warp per chunk; the store clips at L and D. The state h never
+//    leaves registers; the final state is written once at the end.
+//  * The softplus and gate switches are template parameters, so the unrolled step
+//    loops carry no branches; an absent D skip or bias is a zero value.
 // Every mbarrier wait is bounded (tma.cuh); on timeout a warp records the error word
 // and returns, and the TMA issuer waits (bounded) for its loads still in flight.
 #pragma once
@@ -29,18 +33,21 @@ namespace ssm {
 constexpr int kChanCTA = 128;  // channels per CTA (4 consumer warps x 32 lanes)
 constexpr int kChanThreads = 192;
 
-template <int N, int TC>
+template <typename TY, int N, int TC>
 struct ChanLayout {
-  static constexpr int kTileIO = TC * kChanCTA * 2;  // bf16 (TC x 128)
-  static constexpr int kTileBC = TC * N * 2;         // bf16 (TC x N)
-  static constexpr int kTileBC32 = TC * 2 * N * 4;   // fp32 (TC x [B | C])
+  static constexpr int kTileIO = TC * kChanCTA * 2;     // bf16 (TC x 128)
+  static constexpr int kTileBC = TC * N * 2;            // bf16 (TC x N)
+  static constexpr int kTileBC32 = TC * 2 * N * 4;      // fp32 (TC x [B | C])
   static constexpr int kStage = 3 * kTileIO + 2 * kTileBC + kTileBC32;
-  static_assert(kTileIO % 128 == 0 && kTileBC % 128 == 0 && kTileBC32 % 128 == 0, "tile alignment");
+  static constexpr int kTileY = TC * 32 * (int)sizeof(TY);  // one warp's y tile (TC x 32)
+  static_assert(kTileIO % 128 == 0 && kTileBC % 128 == 0 && kTileBC32 % 128 == 0 && kTileY % 128 == 0,
+                "tile alignment");
 };
 
-template <int N, int TC, int S>
+template <typename TY, int N, int TC, int S>
 constexpr int chan_smem_bytes() {
-  return S * ChanLayout<N, TC>::kStage + 3 * S * 8;
+  using Lay = ChanLayout<TY, N, TC>;
+  return S * Lay::kStage + 4 * 2 * Lay::kTileY + 3 * S * 8;
 }
 
 // Softplus for the bf16 path: 2^x and log2 on the SFU; e^r below 2^-10 uses
@@ -59,23 +66,46 @@ __device__ __forceinline__ float silu_fast(float z) {
   return fmaf(hz, tanh_fast(hz), hz);
 }
 
-template <typename TY, int N, int TC, int S>
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most n committed bulk stores still read shared memory.
+template <int n>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(n) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate>
 __global__ void __launch_bounds__(kChanThreads, 1)
 scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-              const __grid_constant__ CUtensorMap tm_C, const FwdParams p) {
-  using Lay = ChanLayout<N, TC>;
+              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
+              const FwdParams p) {
+  using Lay = ChanLayout<TY, N, TC>;
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Lay::kStage);
+  unsigned char* ytiles = smem + S * Lay::kStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ytiles + 4 * 2 * Lay::kTileY);
   uint64_t* ready = full + S;
   uint64_t* empty = ready + S;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t b = blockIdx.y;
+  const int32_t b = (int32_t)blockIdx.y;
   const int64_t d0 = (int64_t)blockIdx.x * kChanCTA;
   const int64_t L = p.L, D = p.D;
   const int nchunks = (int)((L + TC - 1) / TC);
-  const bool has_z = p.z != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -91,23 +121,22 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     if (lane == 0) {
       prefetch_tensormap(&tm_u);
       prefetch_tensormap(&tm_dl);
-      if (has_z) prefetch_tensormap(&tm_z);
+      if (kGate) prefetch_tensormap(&tm_z);
       prefetch_tensormap(&tm_B);
       prefetch_tensormap(&tm_C);
-      const uint32_t tx = (has_z ? 3 : 2) * Lay::kTileIO + 2 * Lay::kTileBC;
+      constexpr uint32_t tx = (kGate ? 3 : 2) * Lay::kTileIO + 2 * Lay::kTileBC;
       int issued = 0;
       for (int k = 0; k < nchunks; ++k) {
         const int s = k % S;
         if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, kErrWaitEmpty)) break;
         unsigned char* st = smem + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], tx);
-        const int32_t row = (int32_t)(b * L + (int64_t)k * TC);
-        const int32_t col = (int32_t)d0;
-        tma_load_2d(st, &tm_u, col, row, &full[s]);
-        tma_load_2d(st + Lay::kTileIO, &tm_dl, col, row, &full[s]);
-        if (has_z) tma_load_2d(st + 2 * Lay::kTileIO, &tm_z, col, row, &full[s]);
-        tma_load_2d(st + 3 * Lay::kTileIO, &tm_B, 0, row, &full[s]);
-        tma_load_2d(st + 3 * Lay::kTileIO + Lay::kTileBC, &tm_C, 0, row, &full[s]);
+        const int32_t t0 = k * TC, col = (int32_t)d0;
+        tma_load_3d(st, &tm_u, col, t0, b, &full[s]);
+        tma_load_3d(st + Lay::kTileIO, &tm_dl, col, t0, b, &full[s]);
+        if (kGate) tma_load_3d(st + 2 * Lay::kTileIO, &tm_z, col, t0, b, &full[s]);
+        tma_load_3d(st + 3 * Lay::kTileIO, &tm_B, 0, t0, b, &full[s]);
+        tma_load_3d(st + 3 * Lay::kTileIO + Lay::kTileBC, &tm_C, 0, t0, b, &full[s]);
         issued = k + 1;
       }
       // Never leave with loads in flight into this CTA's shared memory.
@@ -149,58 +178,92 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   }
   const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
-  const bool has_D = p.Dskip != nullptr;
-  const bool sp = p.delta_softplus != 0;
-  TY* __restrict__ yout = static_cast<TY*>(p.y) + b * L * D + d;
+  unsigned char* ywarp = ytiles + warp * 2 * Lay::kTileY;  // this warp's two y tiles
 
   for (int k = 0; k < nchunks; ++k) {
     const int s = k % S;
     const uint32_t par = (k / S) & 1;
-    if (!mbar_wait(&ready[s], par, kErrWaitReady)) return;
-    if (!mbar_wait(&full[s], par, kErrWaitFull)) return;
+    if (!mbar_wait(&ready[s], par, kErrWaitReady)) break;
+    if (!mbar_wait(&full[s], par, kErrWaitFull)) break;
     const unsigned char* st = smem + s * Lay::kStage;
     const __nv_bfloat16* su = reinterpret_cast<const __nv_bfloat16*>(st) + j;
     const __nv_bfloat16* sd = reinterpret_cast<const __nv_bfloat16*>(st + Lay::kTileIO) + j;
     const __nv_bfloat16* sz = reinterpret_cast<const __nv_bfloat16*>(st + 2 * Lay::kTileIO) + j;
     const float* bc = reinterpret_cast<const float*>(st + 3 * Lay::kTileIO + 2 * Lay::kTileBC);
     const int tc = (int)((L - (int64_t)k * TC) < TC ? (L - (int64_t)k * TC) : TC);
-    TY* yk = yout + (int64_t)k * TC * D;
-
-#pragma unroll 2
-    for (int t = 0; t < tc; ++t) {
-      const float uu = __bfloat162float(su[t * kChanCTA]);
-      const float r = __bfloat162float(sd[t * kChanCTA]) + bias;
-      const float dt = sp ? softplus_fast(r) : r;
-      const float du = dt * uu;
-      const float2 dt2 = make_float2(dt, dt), du2 = make_float2(du, du);
-      const float4* bc4 = reinterpret_cast<const float4*>(bc + t * 2 * N);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < N / 4; ++q) {
-        const float4 bq = bc4[q];
-        const float4 cq = bc4[N / 4 + q];
-        const float2 x0 = __fmul2_rn(dt2, A2[2 * q]);
-        const float2 x1 = __fmul2_rn(dt2, A2[2 * q + 1]);
-        const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));           // A-bar = exp(dt A)
-        const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
-        const float2 b0 = __fmul2_rn(du2, make_float2(bq.x, bq.y));     // (dt u) B
-        const float2 b1 = __fmul2_rn(du2, make_float2(bq.z, bq.w));
-        h[2 * q] = __ffma2_rn(a0, h[2 * q], b0);                        // h = A-bar h + B-bar u
-        h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], b1);
-        acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q], acc0);    // C . h
-        acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q + 1], acc1);
-      }
-      float v = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      if (has_D) v = fmaf(Dk, uu, v);
-      if (has_z) v *= silu_fast(__bfloat162float(sz[t * kChanCTA]));
-      if (vd) yk[(int64_t)t * D] = from_f32<TY>(v);
+    TY* ytile = reinterpret_cast<TY*>(ywarp + (k & 1) * Lay::kTileY);
+    TY* yt = ytile + lane;
+    // The tile written two chunks ago must have been read out by its TMA store.
+    if (k >= 2) {
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
     }
+
+    // Sub-chunks of kSub steps in three phases, so that one warp per SM sub-partition
+    // finds independent work: (1) step sizes for kSub steps (independent softplus
+    // chains), (2) the recurrence (only h carries from step to step), (3) gate and
+    // stage y. Steps past the end of the sequence get dt = 0 and a zero input (the
+    // tiles are zero-filled there): exp(0) = 1 exactly, so h stays bit-for-bit
+    // unchanged and the loops need no branch.
+    constexpr int kSub = 8;
+    static_assert(TC % kSub == 0, "TC must be a multiple of the sub-chunk");
+    for (int t0 = 0; t0 < tc; t0 += kSub) {
+      float uv[kSub], dtv[kSub], duv[kSub], yv[kSub];
+#pragma unroll
+      for (int i = 0; i < kSub; ++i) {
+        const int t = t0 + i;
+        const float uu = __bfloat162float(su[t * kChanCTA]);
+        const float r = __bfloat162float(sd[t * kChanCTA]) + bias;
+        const float dt = kSoftplus ? softplus_fast(r) : r;
+        uv[i] = uu;
+        dtv[i] = t < tc ? dt : 0.f;
+        duv[i] = t < tc ? dt * uu : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kSub; ++i) {
+        const float2 dt2 = make_float2(dtv[i], dtv[i]), du2 = make_float2(duv[i], duv[i]);
+        const float4* bc4 = reinterpret_cast<const float4*>(bc + (t0 + i) * 2 * N);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+          const float4 bq = bc4[q];
+          const float4 cq = bc4[N / 4 + q];
+          const float2 x0 = __fmul2_rn(dt2, A2[2 * q]);
+          const float2 x1 = __fmul2_rn(dt2, A2[2 * q + 1]);
+          const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));           // A-bar = exp(dt A)
+          const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
+          const float2 b0 = __fmul2_rn(du2, make_float2(bq.x, bq.y));     // (dt u) B
+          const float2 b1 = __fmul2_rn(du2, make_float2(bq.z, bq.w));
+          h[2 * q] = __ffma2_rn(a0, h[2 * q], b0);                        // h = A-bar h + B-bar u
+          h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], b1);
+          acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q], acc0);    // C . h
+          acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q + 1], acc1);
+        }
+        yv[i] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      }
+#pragma unroll
+      for (int i = 0; i < kSub; ++i) {
+        const int t = t0 + i;
+        float v = fmaf(Dk, uv[i], yv[i]);
+        if (kGate) v *= silu_fast(__bfloat162float(sz[t * kChanCTA]));
+        yt[t * 32] = from_f32<TY>(v);
+      }
+    }
+    // Release the input stage, then send this chunk's y tile (rows past L and columns
+    // past D are clipped by the TMA store).
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(&tm_y, ytile, (int32_t)(d0 + warp * 32), k * TC, b);
+      bulk_commit();
+    }
   }
+  if (lane == 0) bulk_wait_all();
 
   if (vd && p.last_state) {
-    float4* ls = reinterpret_cast<float4*>(p.last_state + (b * D + d) * N);
+    float4* ls = reinterpret_cast<float4*>(p.last_state + ((int64_t)b * D + d) * N);
 #pragma unroll
     for (int q = 0; q < N / 4; ++q) ls[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
   }

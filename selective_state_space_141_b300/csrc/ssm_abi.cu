@@ -95,56 +95,74 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix (outer x inner), box (box_outer x box_inner), zero fill outside.
-bool encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                    uint32_t box_outer) {
+// Dense (batch, L, inner) tensor as a 3-D TMA map with box (1, box_l, box_inner); loads
+// zero-fill and stores clip outside the tensor, so a chunk never crosses into the next
+// batch row.
+bool encode_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint64_t esize, uint64_t inner,
+               uint64_t L, uint64_t batch, uint32_t box_inner, uint32_t box_l) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  cuuint64_t dims[3] = {inner, L, batch};
+  cuuint64_t strides[2] = {inner * esize, inner * L * esize};
+  cuuint32_t box[3] = {box_inner, box_l, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned16(const void* p) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 // ---- channel-parallel TMA kernel (bf16 I/O) ----------------------------------------------
-constexpr int kChanTC = 64, kChanStages = 3;
+constexpr int kChanTC = 32, kChanStages = 4;
 
 bool chan_eligible(const FwdParams& p, int64_t N) {
-  // TMA needs 16-byte aligned bases and row pitches (D % 8 == 0 for bf16) and int32 row
-  // coordinates; last_state is written with 16-byte vector stores.
-  return (N == 8 || N == 16) && p.D % 8 == 0 && p.batch * p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
-         aligned16(p.delta) && aligned16(p.z) && aligned16(p.B) && aligned16(p.C) &&
+  // TMA needs 16-byte aligned bases and row pitches (D % 8 == 0 covers bf16 and fp32
+  // y) and int32 coordinates; last_state is written with 16-byte vector stores.
+  return (N == 8 || N == 16) && p.D % 8 == 0 && p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
+         aligned16(p.delta) && aligned16(p.z) && aligned16(p.B) && aligned16(p.C) && aligned16(p.y) &&
          aligned16(p.last_state) && encode_fn() != nullptr;
+}
+
+template <typename TY, int N, bool kSP, bool kZ>
+cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, cudaStream_t st) {
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ>;
+  constexpr int smem = ssm::chan_smem_bytes<TY, N, kChanTC, kChanStages>();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  dim3 grid((unsigned)((p.D + ssm::kChanCTA - 1) / ssm::kChanCTA), (unsigned)p.batch);
+  void* args[] = {const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
+                  const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
+                  const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5]),
+                  const_cast<FwdParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(ssm::kChanThreads), args, smem, st);
 }
 
 template <typename TY, int N>
 cudaError_t launch_chan(const FwdParams& p, cudaStream_t st, bool* launched) {
   *launched = false;
-  const uint64_t rows = (uint64_t)(p.batch * p.L);
-  CUtensorMap mu, md, mz, mb, mc;
-  if (!encode_bf16_2d(&mu, p.u, p.D, rows, ssm::kChanCTA, kChanTC) ||
-      !encode_bf16_2d(&md, p.delta, p.D, rows, ssm::kChanCTA, kChanTC) ||
-      !encode_bf16_2d(&mb, p.B, N, rows, N, kChanTC) || !encode_bf16_2d(&mc, p.C, N, rows, N, kChanTC))
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType ydt = sizeof(TY) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : bf;
+  const uint64_t L = (uint64_t)p.L, Bt = (uint64_t)p.batch, D = (uint64_t)p.D;
+  CUtensorMap maps[6];  // u, delta, z, B, C, y
+  if (!encode_3d(&maps[0], p.u, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[1], p.delta, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[3], p.B, bf, 2, N, L, Bt, N, kChanTC) ||
+      !encode_3d(&maps[4], p.C, bf, 2, N, L, Bt, N, kChanTC) ||
+      !encode_3d(&maps[5], p.y, ydt, sizeof(TY), D, L, Bt, 32, kChanTC))
     return cudaSuccess;
   if (p.z) {
-    if (!encode_bf16_2d(&mz, p.z, p.D, rows, ssm::kChanCTA, kChanTC)) return cudaSuccess;
+    if (!encode_3d(&maps[2], p.z, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC)) return cudaSuccess;
   } else {
-    mz = mu;  // never read when z is absent
+    maps[2] = maps[0];  // never read when there is no gate
   }
-  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages>;
-  constexpr int smem = ssm::chan_smem_bytes<N, kChanTC, kChanStages>();
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (attr != cudaSuccess) return attr;
-  dim3 grid((unsigned)((p.D + ssm::kChanCTA - 1) / ssm::kChanCTA), (unsigned)p.batch);
-  void* args[] = {&mu, &md, &mz, &mb, &mc, const_cast<FwdParams*>(&p)};
   *launched = true;
-  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(ssm::kChanThreads), args, smem, st);
+  const bool sp = p.delta_softplus != 0, z = p.z != nullptr;
+  if (sp && z) return launch_chan_k<TY, N, true, true>(p, maps, st);
+  if (sp) return launch_chan_k<TY, N, true, false>(p, maps, st);
+  if (z) return launch_chan_k<TY, N, false, true>(p, maps, st);
+  return launch_chan_k<TY, N, false, false>(p, maps, st);
 }
 
 template <typename TY>

@@ -91,7 +91,12 @@ LONG = FwdWorkload("long-sequence scan (1x131072x2048, N=16)", 1, 131072, 2048, 
 DECODE = DecodeWorkload("decode step, Mamba-2.8B layer (256x5120, N=16) x1024", 256, 5120, 16, 1024,
                         torch.bfloat16, 4)
 
-FWD_WORKLOADS = {"tiny": TINY, "m130m": M130, "m1p4b": M1P4, "long": LONG}
+# A quarter-length cut of the 1.4B layer (135 MB of inputs, still larger than L2) that
+# profilers can replay quickly.
+M1P4_L1024 = FwdWorkload("Mamba-1.4B layer scan, L cut to 1024 (4x1024x4096, N=16)", 4, 1024, 4096, 16,
+                         torch.bfloat16, True, 2)
+
+FWD_WORKLOADS = {"tiny": TINY, "m130m": M130, "m1p4b": M1P4, "long": LONG, "m1p4b_L1024": M1P4_L1024}
 
 BIAS_LO = math.log(math.expm1(0.001))
 BIAS_HI = math.log(math.expm1(0.1))
