@@ -50,20 +50,21 @@ constexpr int chan_smem_bytes() {
   return S * Lay::kStage + 4 * 2 * Lay::kTileY + 3 * S * 8;
 }
 
-// Softplus for the bf16 path: 2^x and log2 on the SFU; e^r below 2^-10 uses
-// log1p(e) ~ e (1 - e/2), where forming 1 + e would lose the low bits.
-__device__ __forceinline__ float softplus_fast(float r) {
-  const float e = ex2(r * kLog2e);
-  const float lg = lg2(1.f + e) * kLn2;
-  const float small = e * fmaf(-0.5f, e, 1.f);
-  const float v = e < 0.0009765625f ? small : lg;
-  return r > 20.f ? r : v;
+// Softplus of two steps for the bf16 path: max(r, 0) + log1p(e^-|r|), with 2^x and
+// log2 on the SFU and the rest as packed f32x2 ops. Overflow-free for any r; for very
+// negative r the rounding of 1 + e leaves an absolute error near 1e-7 in dt.
+__device__ __forceinline__ float2 softplus2_fast(float2 r) {
+  const float2 e = make_float2(ex2(fabsf(r.x) * -kLog2e), ex2(fabsf(r.y) * -kLog2e));
+  const float2 op = __fadd2_rn(e, make_float2(1.f, 1.f));
+  const float2 lg = make_float2(lg2(op.x), lg2(op.y));
+  return __ffma2_rn(lg, make_float2(kLn2, kLn2), make_float2(fmaxf(r.x, 0.f), fmaxf(r.y, 0.f)));
 }
 
-// SiLU for the bf16 path: z sigmoid(z) = 0.5 z (1 + tanh(z / 2)), one SFU op.
-__device__ __forceinline__ float silu_fast(float z) {
-  const float hz = 0.5f * z;
-  return fmaf(hz, tanh_fast(hz), hz);
+// SiLU of two steps for the bf16 path: z sigmoid(z) = 0.5 z (1 + tanh(z / 2)), one SFU
+// op per value.
+__device__ __forceinline__ float2 silu2_fast(float2 z) {
+  const float2 hz = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+  return __ffma2_rn(hz, make_float2(tanh_fast(hz.x), tanh_fast(hz.y)), hz);
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t c0, int32_t c1,
@@ -87,6 +88,69 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+constexpr int kChanSub = 8;  // steps per sub-chunk
+
+// kChanSub steps of one lane (one channel, all N states), in three phases so that one
+// warp per SM sub-partition finds independent work: (1) step sizes (independent
+// softplus chains, two steps per packed op), (2) the recurrence (only h carries from
+// step to step), (3) D skip, gate and y staging (two steps per packed op).
+// kTail: steps at or past tc get dt = 0 and no input, so exp(0) = 1 exactly leaves h
+// bit-for-bit unchanged (selects, not multiplies; those rows hold zero fill).
+template <typename TY, int N, bool kSoftplus, bool kGate, bool kTail>
+__device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __nv_bfloat16* sd,
+                                              const __nv_bfloat16* sz, const float* bc, TY* yt, int t0, int tc,
+                                              float bias, float Dk, const float2 (&A2)[N / 2], float2 (&h)[N / 2]) {
+  float2 u2[kChanSub / 2], dt2[kChanSub / 2], du2[kChanSub / 2], y2[kChanSub / 2];
+#pragma unroll
+  for (int i = 0; i < kChanSub / 2; ++i) {
+    const int t = t0 + 2 * i;
+    u2[i] = make_float2(__bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
+    const float2 r = __fadd2_rn(make_float2(__bfloat162float(sd[t * kChanCTA]), __bfloat162float(sd[(t + 1) * kChanCTA])),
+                                make_float2(bias, bias));
+    float2 d = kSoftplus ? softplus2_fast(r) : r;
+    if (kTail) d = make_float2(t < tc ? d.x : 0.f, t + 1 < tc ? d.y : 0.f);
+    dt2[i] = d;
+    du2[i] = __fmul2_rn(d, u2[i]);
+    if (kTail) du2[i] = make_float2(t < tc ? du2[i].x : 0.f, t + 1 < tc ? du2[i].y : 0.f);
+  }
+  float yv[kChanSub];
+#pragma unroll
+  for (int i = 0; i < kChanSub; ++i) {
+    const float dts = (i & 1) ? dt2[i / 2].y : dt2[i / 2].x;
+    const float dus = (i & 1) ? du2[i / 2].y : du2[i / 2].x;
+    const float2 dtp = make_float2(dts, dts), dup = make_float2(dus, dus);
+    const float4* bc4 = reinterpret_cast<const float4*>(bc + (t0 + i) * 2 * N);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 bq = bc4[q];
+      const float4 cq = bc4[N / 4 + q];
+      const float2 x0 = __fmul2_rn(dtp, A2[2 * q]);
+      const float2 x1 = __fmul2_rn(dtp, A2[2 * q + 1]);
+      const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));           // A-bar = exp(dt A)
+      const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
+      const float2 b0 = __fmul2_rn(dup, make_float2(bq.x, bq.y));     // (dt u) B
+      const float2 b1 = __fmul2_rn(dup, make_float2(bq.z, bq.w));
+      h[2 * q] = __ffma2_rn(a0, h[2 * q], b0);                        // h = A-bar h + B-bar u
+      h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], b1);
+      acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q], acc0);    // C . h
+      acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q + 1], acc1);
+    }
+    const float2 acc = __fadd2_rn(acc0, acc1);
+    yv[i] = acc.x + acc.y;
+  }
+#pragma unroll
+  for (int i = 0; i < kChanSub / 2; ++i) {
+    const int t = t0 + 2 * i;
+    y2[i] = __ffma2_rn(make_float2(Dk, Dk), u2[i], make_float2(yv[2 * i], yv[2 * i + 1]));
+    if (kGate)
+      y2[i] = __fmul2_rn(y2[i], silu2_fast(make_float2(__bfloat162float(sz[t * kChanCTA]),
+                                                      __bfloat162float(sz[(t + 1) * kChanCTA]))));
+    yt[t * 32] = from_f32<TY>(y2[i].x);
+    yt[(t + 1) * 32] = from_f32<TY>(y2[i].y);
+  }
+}
 
 template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate>
 __global__ void __launch_bounds__(kChanThreads, 1)
@@ -199,55 +263,12 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       __syncwarp();
     }
 
-    // Sub-chunks of kSub steps in three phases, so that one warp per SM sub-partition
-    // finds independent work: (1) step sizes for kSub steps (independent softplus
-    // chains), (2) the recurrence (only h carries from step to step), (3) gate and
-    // stage y. Steps past the end of the sequence get dt = 0 and a zero input (the
-    // tiles are zero-filled there): exp(0) = 1 exactly, so h stays bit-for-bit
-    // unchanged and the loops need no branch.
-    constexpr int kSub = 8;
-    static_assert(TC % kSub == 0, "TC must be a multiple of the sub-chunk");
-    for (int t0 = 0; t0 < tc; t0 += kSub) {
-      float uv[kSub], dtv[kSub], duv[kSub], yv[kSub];
-#pragma unroll
-      for (int i = 0; i < kSub; ++i) {
-        const int t = t0 + i;
-        const float uu = __bfloat162float(su[t * kChanCTA]);
-        const float r = __bfloat162float(sd[t * kChanCTA]) + bias;
-        const float dt = kSoftplus ? softplus_fast(r) : r;
-        uv[i] = uu;
-        dtv[i] = t < tc ? dt : 0.f;
-        duv[i] = t < tc ? dt * uu : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kSub; ++i) {
-        const float2 dt2 = make_float2(dtv[i], dtv[i]), du2 = make_float2(duv[i], duv[i]);
-        const float4* bc4 = reinterpret_cast<const float4*>(bc + (t0 + i) * 2 * N);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < N / 4; ++q) {
-          const float4 bq = bc4[q];
-          const float4 cq = bc4[N / 4 + q];
-          const float2 x0 = __fmul2_rn(dt2, A2[2 * q]);
-          const float2 x1 = __fmul2_rn(dt2, A2[2 * q + 1]);
-          const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));           // A-bar = exp(dt A)
-          const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
-          const float2 b0 = __fmul2_rn(du2, make_float2(bq.x, bq.y));     // (dt u) B
-          const float2 b1 = __fmul2_rn(du2, make_float2(bq.z, bq.w));
-          h[2 * q] = __ffma2_rn(a0, h[2 * q], b0);                        // h = A-bar h + B-bar u
-          h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], b1);
-          acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q], acc0);    // C . h
-          acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q + 1], acc1);
-        }
-        yv[i] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      }
-#pragma unroll
-      for (int i = 0; i < kSub; ++i) {
-        const int t = t0 + i;
-        float v = fmaf(Dk, uv[i], yv[i]);
-        if (kGate) v *= silu_fast(__bfloat162float(sz[t * kChanCTA]));
-        yt[t * 32] = from_f32<TY>(v);
-      }
+    if (tc == TC) {
+      for (int t0 = 0; t0 < TC; t0 += kChanSub)
+        chan_subchunk<TY, N, kSoftplus, kGate, false>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
+    } else {
+      for (int t0 = 0; t0 < tc; t0 += kChanSub)
+        chan_subchunk<TY, N, kSoftplus, kGate, true>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
     }
     // Release the input stage, then send this chunk's y tile (rows past L and columns
     // past D are clipped by the TMA store).
