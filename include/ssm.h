@@ -102,6 +102,40 @@ SSM_API ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_ten
                                     ssm_tensor_t* last_state, void* stream);
 
 /*
+ * ssm_selective_scan_fwd_workspace_size -- bytes of device workspace that
+ * ssm_selective_scan_fwd_ws can use for a problem of this shape (0: none needed).
+ * A workspace lets shapes with few channels and a long sequence (for example one
+ * sequence of 131072 steps over 2048 channels) cut the sequence into segments that run
+ * in parallel: a first pass computes each segment's end state from zero and its decay
+ * product exp(A * sum of dt), an associative scan over segments with the operator
+ * (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) gives every segment its start state
+ * ("8.7 State Space Models (Mamba)", section 4.1; "Mamba and State Space Models",
+ * "Hardware-Aware Parallel Scan"), and a second pass produces y. The answer depends only
+ * on the shape and the current device. Returns SSM_OK, SSM_ERR_NULL (bytes == NULL) or
+ * SSM_ERR_SHAPE (negative sizes).
+ */
+SSM_API ssm_status_t ssm_selective_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N,
+                                                          size_t* bytes);
+
+/*
+ * ssm_selective_scan_fwd_ws -- ssm_selective_scan_fwd with a caller-owned device
+ * workspace (16-byte aligned, workspace_bytes long, not overlapping any tensor of the
+ * call). The result is the same computation; with at least the size reported by
+ * ssm_selective_scan_fwd_workspace_size the library may use the segmented schedule
+ * described there. A smaller (or NULL, 0) workspace falls back to the unsegmented
+ * kernels. The workspace contents are scratch: overwritten, not read before written.
+ * Errors as ssm_selective_scan_fwd, plus SSM_ERR_NULL (bytes > 0 with NULL) and
+ * SSM_ERR_LAYOUT (misaligned or overlapping workspace).
+ */
+SSM_API ssm_status_t ssm_selective_scan_fwd_ws(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                               const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                               const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                               const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                               int delta_softplus, ssm_tensor_t* y,
+                                               ssm_tensor_t* last_state, void* workspace,
+                                               size_t workspace_bytes, void* stream);
+
+/*
  * ssm_state_update -- one recurrent decode step, state updated in place.
  *
  * For each batch row b and channel d:

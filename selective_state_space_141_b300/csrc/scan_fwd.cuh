@@ -30,6 +30,14 @@ struct FwdParams {
   void* y;
   float* last_state;        // nullable
   int64_t batch, L, D;
+  // Sequence segments (channel kernel only): CTA z covers steps [z*seg_len, (z+1)*seg_len).
+  // seg_len == L means one segment. seg_h0 (nullable): start state of each segment,
+  // laid out [segment][batch][D][N]. seg_E / seg_P: outputs of the aggregate pass, same
+  // layout: end state from a zero start and the decay product exp(A * sum of dt).
+  int64_t seg_len;
+  const float* seg_h0;
+  float* seg_E;
+  float* seg_P;
 };
 
 // ------------------------------------------------------------------------------------

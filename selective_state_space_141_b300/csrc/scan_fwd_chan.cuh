@@ -152,13 +152,57 @@ __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __n
   }
 }
 
-template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate>
+// Aggregate pass over kChanSub steps: the recurrence from the given state without the
+// read-out (no C, no y), plus the running sum of dt, from which the decay product of a
+// whole segment is exp(A * sum dt). Same tail rule as chan_subchunk.
+template <int N, bool kSoftplus, bool kTail>
+__device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const __nv_bfloat16* sd, const float* bc,
+                                                  int t0, int tc, float bias, const float2 (&A2)[N / 2],
+                                                  float2 (&h)[N / 2], float& sdt) {
+  float2 dt2[kChanSub / 2], du2[kChanSub / 2];
+#pragma unroll
+  for (int i = 0; i < kChanSub / 2; ++i) {
+    const int t = t0 + 2 * i;
+    const float2 u2 = make_float2(__bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
+    const float2 r = __fadd2_rn(make_float2(__bfloat162float(sd[t * kChanCTA]), __bfloat162float(sd[(t + 1) * kChanCTA])),
+                                make_float2(bias, bias));
+    float2 d = kSoftplus ? softplus2_fast(r) : r;
+    if (kTail) d = make_float2(t < tc ? d.x : 0.f, t + 1 < tc ? d.y : 0.f);
+    dt2[i] = d;
+    du2[i] = __fmul2_rn(d, u2);
+    if (kTail) du2[i] = make_float2(t < tc ? du2[i].x : 0.f, t + 1 < tc ? du2[i].y : 0.f);
+    sdt += d.x + d.y;
+  }
+#pragma unroll
+  for (int i = 0; i < kChanSub; ++i) {
+    const float dts = (i & 1) ? dt2[i / 2].y : dt2[i / 2].x;
+    const float dus = (i & 1) ? du2[i / 2].y : du2[i / 2].x;
+    const float2 dtp = make_float2(dts, dts), dup = make_float2(dus, dus);
+    const float4* b4 = reinterpret_cast<const float4*>(bc + (t0 + i) * 2 * N);
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 bq = b4[q];
+      const float2 x0 = __fmul2_rn(dtp, A2[2 * q]);
+      const float2 x1 = __fmul2_rn(dtp, A2[2 * q + 1]);
+      const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));
+      const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
+      h[2 * q] = __ffma2_rn(a0, h[2 * q], __fmul2_rn(dup, make_float2(bq.x, bq.y)));
+      h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], __fmul2_rn(dup, make_float2(bq.z, bq.w)));
+    }
+  }
+}
+
+// kAgg = false: the full pass (y, and last_state from the last segment).
+// kAgg = true:  the aggregate pass of a segmented scan (seg_E, seg_P; no y).
+// blockIdx = (channel block of 128, batch row, sequence segment).
+template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg>
 __global__ void __launch_bounds__(kChanThreads, 1)
 scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
               const FwdParams p) {
   using Lay = ChanLayout<TY, N, TC>;
+  constexpr bool kZ = kGate && !kAgg;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ytiles = smem + S * Lay::kStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(ytiles + 4 * 2 * Lay::kTileY);
@@ -167,9 +211,12 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t b = (int32_t)blockIdx.y;
+  const int seg = (int)blockIdx.z;
   const int64_t d0 = (int64_t)blockIdx.x * kChanCTA;
   const int64_t L = p.L, D = p.D;
-  const int nchunks = (int)((L + TC - 1) / TC);
+  const int64_t t_begin = (int64_t)seg * p.seg_len;
+  const int64_t t_end = (t_begin + p.seg_len) < L ? (t_begin + p.seg_len) : L;
+  const int nchunks = (int)((t_end - t_begin + TC - 1) / TC);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -185,22 +232,22 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     if (lane == 0) {
       prefetch_tensormap(&tm_u);
       prefetch_tensormap(&tm_dl);
-      if (kGate) prefetch_tensormap(&tm_z);
+      if (kZ) prefetch_tensormap(&tm_z);
       prefetch_tensormap(&tm_B);
-      prefetch_tensormap(&tm_C);
-      constexpr uint32_t tx = (kGate ? 3 : 2) * Lay::kTileIO + 2 * Lay::kTileBC;
+      if (!kAgg) prefetch_tensormap(&tm_C);
+      constexpr uint32_t tx = (kZ ? 3 : 2) * Lay::kTileIO + (kAgg ? 1 : 2) * Lay::kTileBC;
       int issued = 0;
       for (int k = 0; k < nchunks; ++k) {
         const int s = k % S;
         if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, kErrWaitEmpty)) break;
         unsigned char* st = smem + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], tx);
-        const int32_t t0 = k * TC, col = (int32_t)d0;
+        const int32_t t0 = (int32_t)(t_begin + (int64_t)k * TC), col = (int32_t)d0;
         tma_load_3d(st, &tm_u, col, t0, b, &full[s]);
         tma_load_3d(st + Lay::kTileIO, &tm_dl, col, t0, b, &full[s]);
-        if (kGate) tma_load_3d(st + 2 * Lay::kTileIO, &tm_z, col, t0, b, &full[s]);
+        if (kZ) tma_load_3d(st + 2 * Lay::kTileIO, &tm_z, col, t0, b, &full[s]);
         tma_load_3d(st + 3 * Lay::kTileIO, &tm_B, 0, t0, b, &full[s]);
-        tma_load_3d(st + 3 * Lay::kTileIO + Lay::kTileBC, &tm_C, 0, t0, b, &full[s]);
+        if (!kAgg) tma_load_3d(st + 3 * Lay::kTileIO + Lay::kTileBC, &tm_C, 0, t0, b, &full[s]);
         issued = k + 1;
       }
       // Never leave with loads in flight into this CTA's shared memory.
@@ -218,11 +265,15 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       const __nv_bfloat16* Bt = reinterpret_cast<const __nv_bfloat16*>(st + 3 * Lay::kTileIO);
       const __nv_bfloat16* Ct = reinterpret_cast<const __nv_bfloat16*>(st + 3 * Lay::kTileIO + Lay::kTileBC);
       float* bc = reinterpret_cast<float*>(smem + s * Lay::kStage + 3 * Lay::kTileIO + 2 * Lay::kTileBC);
+      // Rows past this segment's end become exact zeros (they may hold the next
+      // segment's data), so padded steps add nothing even for non-finite inputs there.
+      const int64_t tk = t_begin + (int64_t)k * TC;
+      const int tc = (int)((t_end - tk) < TC ? (t_end - tk) : TC);
 #pragma unroll 4
       for (int i = lane; i < TC * N; i += 32) {
         const int t = i / N, n = i % N;
-        bc[t * 2 * N + n] = __bfloat162float(Bt[i]);
-        bc[t * 2 * N + N + n] = __bfloat162float(Ct[i]);
+        bc[t * 2 * N + n] = t < tc ? __bfloat162float(Bt[i]) : 0.f;
+        if (!kAgg) bc[t * 2 * N + N + n] = t < tc ? __bfloat162float(Ct[i]) : 0.f;
       }
       mbar_arrive(&ready[s]);
     }
@@ -233,16 +284,19 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   const int j = warp * 32 + lane;
   const int64_t d = d0 + j;
   const bool vd = d < D;
+  const int64_t sidx = (((int64_t)seg * p.batch + b) * D + d) * N;  // [segment][batch][D][N]
   float2 A2[N / 2], h[N / 2];
 #pragma unroll
   for (int q = 0; q < N / 2; ++q) {
     A2[q] = vd ? make_float2(p.A[d * N + 2 * q] * kLog2e, p.A[d * N + 2 * q + 1] * kLog2e)
                : make_float2(0.f, 0.f);
-    h[q] = make_float2(0.f, 0.f);
+    h[q] = (vd && p.seg_h0) ? make_float2(p.seg_h0[sidx + 2 * q], p.seg_h0[sidx + 2 * q + 1])
+                            : make_float2(0.f, 0.f);
   }
   const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
   unsigned char* ywarp = ytiles + warp * 2 * Lay::kTileY;  // this warp's two y tiles
+  float sdt = 0.f;
 
   for (int k = 0; k < nchunks; ++k) {
     const int s = k % S;
@@ -254,7 +308,18 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     const __nv_bfloat16* sd = reinterpret_cast<const __nv_bfloat16*>(st + Lay::kTileIO) + j;
     const __nv_bfloat16* sz = reinterpret_cast<const __nv_bfloat16*>(st + 2 * Lay::kTileIO) + j;
     const float* bc = reinterpret_cast<const float*>(st + 3 * Lay::kTileIO + 2 * Lay::kTileBC);
-    const int tc = (int)((L - (int64_t)k * TC) < TC ? (L - (int64_t)k * TC) : TC);
+    const int64_t tk = t_begin + (int64_t)k * TC;
+    const int tc = (int)((t_end - tk) < TC ? (t_end - tk) : TC);
+    if (kAgg) {
+      if (tc == TC) {
+        for (int t0 = 0; t0 < TC; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, false>(su, sd, bc, t0, tc, bias, A2, h, sdt);
+      } else {
+        for (int t0 = 0; t0 < tc; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, true>(su, sd, bc, t0, tc, bias, A2, h, sdt);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      continue;
+    }
     TY* ytile = reinterpret_cast<TY*>(ywarp + (k & 1) * Lay::kTileY);
     TY* yt = ytile + lane;
     // The tile written two chunks ago must have been read out by its TMA store.
@@ -262,7 +327,6 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       if (lane == 0) bulk_wait_read<1>();
       __syncwarp();
     }
-
     if (tc == TC) {
       for (int t0 = 0; t0 < TC; t0 += kChanSub)
         chan_subchunk<TY, N, kSoftplus, kGate, false>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
@@ -271,23 +335,67 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         chan_subchunk<TY, N, kSoftplus, kGate, true>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
     }
     // Release the input stage, then send this chunk's y tile (rows past L and columns
-    // past D are clipped by the TMA store).
+    // past D are clipped by the TMA store; segments start on chunk boundaries).
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     fence_async_shared();
     __syncwarp();
     if (lane == 0) {
-      tma_store_3d(&tm_y, ytile, (int32_t)(d0 + warp * 32), k * TC, b);
+      tma_store_3d(&tm_y, ytile, (int32_t)(d0 + warp * 32), (int32_t)tk, b);
       bulk_commit();
     }
   }
+
+  if (kAgg) {
+    if (vd) {
+      float4* e4 = reinterpret_cast<float4*>(p.seg_E + sidx);
+      float4* p4 = reinterpret_cast<float4*>(p.seg_P + sidx);
+#pragma unroll
+      for (int q = 0; q < N / 4; ++q) {
+        e4[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
+        p4[q] = make_float4(ex2(A2[2 * q].x * sdt), ex2(A2[2 * q].y * sdt), ex2(A2[2 * q + 1].x * sdt),
+                            ex2(A2[2 * q + 1].y * sdt));
+      }
+    }
+    return;
+  }
   if (lane == 0) bulk_wait_all();
 
-  if (vd && p.last_state) {
+  if (vd && p.last_state && seg == (int)gridDim.z - 1) {
     float4* ls = reinterpret_cast<float4*>(p.last_state + ((int64_t)b * D + d) * N);
 #pragma unroll
     for (int q = 0; q < N / 4; ++q) ls[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
   }
+}
+
+// Carry between sequence segments: for every (batch, channel, state) the segment
+// aggregates (P_s, E_s) are pairs of the recurrence h -> P h + E, combined in time order
+// by (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2). One warp per (batch, channel, state),
+// lane s holding segment s - 1 (lane 0 the identity), runs an inclusive Hillis-Steele
+// scan with __shfl_up_sync; lane s then holds the state at the start of segment s.
+// ("8.7 State Space Models (Mamba)", section 4.1 and "Mamba and State Space Models",
+// "Hardware-Aware Parallel Scan": the recurrence is an associative scan.)
+// Requires nseg <= 32. Layout of E, P, H: [segment][batch * D * N].
+__global__ void __launch_bounds__(256) seg_carry_kernel(const float* __restrict__ E, const float* __restrict__ P,
+                                                       float* __restrict__ H, int nseg, int64_t nbdn) {
+  const int64_t idx = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (idx >= nbdn) return;  // whole warps leave together
+  float a = 1.f, c = 0.f;
+  if (lane >= 1 && lane < nseg) {
+    a = P[(int64_t)(lane - 1) * nbdn + idx];
+    c = E[(int64_t)(lane - 1) * nbdn + idx];
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a_up = __shfl_up_sync(0xffffffffu, a, off);
+    const float c_up = __shfl_up_sync(0xffffffffu, c, off);
+    if (lane >= off) {  // (a_up, c_up) o (a, c)
+      c = fmaf(a, c_up, c);
+      a = a * a_up;
+    }
+  }
+  if (lane < nseg) H[(int64_t)lane * nbdn + idx] = c;
 }
 
 }  // namespace ssm

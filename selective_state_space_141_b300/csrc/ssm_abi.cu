@@ -124,14 +124,14 @@ bool chan_eligible(const FwdParams& p, int64_t N) {
          aligned16(p.last_state) && encode_fn() != nullptr;
 }
 
-template <typename TY, int N, bool kSP, bool kZ>
-cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ>;
+template <typename TY, int N, bool kSP, bool kZ, bool kAgg>
+cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st) {
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg>;
   constexpr int smem = ssm::chan_smem_bytes<TY, N, kChanTC, kChanStages>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (attr != cudaSuccess) return attr;
-  dim3 grid((unsigned)((p.D + ssm::kChanCTA - 1) / ssm::kChanCTA), (unsigned)p.batch);
+  dim3 grid((unsigned)((p.D + ssm::kChanCTA - 1) / ssm::kChanCTA), (unsigned)p.batch, (unsigned)nseg);
   void* args[] = {const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
                   const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
                   const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5]),
@@ -139,36 +139,98 @@ cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, cudaStrea
   return cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(ssm::kChanThreads), args, smem, st);
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+// Sequence segmentation for shapes with too few channel blocks to occupy the GPU: the
+// long sequence is cut into nseg segments of seg_len steps (a multiple of the chunk),
+// each processed by its own CTAs; the workspace holds E, P and H ([nseg][batch][D][N]
+// fp32 each).
+struct SegPlan {
+  int nseg = 1;
+  int64_t seg_len = 0;
+  size_t bytes = 0;
+};
+SegPlan plan_segments(int64_t batch, int64_t L, int64_t D, int64_t N) {
+  SegPlan sp;
+  sp.seg_len = L;
+  const int sms = num_sms();
+  const int64_t ctas = ((D + ssm::kChanCTA - 1) / ssm::kChanCTA) * batch;
+  if (sms <= 0 || ctas <= 0 || ctas * 2 > sms) return sp;
+  int64_t nseg = sms / ctas;
+  if (nseg > 32) nseg = 32;  // one warp scans the segment carries
+  if (nseg < 2) return sp;
+  const int64_t len = ((L + nseg - 1) / nseg + kChanTC - 1) / kChanTC * kChanTC;
+  if (len < 8 * kChanTC) return sp;  // too short to pay for the aggregate pass
+  nseg = (L + len - 1) / len;
+  if (nseg < 2) return sp;
+  sp.nseg = (int)nseg;
+  sp.seg_len = len;
+  sp.bytes = (size_t)3 * nseg * batch * D * N * sizeof(float);
+  return sp;
+}
+
 template <typename TY, int N>
-cudaError_t launch_chan(const FwdParams& p, cudaStream_t st, bool* launched) {
+cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cudaStream_t st, bool* launched) {
   *launched = false;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapDataType ydt = sizeof(TY) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : bf;
-  const uint64_t L = (uint64_t)p.L, Bt = (uint64_t)p.batch, D = (uint64_t)p.D;
+  const uint64_t L = (uint64_t)p0.L, Bt = (uint64_t)p0.batch, D = (uint64_t)p0.D;
   CUtensorMap maps[6];  // u, delta, z, B, C, y
-  if (!encode_3d(&maps[0], p.u, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
-      !encode_3d(&maps[1], p.delta, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
-      !encode_3d(&maps[3], p.B, bf, 2, N, L, Bt, N, kChanTC) ||
-      !encode_3d(&maps[4], p.C, bf, 2, N, L, Bt, N, kChanTC) ||
-      !encode_3d(&maps[5], p.y, ydt, sizeof(TY), D, L, Bt, 32, kChanTC))
+  if (!encode_3d(&maps[0], p0.u, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[1], p0.delta, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[3], p0.B, bf, 2, N, L, Bt, N, kChanTC) ||
+      !encode_3d(&maps[4], p0.C, bf, 2, N, L, Bt, N, kChanTC) ||
+      !encode_3d(&maps[5], p0.y, ydt, sizeof(TY), D, L, Bt, 32, kChanTC))
     return cudaSuccess;
-  if (p.z) {
-    if (!encode_3d(&maps[2], p.z, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC)) return cudaSuccess;
+  if (p0.z) {
+    if (!encode_3d(&maps[2], p0.z, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC)) return cudaSuccess;
   } else {
     maps[2] = maps[0];  // never read when there is no gate
   }
   *launched = true;
-  const bool sp = p.delta_softplus != 0, z = p.z != nullptr;
-  if (sp && z) return launch_chan_k<TY, N, true, true>(p, maps, st);
-  if (sp) return launch_chan_k<TY, N, true, false>(p, maps, st);
-  if (z) return launch_chan_k<TY, N, false, true>(p, maps, st);
-  return launch_chan_k<TY, N, false, false>(p, maps, st);
+  const bool sp = p0.delta_softplus != 0, z = p0.z != nullptr;
+  FwdParams p = p0;
+  p.seg_len = p0.L;
+  p.seg_h0 = nullptr;
+  p.seg_E = p.seg_P = nullptr;
+  int nseg = 1;
+  if (plan.nseg > 1 && ws) {
+    // 1) aggregate pass over segments 0 .. nseg-2; 2) carry scan; 3) full pass.
+    const int64_t stride = (int64_t)plan.nseg * p0.batch * p0.D * N;
+    float* E = static_cast<float*>(ws);
+    float* P = E + stride;
+    float* H = P + stride;
+    nseg = plan.nseg;
+    p.seg_len = plan.seg_len;
+    p.seg_E = E;
+    p.seg_P = P;
+    cudaError_t e = sp ? launch_chan_k<__nv_bfloat16, N, true, false, true>(p, maps, nseg - 1, st)
+                       : launch_chan_k<__nv_bfloat16, N, false, false, true>(p, maps, nseg - 1, st);
+    if (e != cudaSuccess) return e;
+    const int64_t nbdn = p0.batch * p0.D * N;
+    void* cargs[] = {&E, &P, &H, &nseg, const_cast<int64_t*>(&nbdn)};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_kernel), dim3((unsigned)((nbdn + 7) / 8)),
+                         dim3(256), cargs, 0, st);
+    if (e != cudaSuccess) return e;
+    p.seg_h0 = H;
+    p.seg_E = p.seg_P = nullptr;
+  }
+  if (sp && z) return launch_chan_k<TY, N, true, true, false>(p, maps, nseg, st);
+  if (sp) return launch_chan_k<TY, N, true, false, false>(p, maps, nseg, st);
+  if (z) return launch_chan_k<TY, N, false, true, false>(p, maps, nseg, st);
+  return launch_chan_k<TY, N, false, false, false>(p, maps, nseg, st);
 }
 
 template <typename TY>
-cudaError_t launch_chan_n(int64_t N, const FwdParams& p, cudaStream_t st, bool* launched) {
-  if (N == 8) return launch_chan<TY, 8>(p, st, launched);
-  return launch_chan<TY, 16>(p, st, launched);
+cudaError_t launch_chan_n(int64_t N, const FwdParams& p, const SegPlan& plan, void* ws, cudaStream_t st,
+                          bool* launched) {
+  if (N == 8) return launch_chan<TY, 8>(p, plan, ws, st, launched);
+  return launch_chan<TY, 16>(p, plan, ws, st, launched);
 }
 
 // ---- generic forward launch ------------------------------------------------------------
@@ -228,10 +290,14 @@ const char* ssm_status_string(ssm_status_t s) {
   return "SSM_ERR_UNKNOWN";
 }
 
-ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
-                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
-                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
-                                    ssm_tensor_t* y, ssm_tensor_t* last_state, void* stream) {
+}  // extern "C"
+
+namespace {
+
+ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
+                      const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
+                      const ssm_tensor_t* delta_bias, int delta_softplus, ssm_tensor_t* y, ssm_tensor_t* last_state,
+                      void* workspace, size_t workspace_bytes, void* stream) {
   if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
   const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
@@ -264,6 +330,16 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
     if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
   }
   if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
+  if (workspace && workspace_bytes > 0) {
+    ssm_tensor_t w{};
+    w.data = workspace;
+    w.dtype = SSM_F32;
+    w.ndim = 1;
+    w.shape[0] = (int64_t)(workspace_bytes / 4);
+    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state};
+    for (const ssm_tensor_t* t : all)
+      if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (batch == 0 || Dm == 0) return SSM_OK;
@@ -289,12 +365,20 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   p.L = L;
   p.D = Dm;
 
+  p.seg_len = L;
+  p.seg_h0 = nullptr;
+  p.seg_E = p.seg_P = nullptr;
+
   cudaError_t e;
   const FwdVariant var = forward_variant();
   if (io == SSM_BF16 && var != FwdVariant::kGeneric && chan_eligible(p, N)) {
+    SegPlan plan = plan_segments(batch, L, Dm, N);
+    const bool use_ws = plan.nseg > 1 && workspace && workspace_bytes >= plan.bytes &&
+                        reinterpret_cast<uintptr_t>(workspace) % 16 == 0;
+    if (!use_ws) plan = SegPlan{1, L, 0};
     bool launched = false;
-    e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, st, &launched)
-                             : launch_chan_n<float>(N, p, st, &launched);
+    e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, plan, use_ws ? workspace : nullptr, st, &launched)
+                             : launch_chan_n<float>(N, p, plan, use_ws ? workspace : nullptr, st, &launched);
     if (launched || e != cudaSuccess) return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
   }
   if (io == SSM_F32)
@@ -304,6 +388,37 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   else
     e = launch_fwd_n<__nv_bfloat16, float>(N, p, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                    ssm_tensor_t* y, ssm_tensor_t* last_state, void* stream) {
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, nullptr, 0, stream);
+}
+
+ssm_status_t ssm_selective_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N, size_t* bytes) {
+  if (!bytes) return SSM_ERR_NULL;
+  if (batch < 0 || L < 0 || D < 0 || N < 0) return SSM_ERR_SHAPE;
+  *bytes = 0;
+  if (batch == 0 || L == 0 || D == 0 || !n_supported(N)) return SSM_OK;
+  *bytes = plan_segments(batch, L, D, N).bytes;
+  return SSM_OK;
+}
+
+ssm_status_t ssm_selective_scan_fwd_ws(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                       const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                       const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                       ssm_tensor_t* y, ssm_tensor_t* last_state, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (workspace_bytes > 0 && !workspace) return SSM_ERR_NULL;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SSM_ERR_LAYOUT;
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace, workspace_bytes,
+                  stream);
 }
 
 ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta,

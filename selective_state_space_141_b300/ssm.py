@@ -53,6 +53,11 @@ def load_library(path: str | None = None):
     lib = ctypes.CDLL(path)
     lib.ssm_selective_scan_fwd.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P, ctypes.c_void_p]
+    lib.ssm_selective_scan_fwd_ws.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_ws.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P, ctypes.c_void_p, ctypes.c_size_t,
+                                                          ctypes.c_void_p]
+    lib.ssm_selective_scan_fwd_workspace_size.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = [_P] * 9 + [ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -93,13 +98,28 @@ def _stream(stream):
     return ctypes.c_void_p(int(stream))
 
 
+def workspace_size(batch, L, D, N) -> int:
+    """Bytes of workspace ``ssm_selective_scan_fwd_ws`` can use for this shape (0: none)."""
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.ssm_selective_scan_fwd_workspace_size(int(batch), int(L), int(D), int(N), ctypes.byref(n))
+    if st != 0:
+        raise SsmError(st, "ssm_selective_scan_fwd_workspace_size")
+    return int(n.value)
+
+
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, y=None,
-                       last_state=None, return_last_state=True, y_dtype=None, stream=None):
-    """Fused selective-scan forward pass (``ssm_selective_scan_fwd``).
+                       last_state=None, return_last_state=True, y_dtype=None, stream=None, workspace=None,
+                       use_workspace=True):
+    """Fused selective-scan forward pass.
 
     u, delta, z: (batch, L, D); A: (D, N) fp32; B, C: (batch, L, N); D, delta_bias: (D) fp32.
     Outputs are allocated with torch on u's device unless given. Returns (y, last_state);
     last_state is None when ``return_last_state`` is False and none was passed.
+    With ``use_workspace`` (default) the call goes through ``ssm_selective_scan_fwd_ws``
+    with a workspace of ``workspace_size(...)`` bytes (allocated here with torch unless
+    given), which lets long sequences over few channels run as parallel segments;
+    ``use_workspace=False`` calls ``ssm_selective_scan_fwd``.
     """
     lib = load_library()
     if y is None:
@@ -107,10 +127,23 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     if last_state is None and return_last_state:
         last_state = torch.empty((u.shape[0], u.shape[2], A.shape[-1]), dtype=torch.float32, device=u.device)
     ds = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias, y, last_state)]
-    st = lib.ssm_selective_scan_fwd(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
-                                    _ref(ds[9]), _stream(stream))
+    if not use_workspace:
+        st = lib.ssm_selective_scan_fwd(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
+                                        _ref(ds[9]), _stream(stream))
+        if st != 0:
+            raise SsmError(st, "ssm_selective_scan_fwd")
+        return y, last_state
+    if workspace is None:
+        nbytes = workspace_size(u.shape[0], u.shape[1], u.shape[2], A.shape[-1])
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
+    st = lib.ssm_selective_scan_fwd_ws(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
+                                       _ref(ds[9]), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes),
+                                       _stream(stream))
     if st != 0:
-        raise SsmError(st, "ssm_selective_scan_fwd")
+        raise SsmError(st, "ssm_selective_scan_fwd_ws")
     return y, last_state
 
 

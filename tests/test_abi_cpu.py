@@ -167,3 +167,23 @@ def test_binding_refuses_noncontiguous():
     t = torch.zeros(4, 6)[:, ::2]
     with pytest.raises(ssm.SsmError):
         ssm.describe(t)
+
+
+def test_workspace_size_validation(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.ssm_selective_scan_fwd_workspace_size(1, 10, 8, 16, None) == 1
+    assert lib.ssm_selective_scan_fwd_workspace_size(-1, 10, 8, 16, ctypes.byref(n)) == 2
+    assert lib.ssm_selective_scan_fwd_workspace_size(0, 10, 8, 16, ctypes.byref(n)) == 0 and n.value == 0
+
+
+def test_fwd_ws_validation(lib):
+    a = fwd_args()
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    args = [r(k) for k in ("u", "delta", "A", "B", "C", "D", "z", "bias")]
+    # bytes > 0 with a NULL workspace; then a misaligned workspace
+    assert lib.ssm_selective_scan_fwd_ws(*args, 1, r("y"), r("last"), None, ctypes.c_size_t(64), None) == 1
+    assert lib.ssm_selective_scan_fwd_ws(*args, 1, r("y"), r("last"), ctypes.c_void_p(FAKE + 8),
+                                         ctypes.c_size_t(64), None) == 4
+    # a workspace overlapping u
+    assert lib.ssm_selective_scan_fwd_ws(*args, 1, r("y"), r("last"), ctypes.c_void_p(a["u"].data),
+                                         ctypes.c_size_t(64), None) == 4

@@ -231,3 +231,35 @@ def test_chan_optional_inputs(flags, monkeypatch):
     y, last = gpu_fwd(d, y_dtype=torch.float32)
     check(y, yr, TOL_BF16, False, "y")
     check(last, sr, TOL_BF16, False, "last")
+
+
+# ---- the segmented schedule (long sequences over few channels) --------------------------
+
+SEG_SHAPES = [(1, 20000, 256, 16), (1, 10007, 136, 16), (2, 9000, 128, 8)]
+
+
+@pytest.mark.parametrize("shape", SEG_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_segmented_vs_oracle(shape):
+    b, L, D, N = shape
+    assert ssm.workspace_size(b, L, D, N) > 0, "shape expected to use the segmented schedule"
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=torch.bfloat16, seed=200 + sum(shape)))
+    yr, sr = oracle_fwd(d)
+    y, last = gpu_fwd(d, y_dtype=torch.float32)
+    check(y, yr, TOL_BF16, False, "segmented y")
+    check(last, sr, TOL_BF16, False, "segmented last_state")
+    y0, last0 = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                       delta_bias=d["delta_bias"], y_dtype=torch.float32, use_workspace=False)
+    torch.cuda.synchronize()
+    check(y0, yr, TOL_BF16, False, "unsegmented y")
+    check(y, y0, TOL_BF16, False, "segmented vs unsegmented")
+
+
+def test_workspace_too_small_falls_back():
+    b, L, D, N = 1, 20000, 256, 16
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=torch.bfloat16, seed=77))
+    small = torch.empty(64, dtype=torch.uint8, device=DEV)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], y_dtype=torch.float32, workspace=small)
+    torch.cuda.synchronize()
+    yr, sr = oracle_fwd(d)
+    check(y, yr, TOL_BF16, False, "fallback y")
