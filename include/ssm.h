@@ -136,6 +136,35 @@ SSM_API ssm_status_t ssm_selective_scan_fwd_ws(const ssm_tensor_t* u, const ssm_
                                                size_t workspace_bytes, void* stream);
 
 /*
+ * ssm_selective_scan_fwd_noalloc -- the forward pass for callers that cannot allocate
+ * device memory or pass the library a workspace. (Not a method of the pages: the
+ * pages have no counterpart; this is an interface convenience.)
+ *
+ * Who needs it: code that may only touch buffers it was handed -- an inference engine
+ * that reserves its whole memory budget when it starts and forbids allocations later,
+ * a plugin or callback interface that receives only input and output pointers, or a
+ * latency-bound path where an allocation that can stall or fail is not acceptable.
+ *
+ * Same arguments, result and errors as ssm_selective_scan_fwd. When the shape takes
+ * the segmented schedule (see ssm_selective_scan_fwd_workspace_size), its scratch is a
+ * fixed array of SSM_NOALLOC_SCRATCH_BYTES that the library keeps on every GPU that
+ * loads it, until the process exits; a shape that would need more returns
+ * SSM_ERR_UNSUPPORTED. The call itself allocates nothing.
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (other
+ *    streams, other threads) race on it. Nothing in it needs to start at zero; each
+ *    call writes every scratch value before reading it.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES (4u << 20)
+SSM_API ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                                    const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                                    const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                                    int delta_softplus, ssm_tensor_t* y,
+                                                    ssm_tensor_t* last_state, void* stream);
+
+/*
  * ssm_state_update -- one recurrent decode step, state updated in place.
  *
  * For each batch row b and channel d:

@@ -11,6 +11,7 @@
 #include <string.h>
 
 #include <initializer_list>
+#include <mutex>
 
 #include "../../include/ssm.h"
 #include "common.cuh"
@@ -487,6 +488,57 @@ ssm_status_t ssm_device_error(void* stream, int32_t* code) {
   if (cudaMemcpyToSymbol(ssm::g_ssm_error, &zero, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
   *code = v;
   return SSM_OK;
+}
+
+}  // extern "C"
+
+// ---- forward pass with built-in scratch (allocates nothing) ---------------------------
+// For callers that cannot hand the library a workspace: the segmented schedule's scratch
+// (segment end states, decay products and start states) lives in this fixed array
+// instead. Every GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device
+// (with that device current) and cached; nullptr if the lookup fails.
+void* noalloc_scratch() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                            const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                            const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                            ssm_tensor_t* y, ssm_tensor_t* last_state, void* stream) {
+  if (!u || !A) return SSM_ERR_NULL;
+  if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
+  const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
+  if (batch < 0 || L < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
+  size_t need = 0;
+  if (batch > 0 && L > 0 && Dm > 0 && n_supported(N)) need = plan_segments(batch, L, Dm, N).bytes;
+  if (need > (size_t)SSM_NOALLOC_SCRATCH_BYTES) return SSM_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (need > 0) {
+    scratch = noalloc_scratch();
+    if (!scratch) return SSM_ERR_CUDA;
+  }
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, scratch,
+                  scratch ? (size_t)SSM_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 
 }  // extern "C"
