@@ -4,7 +4,12 @@
  * Two operations of the Mamba selective state-space layer, both hand-written CUDA:
  *
  *   ssm_selective_scan_fwd   the fused forward pass over a whole sequence
+ *                            (_ws: with a workspace; _ex: from a given start state
+ *                            and/or with the zero-order-hold B-bar; _noalloc: with
+ *                            built-in scratch)
  *   ssm_state_update         the single-token recurrent update used in decoding
+ *                            (_ex: with the step-size bias and softplus applied,
+ *                            optionally the zero-order-hold B-bar)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -135,6 +140,42 @@ SSM_API ssm_status_t ssm_selective_scan_fwd_ws(const ssm_tensor_t* u, const ssm_
                                                ssm_tensor_t* last_state, void* workspace,
                                                size_t workspace_bytes, void* stream);
 
+/* Flags of the extended entry points (ssm_selective_scan_fwd_ex, ssm_state_update_ex). */
+#define SSM_FWD_ZOH 1u /* B-bar from the exact zero-order hold instead of Delta * B */
+
+/*
+ * ssm_selective_scan_fwd_ex -- ssm_selective_scan_fwd_ws with two options.
+ *
+ * Start state h0: the recurrence begins at h(0) = h0 instead of zeros, so a sequence
+ * can be processed in pieces (chunked prefill, a cached prompt prefix continued with
+ * new tokens): running the prefix, then the rest with h0 = the prefix's last_state,
+ * gives the result of one call over the whole sequence. Sources: "Mamba and State
+ * Space Models", "Common Pitfalls" (the state after a prefix is reusable) and
+ * "Selective scan pseudo-code" (the loop carries h from step to step); "8.7 State Space
+ * Models (Mamba)", section 2.1 fixes h(0) = 0 for a sequence start, the case h0 = NULL.
+ *
+ * flags & SSM_FWD_ZOH: B-bar is the exact zero-order hold of the continuous system,
+ *   B-bar[n] = (exp(dt A[d,n]) - 1) / A[d,n] * B[b,t,n]   (dt * B[b,t,n] where A[d,n] = 0)
+ * ("Arch 02: Mamba SSM", zero-order-hold discretisation; "8.7 State Space Models
+ * (Mamba)", section 3) instead of the simplification dt * B that Mamba uses. This
+ * option runs on the general kernel (fp32 arithmetic, expm1 for the B-bar factor),
+ * not on the fast bf16 channel kernel.
+ *
+ *   h0     (batch, D, N)  f32, nullable   start state (NULL = zeros); read only
+ *   flags  0 or SSM_FWD_ZOH               other bits: SSM_ERR_UNSUPPORTED
+ * last_state may be the same buffer as h0 (same pointer and shape): the start state is
+ * read before the final state is written. Any other overlap of h0 with an output is
+ * SSM_ERR_LAYOUT. L == 0 copies h0 (or zeros) to last_state. Everything else as
+ * ssm_selective_scan_fwd_ws.
+ */
+SSM_API ssm_status_t ssm_selective_scan_fwd_ex(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                               const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                               const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                               const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                               int delta_softplus, const ssm_tensor_t* h0, uint32_t flags,
+                                               ssm_tensor_t* y, ssm_tensor_t* last_state,
+                                               void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * ssm_selective_scan_fwd_noalloc -- the forward pass for callers that cannot allocate
  * device memory or pass the library a workspace. (Not a method of the pages: the
@@ -193,6 +234,27 @@ SSM_API ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x
                               const ssm_tensor_t* B, const ssm_tensor_t* C,
                               const ssm_tensor_t* D, const ssm_tensor_t* z,
                               ssm_tensor_t* y, void* stream);
+
+/*
+ * ssm_state_update_ex -- ssm_state_update with the forward pass's step-size map applied
+ * inside the step: dt = delta[b,d] + delta_bias[d], then softplus(dt) when
+ * delta_softplus is 1, and dt replaces delta in the update. This is the decode step of
+ * a model whose forward pass uses the same bias and softplus ("Mamba and State Space
+ * Models", "Discretization and initialization details": Delta = softplus(W x + b)), so
+ * a decode step continues ssm_selective_scan_fwd exactly.
+ *
+ *   delta_bias  (D)  f32, nullable   added to delta (NULL = 0)
+ *   delta_softplus   0 or 1          anything else is SSM_ERR_UNSUPPORTED
+ *   flags            0 or SSM_FWD_ZOH (the zero-order-hold B-bar, as in
+ *                    ssm_selective_scan_fwd_ex); other bits: SSM_ERR_UNSUPPORTED
+ * Everything else as ssm_state_update.
+ */
+SSM_API ssm_status_t ssm_state_update_ex(ssm_tensor_t* state, const ssm_tensor_t* x,
+                                         const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                         const ssm_tensor_t* B, const ssm_tensor_t* C,
+                                         const ssm_tensor_t* D, const ssm_tensor_t* z,
+                                         const ssm_tensor_t* delta_bias, int delta_softplus,
+                                         uint32_t flags, ssm_tensor_t* y, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

@@ -72,6 +72,11 @@ class Oracle:
                                                                                ctypes.c_int]
         lib.ssm_oracle_state_update.restype = ctypes.c_int
         lib.ssm_oracle_state_update.argtypes = [_i64, _i64, _i64] + [_dp] * 9
+        lib.ssm_oracle_state_update_ex.restype = ctypes.c_int
+        lib.ssm_oracle_state_update_ex.argtypes = [_i64, _i64, _i64] + [_dp] * 9 + [ctypes.c_int, ctypes.c_int, _dp]
+        lib.ssm_oracle_fwd_ex.restype = ctypes.c_int
+        lib.ssm_oracle_fwd_ex.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int, ctypes.c_int, _dp, _dp,
+                                                                                 _dp, ctypes.c_int]
         self.lib = lib
 
     def softplus(self, r: float) -> float:
@@ -81,11 +86,12 @@ class Oracle:
         return self.lib.ssm_oracle_silu(float(z))
 
     def selective_scan_fwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                           delta_softplus=True, h0=None, nthreads=0):
+                           delta_softplus=True, h0=None, nthreads=0, zoh=False):
         """Returns (y, last_state) as fp64 numpy arrays.
 
         u, delta, z: (batch, L, D); A: (D, N); B, C: (batch, L, N); D, delta_bias: (D);
-        h0: (batch, D, N) initial state (zeros if None).
+        h0: (batch, D, N) initial state (zeros if None). zoh: B-bar from the exact
+        zero-order hold, (exp(dt A) - 1) / A * B, instead of dt * B.
         """
         u = _f64(u)
         batch, L, Dm = u.shape
@@ -101,17 +107,21 @@ class Oracle:
         h0 = _f64(h0, (batch, Dm, N))
         y = np.empty((batch, L, Dm), np.float64)
         last = np.empty((batch, Dm, N), np.float64)
-        rc = self.lib.ssm_oracle_fwd(batch, L, Dm, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                                     _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
-                                     _ptr(h0), _ptr(y), _ptr(last), int(nthreads))
+        rc = self.lib.ssm_oracle_fwd_ex(batch, L, Dm, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                        _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                        int(bool(zoh)), _ptr(h0), _ptr(y), _ptr(last), int(nthreads))
         if rc != 0:
             raise RuntimeError("ssm_oracle_fwd rejected its arguments")
         return y, last
 
-    def state_update(self, state, x, delta, A, B, C, D=None, z=None):
+    def state_update(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                     zoh=False):
         """One decode step. Returns (y, new_state); the input state is not modified.
 
         state: (batch, D, N); x, delta, z: (batch, D); A: (D, N); B, C: (batch, N); D: (D).
+        delta_bias (D) / delta_softplus: the forward pass's step-size map applied to delta
+        first (dt = softplus(delta + bias)); by default delta is the final step size.
+        zoh: B-bar from the exact zero-order hold (as in selective_scan_fwd).
         """
         st = _f64(state).copy()
         batch, Dm, N = st.shape
@@ -122,9 +132,11 @@ class Oracle:
         C = _f64(C, (batch, N))
         D = _f64(D, (Dm,))
         z = _f64(z, (batch, Dm))
+        delta_bias = _f64(delta_bias, (Dm,))
         y = np.empty((batch, Dm), np.float64)
-        rc = self.lib.ssm_oracle_state_update(batch, Dm, N, _ptr(st), _ptr(x), _ptr(delta), _ptr(A),
-                                              _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y))
+        rc = self.lib.ssm_oracle_state_update_ex(batch, Dm, N, _ptr(st), _ptr(x), _ptr(delta), _ptr(A),
+                                                 _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                                                 int(bool(delta_softplus)), int(bool(zoh)), _ptr(y))
         if rc != 0:
             raise RuntimeError("ssm_oracle_state_update rejected its arguments")
         return y, st

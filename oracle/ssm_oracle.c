@@ -40,10 +40,18 @@ double ssm_oracle_silu(double z) {
 #endif
 }
 
+/* B-bar factor of the exact zero-order hold for one diagonal entry a of A:
+ * (delta a)^-1 (exp(delta a) - 1) delta = (exp(delta a) - 1) / a ("Arch 02: Mamba SSM",
+ * zero-order-hold discretisation; "8.7 State Space Models (Mamba)", section 3), with
+ * its limit delta at a = 0. */
+static double zoh_factor(double dt, double a) {
+  return a != 0.0 ? expm1(dt * a) / a : dt;
+}
+
 typedef struct {
   int64_t batch, L, D, N;
   const double *u, *delta, *A, *B, *C, *Dskip, *z, *delta_bias, *h0;
-  int delta_softplus;
+  int delta_softplus, zoh;
   double *y, *last_state;
   int64_t ch_begin, ch_end; /* flattened channel range b*D + d */
 } fwd_job_t;
@@ -89,7 +97,8 @@ static void fwd_channel(const fwd_job_t* j, int64_t b, int64_t d, double* h) {
 #elif SSM_ORACLE_PLANT == 3
       const double dB = dt * j->C[ixn + n];         /* planted: B and C swapped */
 #else
-      const double dB = dt * j->B[ixn + n];         /* B-bar = Delta * B */
+      const double dB = j->zoh ? zoh_factor(dt, An) * j->B[ixn + n]  /* B-bar, exact ZOH */
+                               : dt * j->B[ixn + n];                 /* B-bar = Delta * B */
 #endif
 #if SSM_ORACLE_PLANT == 7
       acc += j->C[ixn + n] * h[n];                  /* planted: read out before the update */
@@ -137,12 +146,21 @@ int ssm_oracle_fwd(int64_t batch, int64_t L, int64_t D, int64_t N,
                    const double* B, const double* C, const double* Dskip,
                    const double* z, const double* delta_bias, int delta_softplus,
                    const double* h0, double* y, double* last_state, int nthreads) {
+  return ssm_oracle_fwd_ex(batch, L, D, N, u, delta, A, B, C, Dskip, z, delta_bias, delta_softplus, 0, h0, y,
+                           last_state, nthreads);
+}
+
+int ssm_oracle_fwd_ex(int64_t batch, int64_t L, int64_t D, int64_t N,
+                      const double* u, const double* delta, const double* A,
+                      const double* B, const double* C, const double* Dskip,
+                      const double* z, const double* delta_bias, int delta_softplus, int zoh,
+                      const double* h0, double* y, double* last_state, int nthreads) {
   if (batch < 0 || L < 0 || D < 0 || N <= 0) return -1;
   const int64_t nch = batch * D;
   if (nch == 0) return 0;
   if ((L > 0 && (!u || !delta || !B || !C || !y)) || !A) return -1;
   fwd_job_t base = {batch, L, D, N, u, delta, A, B, C, Dskip, z, delta_bias, h0,
-                    delta_softplus, y, last_state, 0, 0};
+                    delta_softplus, zoh, y, last_state, 0, 0};
   int nt = resolve_threads(nthreads, nch);
   if (nt == 1) {
     base.ch_begin = 0;
@@ -173,22 +191,26 @@ int ssm_oracle_fwd(int64_t batch, int64_t L, int64_t D, int64_t N,
 /* One recurrent step per (batch, channel): the O(1)-per-token inference update
  * ("8.7 State Space Models (Mamba)", section 5; "Mamba and State Space Models",
  * "Selective scan pseudo-code" body for a single t), continuing from a given state. */
-int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
-                            const double* x, const double* delta, const double* A,
-                            const double* B, const double* C, const double* Dskip,
-                            const double* z, double* y) {
+int ssm_oracle_state_update_ex(int64_t batch, int64_t D, int64_t N, double* state,
+                               const double* x, const double* delta, const double* A,
+                               const double* B, const double* C, const double* Dskip,
+                               const double* z, const double* delta_bias, int delta_softplus,
+                               int zoh, double* y) {
   if (batch < 0 || D < 0 || N <= 0) return -1;
   if (batch * D == 0) return 0;
   if (!state || !x || !delta || !A || !B || !C || !y) return -1;
   for (int64_t b = 0; b < batch; ++b) {
     for (int64_t d = 0; d < D; ++d) {
-      const double dt = delta[b * D + d];
+      /* the forward pass's step-size map, when asked: dt = softplus(delta + bias) */
+      const double r = delta[b * D + d] + (delta_bias ? delta_bias[d] : 0.0);
+      const double dt = delta_softplus ? ssm_oracle_softplus(r) : r;
       const double xv = x[b * D + d];
       double acc = 0.0;
       for (int64_t n = 0; n < N; ++n) {
         double* s = &state[(b * D + d) * N + n];
         const double dA = exp(dt * A[d * N + n]);
-        *s = dA * (*s) + dt * B[b * N + n] * xv;
+        const double dB = (zoh ? zoh_factor(dt, A[d * N + n]) : dt) * B[b * N + n];
+        *s = dA * (*s) + dB * xv;
         acc += C[b * N + n] * (*s);
       }
       double v = acc + (Dskip ? Dskip[d] * xv : 0.0);
@@ -196,4 +218,11 @@ int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
     }
   }
   return 0;
+}
+
+int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* Dskip,
+                            const double* z, double* y) {
+  return ssm_oracle_state_update_ex(batch, D, N, state, x, delta, A, B, C, Dskip, z, NULL, 0, 0, y);
 }

@@ -58,6 +58,17 @@ int ssm_oracle_fwd(int64_t batch, int64_t L, int64_t D, int64_t N,
                    const double* h0, double* y, double* last_state, int nthreads);
 
 /*
+ * The same with a choice of B-bar: zoh = 0 takes Delta * B (as above); zoh = 1 the exact
+ * zero-order hold of the continuous system, B-bar[n] = (exp(Delta A[d,n]) - 1) / A[d,n]
+ * * B[b,t,n] (Delta * B[b,t,n] where A[d,n] = 0).
+ */
+int ssm_oracle_fwd_ex(int64_t batch, int64_t L, int64_t D, int64_t N,
+                      const double* u, const double* delta, const double* A,
+                      const double* B, const double* C, const double* Dskip,
+                      const double* z, const double* delta_bias, int delta_softplus, int zoh,
+                      const double* h0, double* y, double* last_state, int nthreads);
+
+/*
  * One recurrent decode step, in place on state (batch, D, N):
  *   x, delta, z, y : (batch, D)   B, C : (batch, N)   A : (D, N)   Dskip : (D)
  * delta is the final step size (no bias, no softplus). Nullable: Dskip, z.
@@ -67,6 +78,17 @@ int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
                             const double* x, const double* delta, const double* A,
                             const double* B, const double* C, const double* Dskip,
                             const double* z, double* y);
+
+/*
+ * The same step with the forward pass's step-size map applied first:
+ *   dt = delta[b,d] + delta_bias[d] (bias 0 if absent), then log(1 + exp(dt)) when
+ *   delta_softplus is 1; and B-bar chosen as in ssm_oracle_fwd_ex (zoh).
+ */
+int ssm_oracle_state_update_ex(int64_t batch, int64_t D, int64_t N, double* state,
+                               const double* x, const double* delta, const double* A,
+                               const double* B, const double* C, const double* Dskip,
+                               const double* z, const double* delta_bias, int delta_softplus,
+                               int zoh, double* y);
 
 #ifdef __cplusplus
 }

@@ -48,6 +48,17 @@ __device__ __forceinline__ float decay(float dt, float A, float A2) {
   return ex2(dt * A2);
 }
 
+// B-bar factor of the exact zero-order hold for one diagonal entry A of the state
+// matrix: (exp(dt A) - 1) / A, with its limit dt at A = 0, so that B-bar = factor * B.
+// expm1 keeps the factor accurate when dt A is small (no cancellation in exp - 1); the
+// fp32 I/O path evaluates it in double like its decay.
+template <bool kAccurate>
+__device__ __forceinline__ float zoh_factor(float dt, float A) {
+  if (A == 0.f) return dt;
+  if (kAccurate) return (float)(expm1((double)dt * (double)A) / (double)A);
+  return expm1f(dt * A) / A;
+}
+
 // ---- step-size map and gate -----------------------------------------------------
 // Accurate softplus log(1 + e^r): identity above 20 (the remainder e^-20 is below
 // fp32 resolution of r), log1p otherwise.

@@ -29,6 +29,8 @@ struct FwdParams {
   int delta_softplus;
   void* y;
   float* last_state;        // nullable
+  const float* h0;          // nullable: start state (batch, D, N); zeros when null
+  int zoh;                  // 1: B-bar = (exp(dt A) - 1) / A B (general kernel only)
   int64_t batch, L, D;
   // Sequence segments (channel kernel only): CTA z covers steps [z*seg_len, (z+1)*seg_len).
   // seg_len == L means one segment. seg_h0 (nullable): start state of each segment,
@@ -48,7 +50,8 @@ struct FwdParams {
 //   scan   : each lane updates its SPL states for every t, writes its partial C.h
 //   finish : y = sum of partials + D u, gated, stored
 // ------------------------------------------------------------------------------------
-template <typename T, typename TY, int N, int SPL, int DT, int TC>
+// kZOH: B-bar = (exp(dt A) - 1) / A B (zero-order hold) instead of dt B.
+template <typename T, typename TY, int N, int SPL, int DT, int TC, bool kZOH>
 __global__ void __launch_bounds__(DT*(N / SPL))
 scan_fwd_generic(const FwdParams p) {
   constexpr int LPC = N / SPL;
@@ -81,7 +84,7 @@ scan_fwd_generic(const FwdParams p) {
   for (int k = 0; k < SPL; ++k) {
     Av[k] = vj ? p.A[dj * N + g * SPL + k] : 0.f;
     A2[k] = Av[k] * kLog2e;
-    h[k] = 0.f;
+    h[k] = (vj && p.h0) ? p.h0[(b * D + dj) * N + g * SPL + k] : 0.f;
   }
 
   for (int64_t t0 = 0; t0 < L; t0 += TC) {
@@ -122,7 +125,8 @@ scan_fwd_generic(const FwdParams p) {
       for (int k = 0; k < SPL; ++k) {
         const int n = g * SPL + k;
         const float a = decay<kAccurate>(dd.x, Av[k], A2[k]);  // A-bar = exp(dt * A)
-        h[k] = fmaf(a, h[k], dd.y * sB[t][n]);             // h = A-bar h + (dt u) B
+        const float bu = kZOH ? zoh_factor<kAccurate>(dd.x, Av[k]) * sU[t][j] : dd.y;
+        h[k] = fmaf(a, h[k], bu * sB[t][n]);               // h = A-bar h + (dt u) B
         acc = fmaf(sC[t][n], h[k], acc);                   // C . h (this lane's states)
       }
       sP[t][tid] = acc;

@@ -371,17 +371,19 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
 // Carry between sequence segments: for every (batch, channel, state) the segment
 // aggregates (P_s, E_s) are pairs of the recurrence h -> P h + E, combined in time order
 // by (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2). One warp per (batch, channel, state),
-// lane s holding segment s - 1 (lane 0 the identity), runs an inclusive Hillis-Steele
-// scan with __shfl_up_sync; lane s then holds the state at the start of segment s.
+// lane s holding segment s - 1 (lane 0 the start state: (1, h0), h0 = 0 when absent),
+// runs an inclusive Hillis-Steele scan with __shfl_up_sync; lane s then holds the state
+// at the start of segment s.
 // ("8.7 State Space Models (Mamba)", section 4.1 and "Mamba and State Space Models",
 // "Hardware-Aware Parallel Scan": the recurrence is an associative scan.)
-// Requires nseg <= 32. Layout of E, P, H: [segment][batch * D * N].
+// Requires nseg <= 32. Layout of E, P, H: [segment][batch * D * N]; h0: [batch * D * N].
 __global__ void __launch_bounds__(256) seg_carry_kernel(const float* __restrict__ E, const float* __restrict__ P,
-                                                       float* __restrict__ H, int nseg, int64_t nbdn) {
+                                                       const float* __restrict__ h0, float* __restrict__ H, int nseg,
+                                                       int64_t nbdn) {
   const int64_t idx = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (idx >= nbdn) return;  // whole warps leave together
-  float a = 1.f, c = 0.f;
+  float a = 1.f, c = (lane == 0 && h0) ? h0[idx] : 0.f;
   if (lane >= 1 && lane < nseg) {
     a = P[(int64_t)(lane - 1) * nbdn + idx];
     c = E[(int64_t)(lane - 1) * nbdn + idx];

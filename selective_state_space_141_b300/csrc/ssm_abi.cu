@@ -120,7 +120,8 @@ constexpr int kChanTC = 32, kChanStages = 4;
 bool chan_eligible(const FwdParams& p, int64_t N) {
   // TMA needs 16-byte aligned bases and row pitches (D % 8 == 0 covers bf16 and fp32
   // y) and int32 coordinates; last_state is written with 16-byte vector stores.
-  return (N == 8 || N == 16) && p.D % 8 == 0 && p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
+  // The zero-order-hold B-bar is a general-kernel option.
+  return !p.zoh && (N == 8 || N == 16) && p.D % 8 == 0 && p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
          aligned16(p.delta) && aligned16(p.z) && aligned16(p.B) && aligned16(p.C) && aligned16(p.y) &&
          aligned16(p.last_state) && encode_fn() != nullptr;
 }
@@ -197,7 +198,7 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
   const bool sp = p0.delta_softplus != 0, z = p0.z != nullptr;
   FwdParams p = p0;
   p.seg_len = p0.L;
-  p.seg_h0 = nullptr;
+  p.seg_h0 = p0.h0;  // one segment: the caller's start state (or zeros)
   p.seg_E = p.seg_P = nullptr;
   int nseg = 1;
   if (plan.nseg > 1 && ws) {
@@ -208,13 +209,15 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     float* H = P + stride;
     nseg = plan.nseg;
     p.seg_len = plan.seg_len;
+    p.seg_h0 = nullptr;  // the aggregate pass runs every segment from zero; h0 enters in the carry scan
     p.seg_E = E;
     p.seg_P = P;
     cudaError_t e = sp ? launch_chan_k<__nv_bfloat16, N, true, false, true>(p, maps, nseg - 1, st)
                        : launch_chan_k<__nv_bfloat16, N, false, false, true>(p, maps, nseg - 1, st);
     if (e != cudaSuccess) return e;
     const int64_t nbdn = p0.batch * p0.D * N;
-    void* cargs[] = {&E, &P, &H, &nseg, const_cast<int64_t*>(&nbdn)};
+    const float* h0 = p0.h0;
+    void* cargs[] = {&E, &P, &h0, &H, &nseg, const_cast<int64_t*>(&nbdn)};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_kernel), dim3((unsigned)((nbdn + 7) / 8)),
                          dim3(256), cargs, 0, st);
     if (e != cudaSuccess) return e;
@@ -241,8 +244,9 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t st) {
   dim3 grid((unsigned)((p.D + DT - 1) / DT), (unsigned)p.batch);
   dim3 block(DT * (N / SPL));
   void* args[] = {const_cast<FwdParams*>(&p)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC>), grid,
-                          block, args, 0, st);
+  const void* kern = p.zoh ? reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC, true>)
+                           : reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC, false>);
+  return cudaLaunchKernel(kern, grid, block, args, 0, st);
 }
 
 template <typename T, typename TY>
@@ -297,8 +301,9 @@ namespace {
 
 ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
                       const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
-                      const ssm_tensor_t* delta_bias, int delta_softplus, ssm_tensor_t* y, ssm_tensor_t* last_state,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+                      const ssm_tensor_t* delta_bias, int delta_softplus, const ssm_tensor_t* h0, uint32_t flags,
+                      ssm_tensor_t* y, ssm_tensor_t* last_state, void* workspace, size_t workspace_bytes,
+                      void* stream) {
   if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
   const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
@@ -314,21 +319,25 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   if (delta_bias && (s = check_tensor(delta_bias, {Dm})) != SSM_OK) return s;
   if ((s = check_tensor(y, {batch, L, Dm})) != SSM_OK) return s;
   if (last_state && (s = check_tensor(last_state, {batch, Dm, N})) != SSM_OK) return s;
+  if (h0 && (s = check_tensor(h0, {batch, Dm, N})) != SSM_OK) return s;
 
   const ssm_dtype_t io = u->dtype;
   if (delta->dtype != io || B->dtype != io || C->dtype != io || (z && z->dtype != io)) return SSM_ERR_DTYPE;
   if (y->dtype != io && y->dtype != SSM_F32) return SSM_ERR_DTYPE;
   if (A->dtype != SSM_F32 || (D && D->dtype != SSM_F32) || (delta_bias && delta_bias->dtype != SSM_F32) ||
-      (last_state && last_state->dtype != SSM_F32))
+      (last_state && last_state->dtype != SSM_F32) || (h0 && h0->dtype != SSM_F32))
     return SSM_ERR_DTYPE;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_UNSUPPORTED;
+  if ((flags & ~SSM_FWD_ZOH) != 0) return SSM_ERR_UNSUPPORTED;
   if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
   if (batch > 65535) return SSM_ERR_UNSUPPORTED;
 
-  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias};
+  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias, h0};
+  // last_state may be exactly the h0 buffer (read first, then overwritten by the same thread).
+  const bool state_in_place = h0 && last_state && h0->data == last_state->data;
   for (const ssm_tensor_t* in : ins) {
     if (overlaps(y, in)) return SSM_ERR_LAYOUT;
-    if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
+    if (last_state && !(state_in_place && in == h0) && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
   }
   if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
   if (workspace && workspace_bytes > 0) {
@@ -337,16 +346,20 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     w.dtype = SSM_F32;
     w.ndim = 1;
     w.shape[0] = (int64_t)(workspace_bytes / 4);
-    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state};
+    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, h0, y, last_state};
     for (const ssm_tensor_t* t : all)
       if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (batch == 0 || Dm == 0) return SSM_OK;
-  if (L == 0) {
-    if (last_state && cudaMemsetAsync(last_state->data, 0, (size_t)(numel(last_state) * 4), st) != cudaSuccess)
-      return SSM_ERR_CUDA;
+  if (L == 0) {  // the state is unchanged: h0, or zeros
+    if (last_state && !state_in_place) {
+      const size_t bytes = (size_t)(numel(last_state) * 4);
+      const cudaError_t e = h0 ? cudaMemcpyAsync(last_state->data, h0->data, bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(last_state->data, 0, bytes, st);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+    }
     return SSM_OK;
   }
 
@@ -362,6 +375,8 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.delta_softplus = delta_softplus;
   p.y = y->data;
   p.last_state = last_state ? static_cast<float*>(last_state->data) : nullptr;
+  p.h0 = h0 ? static_cast<const float*>(h0->data) : nullptr;
+  p.zoh = (flags & SSM_FWD_ZOH) ? 1 : 0;
   p.batch = batch;
   p.L = L;
   p.D = Dm;
@@ -399,7 +414,7 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* d
                                     const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
                                     const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
                                     ssm_tensor_t* y, ssm_tensor_t* last_state, void* stream) {
-  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, nullptr, 0, stream);
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, 0u, y, last_state, nullptr, 0, stream);
 }
 
 ssm_status_t ssm_selective_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N, size_t* bytes) {
@@ -418,13 +433,27 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_tensor_t* u, const ssm_tensor_t
                                        size_t workspace_bytes, void* stream) {
   if (workspace_bytes > 0 && !workspace) return SSM_ERR_NULL;
   if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SSM_ERR_LAYOUT;
-  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace, workspace_bytes,
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, 0u, y, last_state, workspace, workspace_bytes,
                   stream);
 }
 
-ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta,
-                              const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
-                              const ssm_tensor_t* D, const ssm_tensor_t* z, ssm_tensor_t* y, void* stream) {
+ssm_status_t ssm_selective_scan_fwd_ex(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                       const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                       const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                       const ssm_tensor_t* h0, uint32_t flags, ssm_tensor_t* y,
+                                       ssm_tensor_t* last_state, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (workspace_bytes > 0 && !workspace) return SSM_ERR_NULL;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SSM_ERR_LAYOUT;
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, flags, y, last_state, workspace,
+                  workspace_bytes, stream);
+}
+
+namespace {
+ssm_status_t dec_impl(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                      const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
+                      const ssm_tensor_t* delta_bias, int delta_softplus, uint32_t flags, ssm_tensor_t* y,
+                      void* stream) {
   if (!state || !x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (state->ndim != 3) return SSM_ERR_SHAPE;
   const int64_t batch = state->shape[0], Dm = state->shape[1], N = state->shape[2];
@@ -439,14 +468,19 @@ ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const 
   if (D && (s = check_tensor(D, {Dm})) != SSM_OK) return s;
   if (z && (s = check_tensor(z, {batch, Dm})) != SSM_OK) return s;
   if ((s = check_tensor(y, {batch, Dm})) != SSM_OK) return s;
+  if (delta_bias && (s = check_tensor(delta_bias, {Dm})) != SSM_OK) return s;
 
   const ssm_dtype_t io = x->dtype;
   if (delta->dtype != io || B->dtype != io || C->dtype != io || (z && z->dtype != io)) return SSM_ERR_DTYPE;
   if (y->dtype != io && y->dtype != SSM_F32) return SSM_ERR_DTYPE;
-  if (state->dtype != SSM_F32 || A->dtype != SSM_F32 || (D && D->dtype != SSM_F32)) return SSM_ERR_DTYPE;
+  if (state->dtype != SSM_F32 || A->dtype != SSM_F32 || (D && D->dtype != SSM_F32) ||
+      (delta_bias && delta_bias->dtype != SSM_F32))
+    return SSM_ERR_DTYPE;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_UNSUPPORTED;
+  if ((flags & ~SSM_FWD_ZOH) != 0) return SSM_ERR_UNSUPPORTED;
   if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
 
-  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, z};
+  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, z, delta_bias};
   for (const ssm_tensor_t* in : ins) {
     if (overlaps(y, in)) return SSM_ERR_LAYOUT;
     if (overlaps(state, in)) return SSM_ERR_LAYOUT;
@@ -466,6 +500,9 @@ ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const 
   p.Dskip = D ? static_cast<const float*>(D->data) : nullptr;
   p.z = z ? z->data : nullptr;
   p.y = y->data;
+  p.delta_bias = delta_bias ? static_cast<const float*>(delta_bias->data) : nullptr;
+  p.delta_softplus = delta_softplus;
+  p.zoh = (flags & SSM_FWD_ZOH) ? 1 : 0;
   p.batch = batch;
   p.D = Dm;
 
@@ -477,6 +514,20 @@ ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const 
   else
     e = launch_dec_n<__nv_bfloat16, float>(N, p, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+}  // namespace
+
+ssm_status_t ssm_state_update(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta,
+                              const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
+                              const ssm_tensor_t* D, const ssm_tensor_t* z, ssm_tensor_t* y, void* stream) {
+  return dec_impl(state, x, delta, A, B, C, D, z, nullptr, 0, 0u, y, stream);
+}
+
+ssm_status_t ssm_state_update_ex(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta,
+                                 const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
+                                 const ssm_tensor_t* D, const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                 int delta_softplus, uint32_t flags, ssm_tensor_t* y, void* stream) {
+  return dec_impl(state, x, delta, A, B, C, D, z, delta_bias, delta_softplus, flags, y, stream);
 }
 
 ssm_status_t ssm_device_error(void* stream, int32_t* code) {
@@ -537,7 +588,7 @@ ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_tensor_t* u, const ssm_ten
     scratch = noalloc_scratch();
     if (!scratch) return SSM_ERR_CUDA;
   }
-  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, scratch,
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, 0u, y, last_state, scratch,
                   scratch ? (size_t)SSM_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 

@@ -1,6 +1,7 @@
 // state_update.cuh -- single-token recurrent decode step, fp32 state updated in place.
 //
-// For each (b, d):  state[n] = exp(dt A[d,n]) state[n] + dt B[b,n] x
+// For each (b, d):  dt = delta[b,d] (+ bias[d], then softplus, when asked)
+//                   state[n] = exp(dt A[d,n]) state[n] + dt B[b,n] x
 //                   y = (sum_n C[b,n] state[n] + D[d] x) * silu(z)
 // ("8.7 State Space Models (Mamba)", section 5: O(1) work per generated token on a
 //  fixed d*n state; "Mamba and State Space Models", "Selective scan pseudo-code",
@@ -24,6 +25,9 @@ struct DecodeParams {
   const float* Dskip;  // nullable
   const void* z;       // nullable
   void* y;
+  const float* delta_bias;  // nullable: added to delta
+  int delta_softplus;       // 1: dt = softplus(delta + bias)
+  int zoh;                  // 1: B-bar = (exp(dt A) - 1) / A B instead of dt B
   int64_t batch, D;
 };
 
@@ -47,7 +51,9 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
     const T* Bp = static_cast<const T*>(p.B) + b * N + g * 4;
     const T* Cp = static_cast<const T*>(p.C) + b * N + g * 4;
     x = to_f32(xp[bd]);
-    const float dt = to_f32(dp[bd]);
+    float dt = to_f32(dp[bd]);
+    if (p.delta_bias) dt += p.delta_bias[d];
+    if (p.delta_softplus) dt = softplus_precise(dt);
     const float dx = dt * x;
     float4* sp = reinterpret_cast<float4*>(p.state + bd * N + g * 4);
     s = *sp;
@@ -57,7 +63,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float a = decay<sizeof(T) == 4>(dt, av[k], av[k] * kLog2e);
-      sv[k] = fmaf(a, sv[k], dx * to_f32(Bp[k]));
+      const float bx = p.zoh ? zoh_factor<sizeof(T) == 4>(dt, av[k]) * x : dx;  // B-bar u = bx B
+      sv[k] = fmaf(a, sv[k], bx * to_f32(Bp[k]));
       acc = fmaf(to_f32(Cp[k]), sv[k], acc);
     }
     *sp = make_float4(sv[0], sv[1], sv[2], sv[3]);

@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssm_b300.so")
 
 SSM_F32, SSM_BF16 = 0, 1
+SSM_FWD_ZOH = 1  # flag of the extended entry points (include/ssm.h)
 _BAD_DTYPE = 99  # forwarded for any other torch dtype so the library reports SSM_ERR_DTYPE
 _DTYPES = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
 
@@ -58,8 +59,13 @@ def load_library(path: str | None = None):
                                                           ctypes.c_void_p]
     lib.ssm_selective_scan_fwd_workspace_size.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_selective_scan_fwd_ex.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_ex.argtypes = [_P] * 8 + [ctypes.c_int, _P, ctypes.c_uint32, _P, _P, ctypes.c_void_p,
+                                                          ctypes.c_size_t, ctypes.c_void_p]
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = [_P] * 9 + [ctypes.c_void_p]
+    lib.ssm_state_update_ex.restype = ctypes.c_int
+    lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_status_string.argtypes = [ctypes.c_int]
     lib.ssm_device_error.restype = ctypes.c_int
@@ -110,10 +116,14 @@ def workspace_size(batch, L, D, N) -> int:
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True, y=None,
                        last_state=None, return_last_state=True, y_dtype=None, stream=None, workspace=None,
-                       use_workspace=True):
+                       use_workspace=True, h0=None, zoh=False):
     """Fused selective-scan forward pass.
 
     u, delta, z: (batch, L, D); A: (D, N) fp32; B, C: (batch, L, N); D, delta_bias: (D) fp32.
+    h0 (batch, D, N) fp32: start state; None = zeros. ``last_state`` may be the h0 tensor
+    itself (the state is carried in place). zoh: B-bar from the exact zero-order hold,
+    (exp(dt A) - 1) / A B, instead of dt B. Either option goes through
+    ``ssm_selective_scan_fwd_ex``.
     Outputs are allocated with torch on u's device unless given. Returns (y, last_state);
     last_state is None when ``return_last_state`` is False and none was passed.
     With ``use_workspace`` (default) the call goes through ``ssm_selective_scan_fwd_ws``
@@ -127,18 +137,27 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     if last_state is None and return_last_state:
         last_state = torch.empty((u.shape[0], u.shape[2], A.shape[-1]), dtype=torch.float32, device=u.device)
     ds = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias, y, last_state)]
-    if not use_workspace:
+    extended = h0 is not None or zoh
+    if not use_workspace and not extended:
         st = lib.ssm_selective_scan_fwd(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
                                         _ref(ds[9]), _stream(stream))
         if st != 0:
             raise SsmError(st, "ssm_selective_scan_fwd")
         return y, last_state
-    if workspace is None:
+    if workspace is None and use_workspace:
         nbytes = workspace_size(u.shape[0], u.shape[1], u.shape[2], A.shape[-1])
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
     ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
     ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
+    if extended:
+        st = lib.ssm_selective_scan_fwd_ex(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)),
+                                           _ref(describe(h0)), ctypes.c_uint32(SSM_FWD_ZOH if zoh else 0),
+                                           _ref(ds[8]), _ref(ds[9]), ctypes.c_void_p(ws_ptr),
+                                           ctypes.c_size_t(ws_bytes), _stream(stream))
+        if st != 0:
+            raise SsmError(st, "ssm_selective_scan_fwd_ex")
+        return y, last_state
     st = lib.ssm_selective_scan_fwd_ws(*[_ref(x) for x in ds[:8]], int(bool(delta_softplus)), _ref(ds[8]),
                                        _ref(ds[9]), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes),
                                        _stream(stream))
@@ -147,16 +166,26 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     return y, last_state
 
 
-def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, y_dtype=None, stream=None):
-    """One decode step (``ssm_state_update``); ``state`` (batch, D, N) fp32 is updated in
-    place. x, delta, z: (batch, D); B, C: (batch, N). Returns y (batch, D)."""
+def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, y_dtype=None, stream=None, delta_bias=None,
+                 delta_softplus=False, zoh=False):
+    """One decode step; ``state`` (batch, D, N) fp32 is updated in place. x, delta, z:
+    (batch, D); B, C: (batch, N). Returns y (batch, D). With ``delta_bias`` (D) fp32 or
+    ``delta_softplus`` the step size is softplus(delta + bias) as in the forward pass
+    (``ssm_state_update_ex``); otherwise delta is the final step size (``ssm_state_update``).
+    zoh: B-bar from the exact zero-order hold, as in ``selective_scan_fwd``."""
     lib = load_library()
     if y is None:
         y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
     ds = [describe(t) for t in (state, x, delta, A, B, C, D, z, y)]
-    st = lib.ssm_state_update(*[_ref(d) for d in ds], _stream(stream))
+    if delta_bias is None and not delta_softplus and not zoh:
+        st = lib.ssm_state_update(*[_ref(d) for d in ds], _stream(stream))
+        name = "ssm_state_update"
+    else:
+        st = lib.ssm_state_update_ex(*[_ref(d) for d in ds[:8]], _ref(describe(delta_bias)), int(bool(delta_softplus)),
+                                     ctypes.c_uint32(SSM_FWD_ZOH if zoh else 0), _ref(ds[8]), _stream(stream))
+        name = "ssm_state_update_ex"
     if st != 0:
-        raise SsmError(st, "ssm_state_update")
+        raise SsmError(st, name)
     return y
 
 

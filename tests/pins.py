@@ -277,6 +277,86 @@ def pin_scan_operator(o, seed=7):
     assert _rel(last[0, 0], acc[1]) < 1e-13
 
 
+def pin_decode_step_map(o, seed=8):
+    """The decode step with the forward pass's step-size map (dt = softplus(delta + bias),
+    "Mamba and State Space Models", "Discretization and initialization details") equals
+    the plain step given dt computed here with numpy, and equals one forward step from
+    the same start state with the same bias and softplus."""
+    rng = np.random.default_rng(seed)
+    b, D, N = 3, 5, 8
+    st0 = rng.standard_normal((b, D, N))
+    x = rng.standard_normal((b, D))
+    raw = rng.standard_normal((b, D)) * 2
+    bias = rng.uniform(-3, 1, D)
+    z = rng.standard_normal((b, D))
+    A = -rng.uniform(0.1, 4, (D, N))
+    B = rng.standard_normal((b, N))
+    C = rng.standard_normal((b, N))
+    Dk = rng.standard_normal(D)
+    ye, se = o.state_update(st0, x, raw, A, B, C, D=Dk, z=z, delta_bias=bias, delta_softplus=True)
+    yp, sp = o.state_update(st0, x, _softplus(raw + bias), A, B, C, D=Dk, z=z)
+    assert _rel(ye, yp) < 1e-14 and _rel(se, sp) < 1e-14
+    yf, sf = o.selective_scan_fwd(x[:, None], raw[:, None], A, B[:, None], C[:, None], D=Dk, z=z[:, None],
+                                  delta_bias=bias, delta_softplus=True, h0=st0)
+    assert _rel(ye, yf[:, 0]) < 1e-14 and _rel(se, sf) < 1e-14
+    # bias without softplus: dt = delta + bias exactly
+    yb, sb = o.state_update(st0, x, raw, A, B, C, D=Dk, z=z, delta_bias=bias, delta_softplus=False)
+    yq, sq = o.state_update(st0, x, raw + bias, A, B, C, D=Dk, z=z)
+    assert _rel(yb, yq) < 1e-15 and _rel(sb, sq) < 1e-15
+
+
+def pin_zoh_solves_the_ode(o, seed=9):
+    """With zoh, each step is the exact solution of the continuous system
+    dh/ds = A h + B_t u_t over a step of length dt_t with the input held constant
+    ("Arch 02: Mamba SSM", zero-order hold; "8.7 State Space Models (Mamba)", section 3).
+    Checked against a numerical ODE integration of that system."""
+    from scipy.integrate import solve_ivp
+    rng = np.random.default_rng(seed)
+    L, D, N = 6, 2, 4
+    u = rng.standard_normal((1, L, D))
+    dt = rng.uniform(0.05, 0.8, (1, L, D))
+    A = -rng.uniform(0.2, 3.0, (D, N))
+    B = rng.standard_normal((1, L, N))
+    C = rng.standard_normal((1, L, N))
+    y, last = o.selective_scan_fwd(u, dt, A, B, C, delta_softplus=False, zoh=True)
+    for d in range(D):
+        h = np.zeros(N)
+        for t in range(L):
+            f = lambda s, hh, t=t, d=d: A[d] * hh + B[0, t] * u[0, t, d]
+            h = solve_ivp(f, (0.0, dt[0, t, d]), h, method="DOP853", rtol=1e-12, atol=1e-14).y[:, -1]
+            assert abs(y[0, t, d] - C[0, t] @ h) <= 1e-9 * (1 + abs(y[0, t, d]))
+        assert np.max(np.abs(last[0, d] - h)) <= 1e-9 * (1 + np.max(np.abs(h)))
+
+
+def pin_zoh_limits(o, seed=10):
+    """The zero-order-hold B-bar (exp(dt a) - 1) / a B tends to dt B as dt a -> 0 (the
+    simplification the pages take for Mamba) and equals it where a = 0."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 1, 9, 3, 4
+    u = rng.standard_normal((b, L, D))
+    B = rng.standard_normal((b, L, N))
+    C = rng.standard_normal((b, L, N))
+    A = -rng.uniform(0.5, 2.0, (D, N))
+    A[1, 2] = 0.0
+    dt = rng.uniform(0.5, 1.0, (b, L, D))
+    yz, lz = o.selective_scan_fwd(u, dt, A, B, C, delta_softplus=False, zoh=True)
+    yd, ld = o.selective_scan_fwd(u, dt, A, B, C, delta_softplus=False)
+    assert _rel(lz, ld) > 1e-2  # the two discretisations differ at finite dt
+    A0 = np.zeros_like(A)
+    y0z, l0z = o.selective_scan_fwd(u, dt, A0, B, C, delta_softplus=False, zoh=True)
+    y0d, l0d = o.selective_scan_fwd(u, dt, A0, B, C, delta_softplus=False)
+    assert _rel(y0z, y0d) < 1e-15 and _rel(l0z, l0d) < 1e-15
+    eps = 1e-7
+    ys, ls = o.selective_scan_fwd(u, dt * eps, A, B, C, delta_softplus=False, zoh=True)
+    ysd, lsd = o.selective_scan_fwd(u, dt * eps, A, B, C, delta_softplus=False)
+    assert _rel(ls, lsd) < 1e-6
+    # decode with zoh == one forward step with zoh
+    st0 = rng.standard_normal((b, D, N))
+    ye, se = o.state_update(st0, u[:, 0], dt[:, 0], A, B[:, 0], C[:, 0], zoh=True)
+    yf, sf = o.selective_scan_fwd(u[:, :1], dt[:, :1], A, B[:, :1], C[:, :1], delta_softplus=False, zoh=True, h0=st0)
+    assert _rel(ye, yf[:, 0]) < 1e-14 and _rel(se, sf) < 1e-14
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_delta_zero_holds_state, pin_scalar_closed_form,
             pin_bruteforce_unrolling, pin_large_delta_reset, pin_stability_bound, pin_decode_matches_forward,
-            pin_softplus_silu, pin_scan_operator]
+            pin_softplus_silu, pin_scan_operator, pin_decode_step_map, pin_zoh_solves_the_ode, pin_zoh_limits]

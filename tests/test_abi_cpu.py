@@ -187,3 +187,43 @@ def test_fwd_ws_validation(lib):
     # a workspace overlapping u
     assert lib.ssm_selective_scan_fwd_ws(*args, 1, r("y"), r("last"), ctypes.c_void_p(a["u"].data),
                                          ctypes.c_size_t(64), None) == 4
+
+
+def call_fwd_ex(lib, a, h0, softplus=1, flags=0):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    return lib.ssm_selective_scan_fwd_ex(r("u"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("bias"),
+                                         softplus, None if h0 is None else ctypes.byref(h0), ctypes.c_uint32(flags),
+                                         r("y"), r("last"), None, ctypes.c_size_t(0), None)
+
+
+def test_fwd_ex_validation(lib):
+    a = fwd_args()
+    assert call_fwd_ex(lib, a, T((2, 8, 8), ssm.SSM_F32)) == 2          # wrong N
+    assert call_fwd_ex(lib, a, T((2, 8, 16), ssm.SSM_BF16)) == 3        # start state must be f32
+    h = T((2, 8, 16), ssm.SSM_F32, addr=a["y"].data)                    # overlaps the output y
+    assert call_fwd_ex(lib, a, h) == 4
+    h = T((2, 8, 16), ssm.SSM_F32, addr=a["last"].data + 16)            # partial overlap with last_state
+    assert call_fwd_ex(lib, a, h) == 4
+    e = fwd_args(b=0)                                                    # h0 == last_state exactly: allowed
+    e["last"] = T((0, 8, 16), ssm.SSM_F32)
+    assert call_fwd_ex(lib, e, e["last"]) == 0
+    assert call_fwd_ex(lib, fwd_args(), None, softplus=3) == 5
+    assert call_fwd_ex(lib, fwd_args(), None, flags=2) == 5             # unknown flag bit
+    assert call_fwd_ex(lib, fwd_args(b=0), None, flags=ssm.SSM_FWD_ZOH) == 0
+
+
+def call_dec_ex(lib, a, bias, softplus, flags=0):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    return lib.ssm_state_update_ex(r("state"), r("x"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"),
+                                   None if bias is None else ctypes.byref(bias), softplus, ctypes.c_uint32(flags),
+                                   r("y"), None)
+
+
+def test_decode_ex_validation(lib):
+    a = dec_args()
+    assert call_dec_ex(lib, a, T((9,), ssm.SSM_F32), 1) == 2            # bias is (D)
+    assert call_dec_ex(lib, a, T((8,), ssm.SSM_BF16), 1) == 3           # bias must be f32
+    assert call_dec_ex(lib, a, T((8,), ssm.SSM_F32, addr=a["y"].data), 1) == 4
+    assert call_dec_ex(lib, a, None, 2) == 5
+    assert call_dec_ex(lib, dec_args(b=0), T((8,), ssm.SSM_F32), 1) == 0
+    assert call_dec_ex(lib, dec_args(), None, 0, flags=4) == 5
