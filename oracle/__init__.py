@@ -74,6 +74,8 @@ class Oracle:
         lib.ssm_oracle_state_update.argtypes = [_i64, _i64, _i64] + [_dp] * 9
         lib.ssm_oracle_state_update_ex.restype = ctypes.c_int
         lib.ssm_oracle_state_update_ex.argtypes = [_i64, _i64, _i64] + [_dp] * 9 + [ctypes.c_int, ctypes.c_int, _dp]
+        lib.ssm_oracle_conv1d_silu.restype = ctypes.c_int
+        lib.ssm_oracle_conv1d_silu.argtypes = [_i64, _i64, _i64] + [_dp] * 5
         lib.ssm_oracle_fwd_ex.restype = ctypes.c_int
         lib.ssm_oracle_fwd_ex.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int, ctypes.c_int, _dp, _dp,
                                                                                  _dp, ctypes.c_int]
@@ -113,6 +115,39 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("ssm_oracle_fwd rejected its arguments")
         return y, last
+
+    def conv1d_silu(self, x, w, bias=None, conv_state=None):
+        """u = silu(causal depthwise conv of width 4 (+ bias)) as an fp64 array.
+
+        x: (batch, L, D); w: (D, 4); bias: (D); conv_state: (batch, D, 3), the three
+        inputs before x[:, 0], oldest first (zeros if None).
+        """
+        x = _f64(x)
+        batch, L, Dm = x.shape
+        w = _f64(w, (Dm, 4))
+        bias = _f64(bias, (Dm,))
+        conv_state = _f64(conv_state, (batch, Dm, 3))
+        u = np.empty((batch, L, Dm), np.float64)
+        if self.lib.ssm_oracle_conv1d_silu(batch, L, Dm, _ptr(x), _ptr(w), _ptr(bias), _ptr(conv_state), _ptr(u)):
+            raise RuntimeError("ssm_oracle_conv1d_silu rejected its arguments")
+        return u
+
+    @staticmethod
+    def next_conv_state(x, conv_state=None):
+        """The three inputs before step L (what follows x[:, L-1]): the last three of
+        conv_state followed by x, as (batch, D, 3), oldest first."""
+        x = _f64(x)
+        batch, L, Dm = x.shape
+        prev = np.zeros((batch, Dm, 3)) if conv_state is None else _f64(conv_state, (batch, Dm, 3))
+        seq = np.concatenate([prev, np.transpose(x, (0, 2, 1))], axis=2)
+        return np.ascontiguousarray(seq[:, :, -3:])
+
+    def conv_selective_scan_fwd(self, x, conv_weight, A, B, C, delta, conv_bias=None, conv_state=None, **kw):
+        """The conv + SiLU prologue, then selective_scan_fwd on its output. Returns
+        (y, last_state, next_conv_state)."""
+        u = self.conv1d_silu(x, conv_weight, conv_bias, conv_state)
+        y, last = self.selective_scan_fwd(u, delta, A, B, C, **kw)
+        return y, last, self.next_conv_state(x, conv_state)
 
     def state_update(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
                      zoh=False):
@@ -158,3 +193,15 @@ def selective_scan_fwd(*args, **kwargs):
 
 def state_update(*args, **kwargs):
     return default().state_update(*args, **kwargs)
+
+
+def conv1d_silu(*args, **kwargs):
+    return default().conv1d_silu(*args, **kwargs)
+
+
+def conv_selective_scan_fwd(*args, **kwargs):
+    return default().conv_selective_scan_fwd(*args, **kwargs)
+
+
+def next_conv_state(*args, **kwargs):
+    return Oracle.next_conv_state(*args, **kwargs)

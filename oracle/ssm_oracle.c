@@ -226,3 +226,32 @@ int ssm_oracle_state_update(int64_t batch, int64_t D, int64_t N, double* state,
                             const double* z, double* y) {
   return ssm_oracle_state_update_ex(batch, D, N, state, x, delta, A, B, C, Dskip, z, NULL, 0, 0, y);
 }
+
+/* Causal depthwise convolution of width 4 followed by SiLU: the step before the SSM in
+ * the Mamba block ("Mamba and State Space Models", "The Mamba Block": depthwise Conv1d,
+ * kernel 4, then SiLU; "Mamba and State Space Models" model card: d_conv = 4). For every
+ * (b, t, d):  u = silu(bias[d] + sum_{k=0..3} w[d,k] * x[b, t-3+k, d]), where an input
+ * before t = 0 is conv_state[b, d, 3 + (t-3+k)] (the three inputs that preceded the
+ * sequence, oldest first), or 0 when conv_state is NULL. */
+int ssm_oracle_conv1d_silu(int64_t batch, int64_t L, int64_t D, const double* x, const double* w,
+                           const double* bias, const double* conv_state, double* u) {
+  if (batch < 0 || L < 0 || D < 0) return -1;
+  if (batch * L * D == 0) return 0;
+  if (!x || !w || !u) return -1;
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t t = 0; t < L; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = bias ? bias[d] : 0.0;
+        for (int64_t k = 0; k < 4; ++k) {
+          const int64_t s = t - 3 + k;
+          double xv;
+          if (s >= 0)
+            xv = x[(b * L + s) * D + d];
+          else
+            xv = conv_state ? conv_state[(b * D + d) * 3 + (3 + s)] : 0.0;
+          acc += w[d * 4 + k] * xv;
+        }
+        u[(b * L + t) * D + d] = ssm_oracle_silu(acc);
+      }
+  return 0;
+}

@@ -90,6 +90,16 @@ int ssm_oracle_state_update_ex(int64_t batch, int64_t D, int64_t N, double* stat
                                const double* z, const double* delta_bias, int delta_softplus,
                                int zoh, double* y);
 
+/*
+ * Causal depthwise convolution (width 4) + SiLU, the step before the SSM in the block:
+ *   u[b,t,d] = silu(bias[d] + sum_{k=0..3} w[d,k] * x[b,t-3+k,d])
+ * x, u : (batch, L, D)   w : (D, 4)   bias : (D), nullable
+ * conv_state : (batch, D, 3), nullable -- the three inputs before x[b,0,d], oldest first
+ * (zeros if NULL). Returns 0 on success, -1 on bad arguments.
+ */
+int ssm_oracle_conv1d_silu(int64_t batch, int64_t L, int64_t D, const double* x, const double* w,
+                           const double* bias, const double* conv_state, double* u);
+
 #ifdef __cplusplus
 }
 #endif

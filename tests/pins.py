@@ -357,6 +357,42 @@ def pin_zoh_limits(o, seed=10):
     assert _rel(ye, yf[:, 0]) < 1e-14 and _rel(se, sf) < 1e-14
 
 
+def pin_conv_prologue(o, seed=11):
+    """The causal depthwise width-4 convolution + SiLU before the SSM ("Mamba and State
+    Space Models", "The Mamba Block") against numpy's convolution: u_t uses x_{t-3..t},
+    with the carried conv state (the three inputs before the sequence) or zeros in front;
+    and a sequence cut anywhere continues exactly from the next conv state."""
+    rng = np.random.default_rng(seed)
+    b, L, D = 2, 11, 3
+    x = rng.standard_normal((b, L, D))
+    w = rng.standard_normal((D, 4))
+    bias = rng.standard_normal(D)
+    cs = rng.standard_normal((b, D, 3))
+    for state in (None, cs):
+        u = o.conv1d_silu(x, w, bias, state)
+        for bi in range(b):
+            for d in range(D):
+                front = np.zeros(3) if state is None else state[bi, d]
+                seq = np.concatenate([front, x[bi, :, d]])
+                ref = np.convolve(seq, w[d][::-1])[3:3 + L] + bias[d]
+                assert np.max(np.abs(u[bi, :, d] - _silu(ref))) <= 1e-14 * (1 + np.max(np.abs(ref)))
+    u_all = o.conv1d_silu(x, w, bias, cs)
+    for P in (1, 2, 5):
+        nxt = o.next_conv_state(x[:, :P], cs)
+        u_rest = o.conv1d_silu(x[:, P:], w, bias, nxt)
+        assert np.array_equal(u_rest, u_all[:, P:])
+    assert np.array_equal(o.next_conv_state(x, cs), np.transpose(x[:, -3:], (0, 2, 1)))
+    A = -rng.uniform(0.5, 2.0, (D, 4))
+    Bm = rng.standard_normal((b, L, 4))
+    Cm = rng.standard_normal((b, L, 4))
+    dt = rng.uniform(0.01, 0.5, (b, L, D))
+    y, last, nxt = o.conv_selective_scan_fwd(x, w, A, Bm, Cm, dt, conv_bias=bias, conv_state=cs,
+                                             delta_softplus=False)
+    y2, last2 = o.selective_scan_fwd(u_all, dt, A, Bm, Cm, delta_softplus=False)
+    assert np.array_equal(y, y2) and np.array_equal(last, last2)
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_delta_zero_holds_state, pin_scalar_closed_form,
             pin_bruteforce_unrolling, pin_large_delta_reset, pin_stability_bound, pin_decode_matches_forward,
-            pin_softplus_silu, pin_scan_operator, pin_decode_step_map, pin_zoh_solves_the_ode, pin_zoh_limits]
+            pin_softplus_silu, pin_scan_operator, pin_decode_step_map, pin_zoh_solves_the_ode, pin_zoh_limits,
+            pin_conv_prologue]
