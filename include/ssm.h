@@ -10,6 +10,9 @@
  *   ssm_state_update         the single-token recurrent update used in decoding
  *                            (_ex: with the step-size bias and softplus applied,
  *                            optionally the zero-order-hold B-bar)
+ *   ssm_conv_selective_scan_fwd, ssm_conv_state_update
+ *                            the same two with the block's causal width-4 depthwise
+ *                            conv + SiLU (the step before the SSM) fused in front
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -255,6 +258,57 @@ SSM_API ssm_status_t ssm_state_update_ex(ssm_tensor_t* state, const ssm_tensor_t
                                          const ssm_tensor_t* D, const ssm_tensor_t* z,
                                          const ssm_tensor_t* delta_bias, int delta_softplus,
                                          uint32_t flags, ssm_tensor_t* y, void* stream);
+
+/*
+ * ssm_conv_selective_scan_fwd -- the block's conv prologue fused into the forward pass.
+ * In the Mamba block the SSM input is the output of a causal depthwise convolution of
+ * width 4 followed by SiLU ("Mamba and State Space Models", "The Mamba Block" and the
+ * model card's d_conv = 4; "8.7 State Space Models (Mamba)", section 6). This entry
+ * takes the convolution's INPUT x and computes, for every (b, t, d),
+ *   u[b,t,d] = silu(conv_bias[d] + sum_{k=0..3} conv_weight[d,k] * x[b,t-3+k,d])
+ * on the fly, so u is never written to or read from device memory; everything after
+ * that is ssm_selective_scan_fwd_ex with this u.
+ *
+ *   x            (batch, L, D)  I/O type         the convolution's input
+ *   conv_weight  (D, 4)         f32              tap k multiplies x[t-3+k]
+ *   conv_bias    (D)            f32, nullable
+ *   conv_state   (batch, D, 3)  I/O type, nullable
+ *                read: the three inputs before x[:,0] (oldest first; NULL = zeros);
+ *                then overwritten with the three inputs before step L, i.e. the state
+ *                that continues the sequence here or in ssm_conv_state_update
+ *   delta ... stream            as ssm_selective_scan_fwd_ex (h0, flags, workspace)
+ * conv_state may overlap no other tensor. With bf16 I/O and the channel kernel the
+ * SiLU of the prologue uses the SFU tanh (relative error ~5e-4 on u).
+ */
+SSM_API ssm_status_t ssm_conv_selective_scan_fwd(const ssm_tensor_t* x, const ssm_tensor_t* conv_weight,
+                                                 const ssm_tensor_t* conv_bias, ssm_tensor_t* conv_state,
+                                                 const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                                 const ssm_tensor_t* B, const ssm_tensor_t* C,
+                                                 const ssm_tensor_t* D, const ssm_tensor_t* z,
+                                                 const ssm_tensor_t* delta_bias, int delta_softplus,
+                                                 const ssm_tensor_t* h0, uint32_t flags, ssm_tensor_t* y,
+                                                 ssm_tensor_t* last_state, void* workspace,
+                                                 size_t workspace_bytes, void* stream);
+
+/*
+ * ssm_conv_state_update -- one decode step of the block's conv prologue and the SSM:
+ *   u = silu(conv_bias[d] + w0 cs[0] + w1 cs[1] + w2 cs[2] + w3 x[b,d])   (w = conv_weight[d])
+ *   conv_state[b,d] <- (cs[1], cs[2], x[b,d])                           in place
+ *   then ssm_state_update_ex with u as the token input.
+ *
+ *   conv_state  (batch, D, 3)  I/O type   required; read, then shifted in place
+ *   x           (batch, D)     I/O type   the convolution's input for this token
+ *   conv_weight (D, 4) f32, conv_bias (D) f32 nullable
+ * Everything else as ssm_state_update_ex. conv_state may overlap no other tensor.
+ */
+SSM_API ssm_status_t ssm_conv_state_update(ssm_tensor_t* conv_state, ssm_tensor_t* state,
+                                           const ssm_tensor_t* x, const ssm_tensor_t* conv_weight,
+                                           const ssm_tensor_t* conv_bias, const ssm_tensor_t* delta,
+                                           const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                           const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                           const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                           int delta_softplus, uint32_t flags, ssm_tensor_t* y,
+                                           void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

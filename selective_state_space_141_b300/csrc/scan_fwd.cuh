@@ -31,6 +31,12 @@ struct FwdParams {
   float* last_state;        // nullable
   const float* h0;          // nullable: start state (batch, D, N); zeros when null
   int zoh;                  // 1: B-bar = (exp(dt A) - 1) / A B (general kernel only)
+  // Conv prologue (nullable conv_w = none): u then holds the conv input x and the SSM
+  // input is silu(conv_b + sum_k conv_w[d,k] x[t-3+k]); conv_state (batch, D, 3), I/O
+  // type, nullable: the three inputs before t = 0 (zeros when null).
+  const float* conv_w;
+  const float* conv_b;
+  const void* conv_state;
   int64_t batch, L, D;
   // Sequence segments (channel kernel only): CTA z covers steps [z*seg_len, (z+1)*seg_len).
   // seg_len == L means one segment. seg_h0 (nullable): start state of each segment,
@@ -95,7 +101,22 @@ scan_fwd_generic(const FwdParams p) {
       float uu = 0.f, zz = 0.f, dt = 0.f;
       if (t < tc && d < D) {
         const int64_t ix = (t0 + t) * D + d;
-        uu = to_f32(u[ix]);
+        if (p.conv_w) {  // causal width-4 conv + SiLU of the input x (the block's prologue)
+          float acc = p.conv_b ? p.conv_b[d] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int64_t s = t0 + t - 3 + k;
+            float xv = 0.f;
+            if (s >= 0)
+              xv = to_f32(u[s * D + d]);
+            else if (p.conv_state)
+              xv = to_f32(static_cast<const T*>(p.conv_state)[(b * D + d) * 3 + 3 + s]);
+            acc = fmaf(p.conv_w[d * 4 + k], xv, acc);
+          }
+          uu = silu_precise(acc);
+        } else {
+          uu = to_f32(u[ix]);
+        }
         float r = to_f32(dl[ix]);
         if (p.delta_bias) r += p.delta_bias[d];
         dt = p.delta_softplus ? softplus_precise(r) : r;
@@ -152,6 +173,26 @@ scan_fwd_generic(const FwdParams p) {
 #pragma unroll
     for (int k = 0; k < SPL; ++k) p.last_state[(b * D + dj) * N + g * SPL + k] = h[k];
   }
+}
+
+// The conv state after a sequence: the three inputs before step L, oldest first, from
+// the old state where the sequence is shorter than three. One thread per (b, d); it
+// reads before it writes, so the state is updated in place.
+template <typename T>
+__global__ void __launch_bounds__(256) conv_state_next_kernel(const T* __restrict__ x, T* cs, int64_t batch, int64_t L,
+                                                              int64_t D) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= batch * D) return;
+  const int64_t b = i / D, d = i % D;
+  const T old[3] = {cs[i * 3], cs[i * 3 + 1], cs[i * 3 + 2]};
+  T nw[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int64_t s = L - 3 + j;
+    nw[j] = s >= 0 ? x[(b * L + s) * D + d] : old[j + L];
+  }
+#pragma unroll
+  for (int j = 0; j < 3; ++j) cs[i * 3 + j] = nw[j];
 }
 
 }  // namespace ssm

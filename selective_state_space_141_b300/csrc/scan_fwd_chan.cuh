@@ -91,21 +91,45 @@ __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy
 
 constexpr int kChanSub = 8;  // steps per sub-chunk
 
+// The block's causal depthwise width-4 conv + SiLU computed on the fly ("Mamba and State
+// Space Models", "The Mamba Block"): the u tile then holds the conv input x, and each
+// lane (one channel) keeps its weights and the window of its last three inputs.
+//   u_t = silu(b + w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t)
+struct ConvLane {
+  float2 w0, w1, w2, w3, b;  // each weight twice, for two steps per packed op
+  float x0, x1, x2;          // x_{t-3}, x_{t-2}, x_{t-1}
+};
+
+// u of steps t and t+1 from their inputs xa = x_t, xb = x_{t+1}; advances the window.
+template <bool kConv>
+__device__ __forceinline__ float2 chan_u2(ConvLane& c, float xa, float xb) {
+  if (!kConv) return make_float2(xa, xb);
+  float2 acc = __ffma2_rn(c.w0, make_float2(c.x0, c.x1), c.b);
+  acc = __ffma2_rn(c.w1, make_float2(c.x1, c.x2), acc);
+  acc = __ffma2_rn(c.w2, make_float2(c.x2, xa), acc);
+  acc = __ffma2_rn(c.w3, make_float2(xa, xb), acc);
+  c.x0 = c.x2;
+  c.x1 = xa;
+  c.x2 = xb;
+  return silu2_fast(acc);
+}
+
 // kChanSub steps of one lane (one channel, all N states), in three phases so that one
 // warp per SM sub-partition finds independent work: (1) step sizes (independent
 // softplus chains, two steps per packed op), (2) the recurrence (only h carries from
 // step to step), (3) D skip, gate and y staging (two steps per packed op).
 // kTail: steps at or past tc get dt = 0 and no input, so exp(0) = 1 exactly leaves h
 // bit-for-bit unchanged (selects, not multiplies; those rows hold zero fill).
-template <typename TY, int N, bool kSoftplus, bool kGate, bool kTail>
+template <typename TY, int N, bool kSoftplus, bool kGate, bool kTail, bool kConv>
 __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __nv_bfloat16* sd,
                                               const __nv_bfloat16* sz, const float* bc, TY* yt, int t0, int tc,
-                                              float bias, float Dk, const float2 (&A2)[N / 2], float2 (&h)[N / 2]) {
+                                              float bias, float Dk, const float2 (&A2)[N / 2], float2 (&h)[N / 2],
+                                              ConvLane& cv) {
   float2 u2[kChanSub / 2], dt2[kChanSub / 2], du2[kChanSub / 2], y2[kChanSub / 2];
 #pragma unroll
   for (int i = 0; i < kChanSub / 2; ++i) {
     const int t = t0 + 2 * i;
-    u2[i] = make_float2(__bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
+    u2[i] = chan_u2<kConv>(cv, __bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
     const float2 r = __fadd2_rn(make_float2(__bfloat162float(sd[t * kChanCTA]), __bfloat162float(sd[(t + 1) * kChanCTA])),
                                 make_float2(bias, bias));
     float2 d = kSoftplus ? softplus2_fast(r) : r;
@@ -155,15 +179,15 @@ __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __n
 // Aggregate pass over kChanSub steps: the recurrence from the given state without the
 // read-out (no C, no y), plus the running sum of dt, from which the decay product of a
 // whole segment is exp(A * sum dt). Same tail rule as chan_subchunk.
-template <int N, bool kSoftplus, bool kTail>
+template <int N, bool kSoftplus, bool kTail, bool kConv>
 __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const __nv_bfloat16* sd, const float* bc,
                                                   int t0, int tc, float bias, const float2 (&A2)[N / 2],
-                                                  float2 (&h)[N / 2], float& sdt) {
+                                                  float2 (&h)[N / 2], float& sdt, ConvLane& cv) {
   float2 dt2[kChanSub / 2], du2[kChanSub / 2];
 #pragma unroll
   for (int i = 0; i < kChanSub / 2; ++i) {
     const int t = t0 + 2 * i;
-    const float2 u2 = make_float2(__bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
+    const float2 u2 = chan_u2<kConv>(cv, __bfloat162float(su[t * kChanCTA]), __bfloat162float(su[(t + 1) * kChanCTA]));
     const float2 r = __fadd2_rn(make_float2(__bfloat162float(sd[t * kChanCTA]), __bfloat162float(sd[(t + 1) * kChanCTA])),
                                 make_float2(bias, bias));
     float2 d = kSoftplus ? softplus2_fast(r) : r;
@@ -195,7 +219,8 @@ __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const
 // kAgg = false: the full pass (y, and last_state from the last segment).
 // kAgg = true:  the aggregate pass of a segmented scan (seg_E, seg_P; no y).
 // blockIdx = (channel block of 128, batch row, sequence segment).
-template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg>
+// kConv: the u tensor holds the conv input x; u is its causal conv + SiLU (ConvLane).
+template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg, bool kConv>
 __global__ void __launch_bounds__(kChanThreads, 1)
 scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -297,6 +322,29 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
   unsigned char* ywarp = ytiles + warp * 2 * Lay::kTileY;  // this warp's two y tiles
   float sdt = 0.f;
+  ConvLane cv{};
+  if (kConv && vd) {
+    const float* w = p.conv_w + d * 4;
+    cv.w0 = make_float2(w[0], w[0]);
+    cv.w1 = make_float2(w[1], w[1]);
+    cv.w2 = make_float2(w[2], w[2]);
+    cv.w3 = make_float2(w[3], w[3]);
+    const float cb = p.conv_b ? p.conv_b[d] : 0.f;
+    cv.b = make_float2(cb, cb);
+    float xw[3] = {0.f, 0.f, 0.f};
+    if (seg == 0) {  // the three inputs before the sequence: the carried conv state, or zeros
+      if (p.conv_state) {
+        const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(p.conv_state) + ((int64_t)b * D + d) * 3;
+        for (int k = 0; k < 3; ++k) xw[k] = __bfloat162float(cs[k]);
+      }
+    } else {  // a later segment: the three inputs before its first step
+      const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.u);
+      for (int k = 0; k < 3; ++k) xw[k] = __bfloat162float(x[((int64_t)b * L + t_begin - 3 + k) * D + d]);
+    }
+    cv.x0 = xw[0];
+    cv.x1 = xw[1];
+    cv.x2 = xw[2];
+  }
 
   for (int k = 0; k < nchunks; ++k) {
     const int s = k % S;
@@ -312,9 +360,9 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     const int tc = (int)((t_end - tk) < TC ? (t_end - tk) : TC);
     if (kAgg) {
       if (tc == TC) {
-        for (int t0 = 0; t0 < TC; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, false>(su, sd, bc, t0, tc, bias, A2, h, sdt);
+        for (int t0 = 0; t0 < TC; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, false, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
       } else {
-        for (int t0 = 0; t0 < tc; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, true>(su, sd, bc, t0, tc, bias, A2, h, sdt);
+        for (int t0 = 0; t0 < tc; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, true, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -329,10 +377,10 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     }
     if (tc == TC) {
       for (int t0 = 0; t0 < TC; t0 += kChanSub)
-        chan_subchunk<TY, N, kSoftplus, kGate, false>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
+        chan_subchunk<TY, N, kSoftplus, kGate, false, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
     } else {
       for (int t0 = 0; t0 < tc; t0 += kChanSub)
-        chan_subchunk<TY, N, kSoftplus, kGate, true>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h);
+        chan_subchunk<TY, N, kSoftplus, kGate, true, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
     }
     // Release the input stage, then send this chunk's y tile (rows past L and columns
     // past D are clipped by the TMA store; segments start on chunk boundaries).

@@ -126,9 +126,9 @@ bool chan_eligible(const FwdParams& p, int64_t N) {
          aligned16(p.last_state) && encode_fn() != nullptr;
 }
 
-template <typename TY, int N, bool kSP, bool kZ, bool kAgg>
+template <typename TY, int N, bool kSP, bool kZ, bool kAgg, bool kConv>
 cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st) {
-  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg>;
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg, kConv>;
   constexpr int smem = ssm::chan_smem_bytes<TY, N, kChanTC, kChanStages>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -176,6 +176,22 @@ SegPlan plan_segments(int64_t batch, int64_t L, int64_t D, int64_t N) {
   return sp;
 }
 
+// Run-time switches (softplus, gate, conv prologue) to template arguments. The
+// aggregate pass never gates.
+template <typename TY, int N, bool kAgg, bool kConv>
+cudaError_t launch_chan_sz(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st, bool sp, bool z) {
+  if (kAgg) z = false;
+  if (sp && z) return launch_chan_k<TY, N, true, !kAgg, kAgg, kConv>(p, maps, nseg, st);
+  if (sp) return launch_chan_k<TY, N, true, false, kAgg, kConv>(p, maps, nseg, st);
+  if (z) return launch_chan_k<TY, N, false, !kAgg, kAgg, kConv>(p, maps, nseg, st);
+  return launch_chan_k<TY, N, false, false, kAgg, kConv>(p, maps, nseg, st);
+}
+template <typename TY, int N, bool kAgg>
+cudaError_t launch_chan_sw(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st, bool sp, bool z) {
+  return p.conv_w ? launch_chan_sz<TY, N, kAgg, true>(p, maps, nseg, st, sp, z)
+                  : launch_chan_sz<TY, N, kAgg, false>(p, maps, nseg, st, sp, z);
+}
+
 template <typename TY, int N>
 cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cudaStream_t st, bool* launched) {
   *launched = false;
@@ -212,8 +228,7 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     p.seg_h0 = nullptr;  // the aggregate pass runs every segment from zero; h0 enters in the carry scan
     p.seg_E = E;
     p.seg_P = P;
-    cudaError_t e = sp ? launch_chan_k<__nv_bfloat16, N, true, false, true>(p, maps, nseg - 1, st)
-                       : launch_chan_k<__nv_bfloat16, N, false, false, true>(p, maps, nseg - 1, st);
+    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
     if (e != cudaSuccess) return e;
     const int64_t nbdn = p0.batch * p0.D * N;
     const float* h0 = p0.h0;
@@ -224,10 +239,7 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     p.seg_h0 = H;
     p.seg_E = p.seg_P = nullptr;
   }
-  if (sp && z) return launch_chan_k<TY, N, true, true, false>(p, maps, nseg, st);
-  if (sp) return launch_chan_k<TY, N, true, false, false>(p, maps, nseg, st);
-  if (z) return launch_chan_k<TY, N, false, true, false>(p, maps, nseg, st);
-  return launch_chan_k<TY, N, false, false, false>(p, maps, nseg, st);
+  return launch_chan_sw<TY, N, false>(p, maps, nseg, st, sp, z);
 }
 
 template <typename TY>
@@ -299,11 +311,45 @@ const char* ssm_status_string(ssm_status_t s) {
 
 namespace {
 
+// The conv prologue's tensors (all null = no prologue).
+struct ConvArgs {
+  const ssm_tensor_t* w = nullptr;  // (D, 4) f32
+  const ssm_tensor_t* b = nullptr;  // (D) f32, nullable
+  ssm_tensor_t* state = nullptr;    // (batch, D, 3) I/O type, nullable: read, then overwritten
+};
+
+ssm_status_t check_conv(const ConvArgs* c, int64_t batch, int64_t Dm, ssm_dtype_t io) {
+  ssm_status_t s;
+  if ((s = check_tensor(c->w, {Dm, 4})) != SSM_OK) return s;
+  if (c->b && (s = check_tensor(c->b, {Dm})) != SSM_OK) return s;
+  if (c->state && (s = check_tensor(c->state, {batch, Dm, 3})) != SSM_OK) return s;
+  if (c->w->dtype != SSM_F32 || (c->b && c->b->dtype != SSM_F32) || (c->state && c->state->dtype != io))
+    return SSM_ERR_DTYPE;
+  return SSM_OK;
+}
+
+// After the scan: the conv state moves on to the last three inputs (stream order puts
+// this after every read of the old state).
+ssm_status_t finish_fwd(cudaError_t e, const FwdParams& p, ssm_dtype_t io, ssm_tensor_t* conv_state, cudaStream_t st) {
+  if (e == cudaSuccess && conv_state) {
+    const int64_t n = p.batch * p.D;
+    dim3 grid((unsigned)((n + 255) / 256)), block(256);
+    int64_t batch = p.batch, L = p.L, D = p.D;
+    const void* x = p.u;
+    void* cs = conv_state->data;
+    void* args[] = {&x, &cs, &batch, &L, &D};
+    const void* kern = io == SSM_F32 ? reinterpret_cast<const void*>(&ssm::conv_state_next_kernel<float>)
+                                     : reinterpret_cast<const void*>(&ssm::conv_state_next_kernel<__nv_bfloat16>);
+    e = cudaLaunchKernel(kern, grid, block, args, 0, st);
+  }
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
                       const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
                       const ssm_tensor_t* delta_bias, int delta_softplus, const ssm_tensor_t* h0, uint32_t flags,
                       ssm_tensor_t* y, ssm_tensor_t* last_state, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      void* stream, const ConvArgs* conv = nullptr) {
   if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
   const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
@@ -332,7 +378,17 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
   if (batch > 65535) return SSM_ERR_UNSUPPORTED;
 
-  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias, h0};
+  if (conv && (s = check_conv(conv, batch, Dm, io)) != SSM_OK) return s;
+  const ssm_tensor_t* cw = conv ? conv->w : nullptr;
+  const ssm_tensor_t* cb = conv ? conv->b : nullptr;
+  ssm_tensor_t* cst = conv ? conv->state : nullptr;
+  if (cst) {  // in/out: it may overlap nothing else
+    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, h0, y, last_state, cw, cb};
+    for (const ssm_tensor_t* t : all)
+      if (overlaps(cst, t)) return SSM_ERR_LAYOUT;
+  }
+
+  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias, h0, cw, cb};
   // last_state may be exactly the h0 buffer (read first, then overwritten by the same thread).
   const bool state_in_place = h0 && last_state && h0->data == last_state->data;
   for (const ssm_tensor_t* in : ins) {
@@ -346,7 +402,7 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     w.dtype = SSM_F32;
     w.ndim = 1;
     w.shape[0] = (int64_t)(workspace_bytes / 4);
-    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, h0, y, last_state};
+    const ssm_tensor_t* all[] = {u, delta, A, B, C, D, z, delta_bias, h0, y, last_state, cw, cb, cst};
     for (const ssm_tensor_t* t : all)
       if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
   }
@@ -377,6 +433,9 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.last_state = last_state ? static_cast<float*>(last_state->data) : nullptr;
   p.h0 = h0 ? static_cast<const float*>(h0->data) : nullptr;
   p.zoh = (flags & SSM_FWD_ZOH) ? 1 : 0;
+  p.conv_w = cw ? static_cast<const float*>(cw->data) : nullptr;
+  p.conv_b = cb ? static_cast<const float*>(cb->data) : nullptr;
+  p.conv_state = cst ? cst->data : nullptr;
   p.batch = batch;
   p.L = L;
   p.D = Dm;
@@ -395,7 +454,7 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     bool launched = false;
     e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, plan, use_ws ? workspace : nullptr, st, &launched)
                              : launch_chan_n<float>(N, p, plan, use_ws ? workspace : nullptr, st, &launched);
-    if (launched || e != cudaSuccess) return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    if (launched || e != cudaSuccess) return finish_fwd(e, p, io, cst, st);
   }
   if (io == SSM_F32)
     e = launch_fwd_n<float, float>(N, p, st);
@@ -403,7 +462,7 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     e = launch_fwd_n<__nv_bfloat16, __nv_bfloat16>(N, p, st);
   else
     e = launch_fwd_n<__nv_bfloat16, float>(N, p, st);
-  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return finish_fwd(e, p, io, cst, st);
 }
 
 }  // namespace
@@ -453,8 +512,9 @@ namespace {
 ssm_status_t dec_impl(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tensor_t* delta, const ssm_tensor_t* A,
                       const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
                       const ssm_tensor_t* delta_bias, int delta_softplus, uint32_t flags, ssm_tensor_t* y,
-                      void* stream) {
+                      void* stream, const ConvArgs* conv = nullptr) {
   if (!state || !x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+  if (conv && (!conv->w || !conv->state)) return SSM_ERR_NULL;
   if (state->ndim != 3) return SSM_ERR_SHAPE;
   const int64_t batch = state->shape[0], Dm = state->shape[1], N = state->shape[2];
   if (batch < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
@@ -480,12 +540,18 @@ ssm_status_t dec_impl(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tens
   if ((flags & ~SSM_FWD_ZOH) != 0) return SSM_ERR_UNSUPPORTED;
   if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
 
-  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, z, delta_bias};
+  if (conv && (s = check_conv(conv, batch, Dm, io)) != SSM_OK) return s;
+  const ssm_tensor_t* cw = conv ? conv->w : nullptr;
+  const ssm_tensor_t* cb = conv ? conv->b : nullptr;
+  ssm_tensor_t* cst = conv ? conv->state : nullptr;
+  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, z, delta_bias, cw, cb};
   for (const ssm_tensor_t* in : ins) {
     if (overlaps(y, in)) return SSM_ERR_LAYOUT;
     if (overlaps(state, in)) return SSM_ERR_LAYOUT;
+    if (cst && overlaps(cst, in)) return SSM_ERR_LAYOUT;
   }
   if (overlaps(state, y)) return SSM_ERR_LAYOUT;
+  if (cst && (overlaps(cst, y) || overlaps(cst, state))) return SSM_ERR_LAYOUT;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (batch == 0 || Dm == 0) return SSM_OK;
@@ -503,6 +569,9 @@ ssm_status_t dec_impl(ssm_tensor_t* state, const ssm_tensor_t* x, const ssm_tens
   p.delta_bias = delta_bias ? static_cast<const float*>(delta_bias->data) : nullptr;
   p.delta_softplus = delta_softplus;
   p.zoh = (flags & SSM_FWD_ZOH) ? 1 : 0;
+  p.conv_w = cw ? static_cast<const float*>(cw->data) : nullptr;
+  p.conv_b = cb ? static_cast<const float*>(cb->data) : nullptr;
+  p.conv_state = cst ? cst->data : nullptr;
   p.batch = batch;
   p.D = Dm;
 
@@ -528,6 +597,37 @@ ssm_status_t ssm_state_update_ex(ssm_tensor_t* state, const ssm_tensor_t* x, con
                                  const ssm_tensor_t* D, const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
                                  int delta_softplus, uint32_t flags, ssm_tensor_t* y, void* stream) {
   return dec_impl(state, x, delta, A, B, C, D, z, delta_bias, delta_softplus, flags, y, stream);
+}
+
+ssm_status_t ssm_conv_selective_scan_fwd(const ssm_tensor_t* x, const ssm_tensor_t* conv_weight,
+                                         const ssm_tensor_t* conv_bias, ssm_tensor_t* conv_state,
+                                         const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                         const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
+                                         const ssm_tensor_t* delta_bias, int delta_softplus, const ssm_tensor_t* h0,
+                                         uint32_t flags, ssm_tensor_t* y, ssm_tensor_t* last_state, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!conv_weight) return SSM_ERR_NULL;
+  if (workspace_bytes > 0 && !workspace) return SSM_ERR_NULL;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SSM_ERR_LAYOUT;
+  ConvArgs c;
+  c.w = conv_weight;
+  c.b = conv_bias;
+  c.state = conv_state;
+  return fwd_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, flags, y, last_state, workspace,
+                  workspace_bytes, stream, &c);
+}
+
+ssm_status_t ssm_conv_state_update(ssm_tensor_t* conv_state, ssm_tensor_t* state, const ssm_tensor_t* x,
+                                   const ssm_tensor_t* conv_weight, const ssm_tensor_t* conv_bias,
+                                   const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                   const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
+                                   const ssm_tensor_t* delta_bias, int delta_softplus, uint32_t flags,
+                                   ssm_tensor_t* y, void* stream) {
+  ConvArgs c;
+  c.w = conv_weight;
+  c.b = conv_bias;
+  c.state = conv_state;
+  return dec_impl(state, x, delta, A, B, C, D, z, delta_bias, delta_softplus, flags, y, stream, &c);
 }
 
 ssm_status_t ssm_device_error(void* stream, int32_t* code) {

@@ -28,6 +28,12 @@ struct DecodeParams {
   const float* delta_bias;  // nullable: added to delta
   int delta_softplus;       // 1: dt = softplus(delta + bias)
   int zoh;                  // 1: B-bar = (exp(dt A) - 1) / A B instead of dt B
+  // Conv prologue (nullable conv_w = none): x is the conv input; the SSM input is
+  // silu(conv_b + w0 cs0 + w1 cs1 + w2 cs2 + w3 x) with conv_state (batch, D, 3), I/O
+  // type, the previous three inputs oldest first, shifted in place to (cs1, cs2, x).
+  const float* conv_w;
+  const float* conv_b;
+  void* conv_state;
   int64_t batch, D;
 };
 
@@ -51,6 +57,16 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
     const T* Bp = static_cast<const T*>(p.B) + b * N + g * 4;
     const T* Cp = static_cast<const T*>(p.C) + b * N + g * 4;
     x = to_f32(xp[bd]);
+    if (p.conv_w) {  // the block's causal conv + SiLU over (cs0, cs1, cs2, x)
+      const T* cs = static_cast<const T*>(p.conv_state) + bd * 3;
+      const float* w = p.conv_w + d * 4;
+      float c = p.conv_b ? p.conv_b[d] : 0.f;
+      c = fmaf(w[0], to_f32(cs[0]), c);
+      c = fmaf(w[1], to_f32(cs[1]), c);
+      c = fmaf(w[2], to_f32(cs[2]), c);
+      c = fmaf(w[3], x, c);
+      x = silu_precise(c);
+    }
     float dt = to_f32(dp[bd]);
     if (p.delta_bias) dt += p.delta_bias[d];
     if (p.delta_softplus) dt = softplus_precise(dt);
@@ -71,6 +87,14 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
   }
 #pragma unroll
   for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  __syncwarp();  // every lane of a channel has read the conv state before it is shifted
+  if (v && g == 0 && p.conv_w) {
+    T* cs = static_cast<T*>(p.conv_state) + bd * 3;
+    const T c1 = cs[1], c2 = cs[2];
+    cs[0] = c1;
+    cs[1] = c2;
+    cs[2] = static_cast<const T*>(p.x)[bd];
+  }
   if (v && g == 0) {
     float out = acc;
     if (p.Dskip) out = fmaf(p.Dskip[d], x, out);

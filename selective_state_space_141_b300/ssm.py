@@ -64,6 +64,11 @@ def load_library(path: str | None = None):
                                                           ctypes.c_size_t, ctypes.c_void_p]
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = [_P] * 9 + [ctypes.c_void_p]
+    lib.ssm_conv_selective_scan_fwd.restype = ctypes.c_int
+    lib.ssm_conv_selective_scan_fwd.argtypes = [_P] * 11 + [ctypes.c_int, _P, ctypes.c_uint32, _P, _P, ctypes.c_void_p,
+                                                            ctypes.c_size_t, ctypes.c_void_p]
+    lib.ssm_conv_state_update.restype = ctypes.c_int
+    lib.ssm_conv_state_update.argtypes = [_P] * 12 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_state_update_ex.restype = ctypes.c_int
     lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -164,6 +169,51 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     if st != 0:
         raise SsmError(st, "ssm_selective_scan_fwd_ws")
     return y, last_state
+
+
+def conv_selective_scan_fwd(x, conv_weight, delta, A, B, C, conv_bias=None, conv_state=None, D=None, z=None,
+                            delta_bias=None, delta_softplus=True, h0=None, zoh=False, y=None, last_state=None,
+                            return_last_state=True, y_dtype=None, stream=None, workspace=None, use_workspace=True):
+    """The block's causal width-4 depthwise conv + SiLU fused in front of the forward pass
+    (``ssm_conv_selective_scan_fwd``): x (batch, L, D) is the conv input, conv_weight (D, 4)
+    fp32, conv_bias (D) fp32. ``conv_state`` (batch, D, 3), I/O dtype, holds the three
+    inputs before x[:, 0] and is overwritten with the three before step L (None: zeros, not
+    returned). Other arguments as ``selective_scan_fwd``. Returns (y, last_state)."""
+    lib = load_library()
+    if y is None:
+        y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((x.shape[0], x.shape[2], A.shape[-1]), dtype=torch.float32, device=x.device)
+    if workspace is None and use_workspace:
+        nbytes = workspace_size(x.shape[0], x.shape[1], x.shape[2], A.shape[-1])
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
+    ds = [describe(t) for t in (x, conv_weight, conv_bias, conv_state, delta, A, B, C, D, z, delta_bias)]
+    st = lib.ssm_conv_selective_scan_fwd(*[_ref(d) for d in ds], int(bool(delta_softplus)), _ref(describe(h0)),
+                                         ctypes.c_uint32(SSM_FWD_ZOH if zoh else 0), _ref(describe(y)),
+                                         _ref(describe(last_state)), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes),
+                                         _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_conv_selective_scan_fwd")
+    return y, last_state
+
+
+def conv_state_update(conv_state, state, x, conv_weight, delta, A, B, C, conv_bias=None, D=None, z=None,
+                      delta_bias=None, delta_softplus=True, zoh=False, y=None, y_dtype=None, stream=None):
+    """One decode step with the conv prologue (``ssm_conv_state_update``): conv_state
+    (batch, D, 3) and state (batch, D, N) are updated in place; x (batch, D) is the conv
+    input of this token. Returns y (batch, D)."""
+    lib = load_library()
+    if y is None:
+        y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
+    ds = [describe(t) for t in (conv_state, state, x, conv_weight, conv_bias, delta, A, B, C, D, z, delta_bias)]
+    st = lib.ssm_conv_state_update(*[_ref(d) for d in ds], int(bool(delta_softplus)),
+                                   ctypes.c_uint32(SSM_FWD_ZOH if zoh else 0), _ref(describe(y)), _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_conv_state_update")
+    return y
 
 
 def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, y_dtype=None, stream=None, delta_bias=None,

@@ -227,3 +227,40 @@ def test_decode_ex_validation(lib):
     assert call_dec_ex(lib, a, None, 2) == 5
     assert call_dec_ex(lib, dec_args(b=0), T((8,), ssm.SSM_F32), 1) == 0
     assert call_dec_ex(lib, dec_args(), None, 0, flags=4) == 5
+
+
+def call_conv_fwd(lib, a, w, cb, cs, softplus=1):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    o = lambda t: None if t is None else ctypes.byref(t)
+    return lib.ssm_conv_selective_scan_fwd(r("u"), o(w), o(cb), o(cs), r("delta"), r("A"), r("B"), r("C"), r("D"),
+                                           r("z"), r("bias"), softplus, None, ctypes.c_uint32(0), r("y"), r("last"),
+                                           None, ctypes.c_size_t(0), None)
+
+
+def test_conv_fwd_validation(lib):
+    a = fwd_args()  # batch 2, L 5, D 8, bf16
+    w, cb, cs = T((8, 4), ssm.SSM_F32), T((8,), ssm.SSM_F32), T((2, 8, 3))
+    assert call_conv_fwd(lib, a, None, cb, cs) == 1                          # weights are required
+    assert call_conv_fwd(lib, a, T((8, 3), ssm.SSM_F32), cb, cs) == 2       # width must be 4
+    assert call_conv_fwd(lib, a, w, T((9,), ssm.SSM_F32), cs) == 2
+    assert call_conv_fwd(lib, a, w, cb, T((2, 8, 4))) == 2                  # state holds 3 inputs
+    assert call_conv_fwd(lib, a, T((8, 4), ssm.SSM_BF16), cb, cs) == 3      # weights are f32
+    assert call_conv_fwd(lib, a, w, cb, T((2, 8, 3), ssm.SSM_F32)) == 3     # state has the I/O type
+    assert call_conv_fwd(lib, a, w, cb, T((2, 8, 3), addr=a["y"].data)) == 4   # state overlaps y
+    assert call_conv_fwd(lib, a, w, cb, T((2, 8, 3), addr=a["u"].data)) == 4   # state overlaps x
+    assert call_conv_fwd(lib, fwd_args(b=0), w, cb, T((0, 8, 3))) == 0
+
+
+def test_conv_decode_validation(lib):
+    a = dec_args()  # batch 3, D 8, bf16
+    w, cs = T((8, 4), ssm.SSM_F32), T((3, 8, 3))
+    r = lambda k: ctypes.byref(a[k])
+    call = lambda cs_, w_: lib.ssm_conv_state_update(None if cs_ is None else ctypes.byref(cs_), r("state"), r("x"),
+                                                     None if w_ is None else ctypes.byref(w_), None, r("delta"),
+                                                     r("A"), r("B"), r("C"), r("D"), r("z"), None, 1,
+                                                     ctypes.c_uint32(0), r("y"), None)
+    assert call(None, w) == 1
+    assert call(cs, None) == 1
+    assert call(T((3, 8, 2)), w) == 2
+    assert call(cs, T((8, 5), ssm.SSM_F32)) == 2
+    assert call(T((3, 8, 3), addr=a["state"].data), w) == 4
