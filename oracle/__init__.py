@@ -76,6 +76,8 @@ class Oracle:
         lib.ssm_oracle_state_update_ex.argtypes = [_i64, _i64, _i64] + [_dp] * 9 + [ctypes.c_int, ctypes.c_int, _dp]
         lib.ssm_oracle_conv1d_silu.restype = ctypes.c_int
         lib.ssm_oracle_conv1d_silu.argtypes = [_i64, _i64, _i64] + [_dp] * 5
+        lib.ssm_oracle_bwd.restype = ctypes.c_int
+        lib.ssm_oracle_bwd.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12
         lib.ssm_oracle_fwd_ex.restype = ctypes.c_int
         lib.ssm_oracle_fwd_ex.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int, ctypes.c_int, _dp, _dp,
                                                                                  _dp, ctypes.c_int]
@@ -115,6 +117,39 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("ssm_oracle_fwd rejected its arguments")
         return y, last
+
+    def selective_scan_bwd(self, u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
+                           h0=None, dlast=None):
+        """Gradients of sum(dy * y) + sum(dlast * last_state) of selective_scan_fwd (dt B
+        discretisation). Returns a dict of fp64 arrays: du, ddelta, dA, dB, dC and, when
+        the matching input is given, dD, dz, dbias, dh0."""
+        u = _f64(u)
+        batch, L, Dm = u.shape
+        A = _f64(A)
+        N = A.shape[1]
+        delta = _f64(delta, (batch, L, Dm))
+        B = _f64(B, (batch, L, N))
+        C = _f64(C, (batch, L, N))
+        D = _f64(D, (Dm,))
+        z = _f64(z, (batch, L, Dm))
+        delta_bias = _f64(delta_bias, (Dm,))
+        h0 = _f64(h0, (batch, Dm, N))
+        dy = _f64(dy, (batch, L, Dm))
+        dlast = _f64(dlast, (batch, Dm, N))
+        out = dict(du=np.empty((batch, L, Dm)), ddelta=np.empty((batch, L, Dm)), dA=np.empty((Dm, N)),
+                   dB=np.empty((batch, L, N)), dC=np.empty((batch, L, N)))
+        out["dD"] = np.empty(Dm) if D is not None else None
+        out["dz"] = np.empty((batch, L, Dm)) if z is not None else None
+        out["dbias"] = np.empty(Dm) if delta_bias is not None else None
+        out["dh0"] = np.empty((batch, Dm, N)) if h0 is not None else None
+        rc = self.lib.ssm_oracle_bwd(batch, L, Dm, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dy),
+                                     _ptr(dlast), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                                     _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                                     _ptr(out["dbias"]), _ptr(out["dh0"]))
+        if rc != 0:
+            raise RuntimeError("ssm_oracle_bwd rejected its arguments")
+        return {k: v for k, v in out.items() if v is not None}
 
     def conv1d_silu(self, x, w, bias=None, conv_state=None):
         """u = silu(causal depthwise conv of width 4 (+ bias)) as an fp64 array.
@@ -197,6 +232,10 @@ def state_update(*args, **kwargs):
 
 def conv1d_silu(*args, **kwargs):
     return default().conv1d_silu(*args, **kwargs)
+
+
+def selective_scan_bwd(*args, **kwargs):
+    return default().selective_scan_bwd(*args, **kwargs)
 
 
 def conv_selective_scan_fwd(*args, **kwargs):

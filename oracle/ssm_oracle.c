@@ -255,3 +255,94 @@ int ssm_oracle_conv1d_silu(int64_t batch, int64_t L, int64_t D, const double* x,
       }
   return 0;
 }
+
+/* d silu(z) / dz = sigma(z) (1 + z (1 - sigma(z))). */
+static double silu_grad(double z) {
+  const double sg = 1.0 / (1.0 + exp(-z));
+  return sg * (1.0 + z * (1.0 - sg));
+}
+
+/* Backward pass of ssm_oracle_fwd (Delta * B discretisation), the chain rule applied to
+ * the recurrence in reverse time with every h_t kept from a forward sweep. For one
+ * channel, with g = dL/dh_t (starting from dlast at t = L-1):
+ *   dv   = dy_t silu(z_t)              dz_t = dy_t v_t silu'(z_t)      dD += dv u_t
+ *   g   += dv C_t                      dC_t += dv h_t
+ *   dB_t += g dt u_t                   du_t  = dv D + sum_n g dt B_t
+ *   d(dt) = sum_n g (B_t u_t + A a_t h_{t-1})      dA += g a_t h_{t-1} dt
+ *   ddelta_t = d(dt) * (softplus ? sigmoid(r_t) : 1)                  dbias += ddelta_t
+ *   g   *= a_t                          (dL/dh_{t-1}; after t = 0 it is dL/dh0)
+ * dA, dB, dC, dD, dbias accumulate over channels and batch rows and are zeroed here. */
+int ssm_oracle_bwd(int64_t batch, int64_t L, int64_t D, int64_t N,
+                   const double* u, const double* delta, const double* A,
+                   const double* B, const double* C, const double* Dskip,
+                   const double* z, const double* delta_bias, int delta_softplus,
+                   const double* h0, const double* dy, const double* dlast,
+                   double* du, double* ddelta, double* dA, double* dB, double* dC,
+                   double* dD, double* dz, double* dbias, double* dh0) {
+  if (batch < 0 || L < 0 || D < 0 || N <= 0) return -1;
+  if (!A || !dA) return -1;
+  if (L > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)) return -1;
+  for (int64_t i = 0; i < D * N; ++i) dA[i] = 0.0;
+  for (int64_t i = 0; i < batch * L * N; ++i) dB[i] = dC[i] = 0.0;
+  if (dD) for (int64_t i = 0; i < D; ++i) dD[i] = 0.0;
+  if (dbias) for (int64_t i = 0; i < D; ++i) dbias[i] = 0.0;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N)); /* h_{-1} .. h_{L-1} */
+  double* dts = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  double* rs = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  double* g = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!hs || !dts || !rs || !g) {
+    free(hs); free(dts); free(rs); free(g);
+    return -1;
+  }
+  for (int64_t b = 0; b < batch; ++b) {
+    for (int64_t d = 0; d < D; ++d) {
+      /* forward sweep, keeping every state */
+      for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        const int64_t ix = (b * L + t) * D + d, ixn = (b * L + t) * N;
+        const double r = delta[ix] + (delta_bias ? delta_bias[d] : 0.0);
+        const double dt = delta_softplus ? ssm_oracle_softplus(r) : r;
+        rs[t] = r;
+        dts[t] = dt;
+        for (int64_t n = 0; n < N; ++n)
+          hs[(t + 1) * N + n] = exp(dt * A[d * N + n]) * hs[t * N + n] + dt * B[ixn + n] * u[ix];
+      }
+      /* reverse sweep */
+      for (int64_t n = 0; n < N; ++n) g[n] = dlast ? dlast[(b * D + d) * N + n] : 0.0;
+      for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t ix = (b * L + t) * D + d, ixn = (b * L + t) * N;
+        const double dt = dts[t], x = u[ix];
+        const double* ht = &hs[(t + 1) * N];
+        const double* hp = &hs[t * N];
+        double v = Dskip ? Dskip[d] * x : 0.0;
+        for (int64_t n = 0; n < N; ++n) v += C[ixn + n] * ht[n];
+        double dv = dy[ix];
+        if (z) {
+          dz[ix] = dy[ix] * v * silu_grad(z[ix]);
+          dv = dy[ix] * ssm_oracle_silu(z[ix]);
+        }
+        if (dD) dD[d] += dv * x;
+        double dux = Dskip ? dv * Dskip[d] : 0.0, ddt = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          const double An = A[d * N + n];
+          const double a = exp(dt * An);
+          g[n] += dv * C[ixn + n];
+          dC[ixn + n] += dv * ht[n];
+          dB[ixn + n] += g[n] * dt * x;
+          dux += g[n] * dt * B[ixn + n];
+          ddt += g[n] * (B[ixn + n] * x + An * a * hp[n]);
+          dA[d * N + n] += g[n] * a * hp[n] * dt;
+          g[n] *= a;
+        }
+        du[ix] = dux;
+        const double dr = delta_softplus ? ddt / (1.0 + exp(-rs[t])) : ddt;
+        ddelta[ix] = dr;
+        if (dbias) dbias[d] += dr;
+      }
+      if (dh0)
+        for (int64_t n = 0; n < N; ++n) dh0[(b * D + d) * N + n] = g[n];
+    }
+  }
+  free(hs); free(dts); free(rs); free(g);
+  return 0;
+}

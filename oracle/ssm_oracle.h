@@ -100,6 +100,22 @@ int ssm_oracle_state_update_ex(int64_t batch, int64_t D, int64_t N, double* stat
 int ssm_oracle_conv1d_silu(int64_t batch, int64_t L, int64_t D, const double* x, const double* w,
                            const double* bias, const double* conv_state, double* u);
 
+/*
+ * Backward pass of ssm_oracle_fwd (Delta * B discretisation): given dy (batch, L, D) and
+ * dlast (batch, D, N, nullable = 0), the gradients of sum(dy * y) + sum(dlast * last_state)
+ * with respect to every input: du, ddelta, dz (batch, L, D); dB, dC (batch, L, N);
+ * dA (D, N); dD, dbias (D); dh0 (batch, D, N). dD, dz, dbias, dh0 are nullable (needed
+ * only when Dskip, z, delta_bias, h0 are given). Single-threaded; keeps every state of a
+ * channel, so it is meant for small problems. Returns 0, or -1 on bad arguments.
+ */
+int ssm_oracle_bwd(int64_t batch, int64_t L, int64_t D, int64_t N,
+                   const double* u, const double* delta, const double* A,
+                   const double* B, const double* C, const double* Dskip,
+                   const double* z, const double* delta_bias, int delta_softplus,
+                   const double* h0, const double* dy, const double* dlast,
+                   double* du, double* ddelta, double* dA, double* dB, double* dC,
+                   double* dD, double* dz, double* dbias, double* dh0);
+
 #ifdef __cplusplus
 }
 #endif

@@ -392,7 +392,45 @@ def pin_conv_prologue(o, seed=11):
     assert np.array_equal(y, y2) and np.array_equal(last, last2)
 
 
+def pin_backward_finite_differences(o, seed=12):
+    """The backward pass against central finite differences of the forward pass: for the
+    loss sum(dy * y) + sum(dlast * last_state), every element of every input."""
+    rng = np.random.default_rng(seed)
+    b, L, D, N = 2, 7, 3, 4
+    base = dict(u=rng.standard_normal((b, L, D)), delta=rng.standard_normal((b, L, D)) * 0.5 - 1.0,
+                A=-rng.uniform(0.3, 2.0, (D, N)), B=rng.standard_normal((b, L, N)), C=rng.standard_normal((b, L, N)),
+                D=rng.standard_normal(D), z=rng.standard_normal((b, L, D)), delta_bias=rng.uniform(-0.5, 0.5, D),
+                h0=rng.standard_normal((b, D, N)))
+    dy = rng.standard_normal((b, L, D))
+    dlast = rng.standard_normal((b, D, N))
+    for softplus, keys in ((True, list(base)), (False, ["u", "delta", "A", "B", "C"])):
+        inp = {k: base[k] for k in keys}
+        if not softplus:
+            inp["delta"] = np.abs(base["delta"]) + 0.05  # a positive step size
+
+        def loss(x):
+            y, last = o.selective_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x.get("D"), z=x.get("z"),
+                                           delta_bias=x.get("delta_bias"), delta_softplus=softplus, h0=x.get("h0"))
+            return float(np.sum(dy * y) + np.sum(dlast * last))
+
+        gr = o.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, D=inp.get("D"),
+                                  z=inp.get("z"), delta_bias=inp.get("delta_bias"), delta_softplus=softplus,
+                                  h0=inp.get("h0"), dlast=dlast)
+        names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+                 "delta_bias": "dbias", "h0": "dh0"}
+        eps = 1e-6
+        for k in keys:
+            g = gr[names[k]]
+            for idx in np.ndindex(inp[k].shape):
+                xp = {kk: v.copy() for kk, v in inp.items()}
+                xm = {kk: v.copy() for kk, v in inp.items()}
+                xp[k][idx] += eps
+                xm[k][idx] -= eps
+                fd = (loss(xp) - loss(xm)) / (2 * eps)
+                assert abs(fd - g[idx]) <= 1e-6 * (1 + abs(fd)), (k, idx, fd, g[idx])
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_delta_zero_holds_state, pin_scalar_closed_form,
             pin_bruteforce_unrolling, pin_large_delta_reset, pin_stability_bound, pin_decode_matches_forward,
             pin_softplus_silu, pin_scan_operator, pin_decode_step_map, pin_zoh_solves_the_ode, pin_zoh_limits,
-            pin_conv_prologue]
+            pin_conv_prologue, pin_backward_finite_differences]
