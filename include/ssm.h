@@ -13,6 +13,7 @@
  *   ssm_conv_selective_scan_fwd, ssm_conv_state_update
  *                            the same two with the block's causal width-4 depthwise
  *                            conv + SiLU (the step before the SSM) fused in front
+ *   ssm_selective_scan_bwd   the backward pass of the forward pass (all gradients)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -309,6 +310,52 @@ SSM_API ssm_status_t ssm_conv_state_update(ssm_tensor_t* conv_state, ssm_tensor_
                                            const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
                                            int delta_softplus, uint32_t flags, ssm_tensor_t* y,
                                            void* stream);
+
+/*
+ * ssm_selective_scan_bwd -- backward pass of the forward pass (Delta * B discretisation,
+ * with or without a start state; not the conv prologue or the ZOH option): the
+ * gradients of the loss sum(dy * y) + sum(dlast * last_state) with respect to every
+ * input. Per channel, in reverse time with g = dL/dh_t (from dlast at t = L-1):
+ *   dv = dy silu(z)      dz = dy v silu'(z)     dD += dv u      g += dv C_t     dC_t += dv h_t
+ *   dB_t += g dt u       du = dv D + sum_n g dt B_t             dA += g a h_{t-1} dt
+ *   ddelta = sum_n g (B_t u + A a h_{t-1}) * (softplus ? sigmoid(delta + bias) : 1)
+ *   dbias += ddelta      g *= a                 (after t = 0: dh0 = g)
+ * Sources: the recurrence of "Mamba and State Space Models", "Selective scan
+ * pseudo-code", differentiated; the states are recomputed from checkpoints rather than
+ * stored ("Mamba and State Space Models", "Hardware-Aware Parallel Scan": kernel fusion
+ * with recomputation in the backward pass).
+ *
+ *   u ... delta_softplus, h0    the forward pass's inputs (as ssm_selective_scan_fwd_ex)
+ *   dy      (batch, L, D)  gradient type G     dL/dy
+ *   dlast   (batch, D, N)  f32, nullable       dL/dlast_state (NULL = 0)
+ *   du, ddelta (batch, L, D), dB, dC (batch, L, N): type G, written
+ *   dA      (D, N) f32, written                dD, dbias (D) f32: required exactly when
+ *   dz      (batch, L, D) type G: required exactly when z is given     D / delta_bias are
+ *   dh0     (batch, D, N) f32, nullable: dL/dh0 (also without h0)      given
+ *   workspace: at least ssm_selective_scan_bwd_workspace_size bytes, 256-byte aligned,
+ *              overlapping no tensor; scratch
+ * G is the I/O type or SSM_F32, the same for dy and every gradient of an I/O tensor.
+ * Gradients are accumulated in fp32 and summed in a fixed order: the result is
+ * deterministic. Outputs may overlap no input and no other output. A missing gradient
+ * output for a given optional input (or one for an absent input) is SSM_ERR_NULL; a
+ * short workspace is SSM_ERR_SHAPE. L == 0 or batch == 0 writes zeros (dh0 = dlast).
+ */
+SSM_API ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                            const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                            const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                            const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                            int delta_softplus, const ssm_tensor_t* h0,
+                                            const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
+                                            ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA,
+                                            ssm_tensor_t* dB, ssm_tensor_t* dC, ssm_tensor_t* dD,
+                                            ssm_tensor_t* dz, ssm_tensor_t* dbias, ssm_tensor_t* dh0,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ssm_selective_scan_bwd needs for this shape (0 for an empty problem):
+ * the state before every 16-step chunk, per-warp partial sums of dB and dC, and per-row
+ * partials of dA, dD, dbias. SSM_ERR_NULL (bytes == NULL) or SSM_ERR_SHAPE (negative). */
+SSM_API ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N,
+                                                          size_t* bytes);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

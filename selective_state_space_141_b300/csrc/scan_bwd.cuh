@@ -1,0 +1,435 @@
+// scan_bwd.cuh -- backward pass of the selective scan (Delta * B discretisation), sm_103a.
+//
+// For the loss sum(dy * y) + sum(dlast * last_state), per channel, in reverse time with
+// g = dL/dh_t (starting from dlast):
+//   dv = dy silu(z)          dz = dy v silu'(z)          dD += dv u
+//   g += dv C_t              dC_t += dv h_t
+//   dB_t += g dt u           du = dv D + sum_n g dt B_t
+//   d(dt) = sum_n g (B_t u + A a h_{t-1})                 dA += g a h_{t-1} dt
+//   ddelta = d(dt) sigmoid(r) with softplus (else d(dt))   dbias += ddelta
+//   g *= a                   (after t = 0: dh0 = g)
+// The chain rule through the recurrence of "Mamba and State Space Models", "Selective
+// scan pseudo-code"; the reverse sweep is the backward of the scan with recomputation
+// of the states that "Hardware-Aware Parallel Scan" describes ("8.7 State Space Models
+// (Mamba)", section 4.1: the same (a, b) recurrence run backwards).
+//
+// Layout: one lane = one channel with all N states in registers (as the forward's
+// channel kernel), one warp per CTA. A forward sweep stores the state before every
+// chunk of kBwdK steps (checkpoints); the reverse sweep recomputes a chunk's states into
+// shared memory, then walks it backwards. Each chunk's inputs are staged into shared
+// memory with asynchronous copies (cp.async), double-buffered: the next chunk streams
+// in while the current one is computed, and B, C are read as shared-memory broadcasts.
+// dB and dC are sums over channels: each warp
+// reduces its 32 lanes with a transpose-reduce butterfly (shuffles) and writes one
+// partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over warps, and
+// dA, dD, dbias over batch rows, in a fixed order (deterministic, no atomics).
+#pragma once
+
+#include "common.cuh"
+
+namespace ssm {
+
+struct BwdParams {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* Dskip;       // nullable
+  const void* z;            // nullable
+  const float* delta_bias;  // nullable
+  int delta_softplus;
+  const float* h0;          // nullable
+  const void* dy;           // gradient type TG
+  const float* dlast;       // nullable
+  void* du;                 // TG
+  void* ddelta;             // TG
+  void* dz;                 // TG, nullable (iff z)
+  float* dh0;               // nullable
+  // workspace
+  float* ck;          // [b][nc][D][N]: state before each chunk
+  float* part;        // [b][L][W][2][N]: per-warp partials of dB (0) and dC (1)
+  float* dA_part;     // [b][D][N]
+  float* dD_part;     // [b][D]
+  float* dbias_part;  // [b][D]
+  int64_t batch, L, D;
+  int nc, W;          // chunks of kBwdK steps; warps along D
+  bool async_ok;      // every staged row starts 16-byte aligned: stage with cp.async
+};
+
+constexpr int kBwdK = 16;
+
+// Sum over the 32 lanes of a warp of each of v[0..N-1]; lane l ends with the sum of
+// v[(l >> (5 - log2 N)) & (N - 1)] (two or more lanes hold each n). Each round halves
+// the values a lane holds: the lanes with the round's bit set keep the upper half and
+// send the lower, the others the reverse.
+template <int N>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+  constexpr int kLogN = N == 16 ? 4 : N == 8 ? 3 : 2;
+  int m = N;
+#pragma unroll
+  for (int r = 0; r < kLogN; ++r) {
+    const int o = 16 >> r;
+    const bool upper = (lane & o) != 0;
+    const int half = m / 2;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      if (i < half) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    m = half;
+  }
+  float s = v[0];
+#pragma unroll
+  for (int o = 16 >> kLogN; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+// ---- chunk staging: global -> shared memory, asynchronous (cp.async) ----
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Raw inputs of one chunk of kBwdK steps for the 32 channels of this warp.
+template <typename T, typename TG, int N>
+struct BwdStage {
+  T u[kBwdK][32];
+  T dl[kBwdK][32];
+  T z[kBwdK][32];
+  TG dy[kBwdK][32];
+  T B[kBwdK * N];
+  T C[kBwdK * N];
+};
+
+// One (kBwdK x 32) tile of a (batch, L, D) tensor into smem. Asynchronous 16-byte copies
+// when every row start is 16-byte aligned (zero-filled past L and D), else plain loads.
+template <typename E>
+__device__ __forceinline__ void stage_rows(E (*dst)[32], const E* src, int64_t b, int64_t t0, int64_t L, int64_t D,
+                                           int64_t d0, bool async_ok, int lane) {
+  if (async_ok) {
+    constexpr int kPieces = 32 * (int)sizeof(E) / 16;  // 16-byte pieces per row
+    const int64_t valid_row = (D - d0) * (int64_t)sizeof(E);
+    for (int q = lane; q < kBwdK * kPieces; q += 32) {
+      const int k = q / kPieces, j = q % kPieces;
+      const int64_t t = t0 + k;
+      int64_t nb = t < L ? valid_row - j * 16 : 0;
+      nb = nb < 0 ? 0 : (nb > 16 ? 16 : nb);
+      const E* g = nb > 0 ? src + ((b * L + t) * D + d0) + j * (16 / (int)sizeof(E)) : src;
+      cp_async16(reinterpret_cast<unsigned char*>(&dst[k][0]) + j * 16, g, (int)nb);
+    }
+  } else {
+    for (int k = 0; k < kBwdK; ++k) {
+      const int64_t t = t0 + k, d = d0 + lane;
+      dst[k][lane] = (t < L && d < D) ? src[(b * L + t) * D + d] : E(0.f);
+    }
+  }
+}
+
+// The chunk's (kBwdK x N) block of a (batch, L, N) tensor.
+template <typename E, int N>
+__device__ __forceinline__ void stage_bc(E* dst, const E* src, int64_t b, int64_t t0, int64_t L, bool async_ok,
+                                         int lane) {
+  constexpr int kBytes = kBwdK * N * (int)sizeof(E);
+  if (async_ok) {
+    const int64_t valid = (L - t0) * N * (int64_t)sizeof(E);
+    for (int j = lane; j < kBytes / 16; j += 32) {
+      int64_t nb = valid - j * 16;
+      nb = nb < 0 ? 0 : (nb > 16 ? 16 : nb);
+      const E* g = nb > 0 ? src + (b * L + t0) * N + j * (16 / (int)sizeof(E)) : src;
+      cp_async16(reinterpret_cast<unsigned char*>(dst) + j * 16, g, (int)nb);
+    }
+  } else {
+    for (int i = lane; i < kBwdK * N; i += 32) {
+      const int64_t t = t0 + i / N;
+      dst[i] = t < L ? src[(b * L + t0) * N + i] : E(0.f);
+    }
+  }
+}
+
+template <typename T, typename TG, int N>
+__device__ __forceinline__ void stage_chunk(BwdStage<T, TG, N>& sg, const BwdParams& p, int64_t b, int c, int64_t d0,
+                                            bool reverse, int lane) {
+  const int64_t t0 = (int64_t)c * kBwdK;
+  stage_rows<T>(sg.u, static_cast<const T*>(p.u), b, t0, p.L, p.D, d0, p.async_ok, lane);
+  stage_rows<T>(sg.dl, static_cast<const T*>(p.delta), b, t0, p.L, p.D, d0, p.async_ok, lane);
+  stage_bc<T, N>(sg.B, static_cast<const T*>(p.B), b, t0, p.L, p.async_ok, lane);
+  if (reverse) {
+    stage_rows<TG>(sg.dy, static_cast<const TG*>(p.dy), b, t0, p.L, p.D, d0, p.async_ok, lane);
+    if (p.z) stage_rows<T>(sg.z, static_cast<const T*>(p.z), b, t0, p.L, p.D, d0, p.async_ok, lane);
+    stage_bc<T, N>(sg.C, static_cast<const T*>(p.C), b, t0, p.L, p.async_ok, lane);
+  }
+  cp_async_commit();
+}
+
+// Decay factors of two states: 2^(dt A log2 e) on the SFU, or exp in double on the
+// fp32 I/O path (as the forward kernels).
+template <bool kAccurate>
+__device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
+  if (kAccurate) return make_float2(decay<true>(dt2.x, A.x, A2.x), decay<true>(dt2.y, A.y, A2.y));
+  const float2 x = __fmul2_rn(dt2, A2);
+  return make_float2(ex2(x.x), ex2(x.y));
+}
+
+// grid (W = ceil(D / 32), batch), block 32 (one warp); dynamic shared memory:
+//   hs  [kBwdK + 1][N][32] f32   states h_{t0-1} .. h_{t0+K-1} of the chunk being walked
+//   bc  [kBwdK][2N]        f32   the chunk's B | C rows
+//   dts [kBwdK][32]        f32   its step sizes
+//   vs  [kBwdK][32]        f32   its read-outs C.h + D u (before the gate)
+//   stage[2]                     raw inputs of the current and the next chunk
+template <typename T, typename TG, int N>
+constexpr int bwd_smem_bytes() {
+  return ((kBwdK + 1) * N * 32 + kBwdK * 2 * N + 2 * kBwdK * 32) * 4 + 2 * (int)sizeof(BwdStage<T, TG, N>);
+}
+
+template <typename T, typename TG, int N>
+__global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
+  constexpr int P = N / 2;  // state pairs (packed f32x2 arithmetic)
+  extern __shared__ __align__(16) float sm[];
+  float* hs = sm;
+  float* bc = hs + (kBwdK + 1) * N * 32;
+  float* dts = bc + kBwdK * 2 * N;
+  float* vs = dts + kBwdK * 32;
+  BwdStage<T, TG, N>* stg = reinterpret_cast<BwdStage<T, TG, N>*>(vs + kBwdK * 32);
+  const int lane = threadIdx.x;
+  const int w = blockIdx.x;
+  const int64_t b = blockIdx.y;
+  const int64_t L = p.L, D = p.D;
+  const int64_t d0 = (int64_t)w * 32, d = d0 + lane;
+  const bool vd = d < D;
+  constexpr bool kAccurate = sizeof(T) == 4;
+  const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
+
+  float2 Av[P], A2[P], h[P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    Av[q] = vd ? make_float2(p.A[d * N + 2 * q], p.A[d * N + 2 * q + 1]) : make_float2(0.f, 0.f);
+    A2[q] = __fmul2_rn(Av[q], make_float2(kLog2e, kLog2e));
+    h[q] = (vd && p.h0) ? make_float2(p.h0[(b * D + d) * N + 2 * q], p.h0[(b * D + d) * N + 2 * q + 1])
+                        : make_float2(0.f, 0.f);
+  }
+  // Converts the staged B (and C) of a chunk to fp32 for broadcast reads.
+  auto convert_bc = [&](const BwdStage<T, TG, N>& sg, bool with_c) {
+    for (int i = lane; i < kBwdK * N; i += 32) {
+      const int k = i / N, n = i % N;
+      bc[k * 2 * N + n] = to_f32(sg.B[i]);
+      if (with_c) bc[k * 2 * N + N + n] = to_f32(sg.C[i]);
+    }
+    __syncwarp();
+  };
+  auto step_dt = [&](const BwdStage<T, TG, N>& sg, int k, float* r_out) {
+    const float r = to_f32(sg.dl[k][lane]) + bias;
+    if (r_out) *r_out = r;
+    if (!p.delta_softplus) return r;
+    if (kAccurate) return softplus_precise(r);
+    return fmaxf(r, 0.f) + kLn2 * lg2(1.f + ex2(fabsf(r) * -kLog2e));  // SFU form, as the forward
+  };
+  auto sigmoid = [&](float x) { return __frcp_rn(1.f + __expf(-x)); };
+
+  // ---- forward sweep: the state before every chunk ----
+  if (p.nc > 1) stage_chunk<T, TG, N>(stg[0], p, b, 0, d0, false, lane);
+  for (int c = 0; c < p.nc; ++c) {
+    if (vd) {
+      float4* ckp = reinterpret_cast<float4*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N);
+#pragma unroll
+      for (int q = 0; q < P; q += 2) ckp[q / 2] = make_float4(h[q].x, h[q].y, h[q + 1].x, h[q + 1].y);
+    }
+    if (c == p.nc - 1) break;  // the state after the last chunk is not needed
+    cp_async_wait_all();
+    __syncwarp();
+    const BwdStage<T, TG, N>& sg = stg[c & 1];
+    convert_bc(sg, false);
+    if (c + 1 < p.nc - 1) stage_chunk<T, TG, N>(stg[(c + 1) & 1], p, b, c + 1, d0, false, lane);
+    for (int k = 0; k < kBwdK; ++k) {  // chunks before the last are full
+      const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
+      const float dx = dt * to_f32(sg.u[k][lane]);
+      const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
+      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
+#pragma unroll
+      for (int q = 0; q < P; ++q)
+        h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
+    }
+    __syncwarp();
+  }
+
+  // ---- reverse sweep ----
+  float2 g[P], dA_acc[P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    g[q] = (vd && p.dlast) ? make_float2(p.dlast[(b * D + d) * N + 2 * q], p.dlast[(b * D + d) * N + 2 * q + 1])
+                           : make_float2(0.f, 0.f);
+    dA_acc[q] = make_float2(0.f, 0.f);
+  }
+  float dD_acc = 0.f, dbias_acc = 0.f;
+  const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
+  constexpr int kLogN = N == 16 ? 4 : N == 8 ? 3 : 2;
+  const int n_red = (lane >> (5 - kLogN)) & (N - 1);
+  const bool writer = (lane & ((32 / N) - 1)) == 0;
+  TG* du = static_cast<TG*>(p.du) + b * L * D + d;
+  TG* ddl = static_cast<TG*>(p.ddelta) + b * L * D + d;
+  TG* dzp = p.dz ? static_cast<TG*>(p.dz) + b * L * D + d : nullptr;
+  float* part = p.part + ((b * L) * p.W + w) * 2 * N;  // + t * W * 2N
+
+  stage_chunk<T, TG, N>(stg[(p.nc - 1) & 1], p, b, p.nc - 1, d0, true, lane);
+  for (int c = p.nc - 1; c >= 0; --c) {
+    const int64_t t0 = (int64_t)c * kBwdK;
+    const int kc = (int)((L - t0) < kBwdK ? (L - t0) : kBwdK);
+    cp_async_wait_all();
+    __syncwarp();
+    const BwdStage<T, TG, N>& sg = stg[c & 1];
+    convert_bc(sg, true);
+    if (c > 0) stage_chunk<T, TG, N>(stg[(c - 1) & 1], p, b, c - 1, d0, true, lane);
+    // recompute the chunk's states and read-outs
+    {
+      const float4* ckp = reinterpret_cast<const float4*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N);
+#pragma unroll
+      for (int q = 0; q < P; q += 2) {
+        const float4 v4 = vd ? ckp[q / 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+        h[q] = make_float2(v4.x, v4.y);
+        h[q + 1] = make_float2(v4.z, v4.w);
+      }
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        hs[(2 * q) * 32 + lane] = h[q].x;
+        hs[(2 * q + 1) * 32 + lane] = h[q].y;
+      }
+      for (int k = 0; k < kc; ++k) {
+        const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
+        const float x = to_f32(sg.u[k][lane]);
+        const float dx = dt * x;
+        dts[k * 32 + lane] = dt;
+        const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
+        const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
+        const float2* c2 = b2 + P;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
+          acc = __ffma2_rn(c2[q], h[q], acc);
+          hs[((k + 1) * N + 2 * q) * 32 + lane] = h[q].x;
+          hs[((k + 1) * N + 2 * q + 1) * 32 + lane] = h[q].y;
+        }
+        vs[k * 32 + lane] = fmaf(Dk, x, acc.x + acc.y);
+      }
+    }
+    // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
+    for (int k = kc - 1; k >= 0; --k) {
+      const int64_t t = t0 + k;
+      const float dt = dts[k * 32 + lane];
+      float r = 0.f;
+      if (vd) step_dt(sg, k, &r);
+      const float x = to_f32(sg.u[k][lane]), dyv = to_f32(sg.dy[k][lane]);
+      const float v = vs[k * 32 + lane];
+      float dv = dyv;
+      if (dzp) {
+        const float zz = to_f32(sg.z[k][lane]);
+        const float sgm = sigmoid(zz);
+        if (vd) dzp[t * D] = from_f32<TG>(dyv * v * (sgm * (1.f + zz * (1.f - sgm))));
+        dv = dyv * zz * sgm;
+      }
+      dD_acc = fmaf(dv, x, dD_acc);
+      const float2 dv2 = make_float2(dv, dv), dt2 = make_float2(dt, dt), x2 = make_float2(x, x);
+      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
+      const float2* c2 = b2 + P;
+      float2 dux2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
+      float vb[N], vc[N];
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        const float2 hp = make_float2(hs[(k * N + 2 * q) * 32 + lane], hs[(k * N + 2 * q + 1) * 32 + lane]);
+        const float2 a = decay2<kAccurate>(dt2, Av[q], A2[q]);
+        const float2 B2 = b2[q];
+        g[q] = __ffma2_rn(dv2, c2[q], g[q]);                 // g = dL/dh_t
+        const float2 cv = __fmul2_rn(dv2, h[q]);             // dC_t contribution: dv h_t
+        const float2 gdt = __fmul2_rn(g[q], dt2);
+        const float2 bv = __fmul2_rn(gdt, x2);               // dB_t contribution: g dt u
+        dux2 = __ffma2_rn(gdt, B2, dux2);
+        const float2 ah = __fmul2_rn(a, hp);
+        ddt2 = __ffma2_rn(g[q], __ffma2_rn(B2, x2, __fmul2_rn(Av[q], ah)), ddt2);
+        dA_acc[q] = __ffma2_rn(__fmul2_rn(g[q], ah), dt2, dA_acc[q]);
+        g[q] = __fmul2_rn(g[q], a);                          // dL/dh_{t-1} (through the recurrence)
+        h[q] = hp;                                           // h_t of step t-1
+        vb[2 * q] = bv.x;
+        vb[2 * q + 1] = bv.y;
+        vc[2 * q] = cv.x;
+        vc[2 * q + 1] = cv.y;
+      }
+      const float dux = fmaf(dv, Dk, dux2.x + dux2.y), ddt = ddt2.x + ddt2.y;
+      const float dr = p.delta_softplus ? ddt * sigmoid(r) : ddt;
+      dbias_acc += dr;
+      if (vd) {
+        du[t * D] = from_f32<TG>(dux);
+        ddl[t * D] = from_f32<TG>(dr);
+      }
+      const float sb = warp_transpose_reduce<N>(vb, lane);
+      const float sc = warp_transpose_reduce<N>(vc, lane);
+      if (writer) {
+        float* pp = part + t * p.W * 2 * N;
+        pp[n_red] = sb;
+        pp[N + n_red] = sc;
+      }
+    }
+    __syncwarp();
+  }
+
+  if (vd) {
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      p.dA_part[(b * D + d) * N + 2 * q] = dA_acc[q].x;
+      p.dA_part[(b * D + d) * N + 2 * q + 1] = dA_acc[q].y;
+    }
+    p.dD_part[b * D + d] = dD_acc;
+    p.dbias_part[b * D + d] = dbias_acc;
+    if (p.dh0) {
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        p.dh0[(b * D + d) * N + 2 * q] = g[q].x;
+        p.dh0[(b * D + d) * N + 2 * q + 1] = g[q].y;
+      }
+    }
+  }
+}
+
+// Fixed-order sums of the partials: dB, dC (batch, L, N) over the W warps along D;
+// dA (D, N), dD (D), dbias (D) over the batch rows. One thread per output element.
+template <typename TG>
+__global__ void __launch_bounds__(256) scan_bwd_reduce(const float* __restrict__ part, const float* __restrict__ dA_part,
+                                                       const float* __restrict__ dD_part,
+                                                       const float* __restrict__ dbias_part, TG* dB, TG* dC, float* dA,
+                                                       float* dD, float* dbias, int64_t batch, int64_t L, int64_t D,
+                                                       int N, int W) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nbc = batch * L * N, na = D * N;
+  if (i < nbc) {
+    const int64_t n = i % N, bt = i / N;
+    float sb = 0.f, sc = 0.f;
+    for (int w = 0; w < W; ++w) {
+      const float* pp = part + ((bt * W + w) * 2) * N;
+      sb += pp[n];
+      sc += pp[N + n];
+    }
+    dB[i] = from_f32<TG>(sb);
+    dC[i] = from_f32<TG>(sc);
+  } else if (i < nbc + na) {
+    const int64_t j = i - nbc;
+    float s = 0.f;
+    for (int64_t b = 0; b < batch; ++b) s += dA_part[b * na + j];
+    dA[j] = s;
+  } else if (i < nbc + na + D) {
+    const int64_t j = i - nbc - na;
+    float s = 0.f, sb = 0.f;
+    for (int64_t b = 0; b < batch; ++b) {
+      s += dD_part[b * D + j];
+      sb += dbias_part[b * D + j];
+    }
+    if (dD) dD[j] = s;
+    if (dbias) dbias[j] = sb;
+  }
+}
+
+}  // namespace ssm

@@ -16,6 +16,7 @@
 #include "../../include/ssm.h"
 #include "common.cuh"
 #include "scan_fwd.cuh"
+#include "scan_bwd.cuh"
 #include "scan_fwd_chan.cuh"
 #include "state_update.cuh"
 
@@ -628,6 +629,217 @@ ssm_status_t ssm_conv_state_update(ssm_tensor_t* conv_state, ssm_tensor_t* state
   c.b = conv_bias;
   c.state = conv_state;
   return dec_impl(state, x, delta, A, B, C, D, z, delta_bias, delta_softplus, flags, y, stream, &c);
+}
+
+}  // extern "C"
+
+namespace {
+// ---- backward pass -------------------------------------------------------------------
+struct BwdPlan {
+  int nc = 0, W = 0;
+  size_t off_ck = 0, off_part = 0, off_dA = 0, off_dD = 0, off_db = 0, bytes = 0;
+};
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+BwdPlan plan_bwd(int64_t batch, int64_t L, int64_t D, int64_t N) {
+  BwdPlan pl;
+  pl.nc = (int)((L + ssm::kBwdK - 1) / ssm::kBwdK);
+  pl.W = (int)((D + 31) / 32);
+  size_t o = 0;
+  pl.off_ck = o;
+  o += round256((size_t)batch * pl.nc * D * N * 4);
+  pl.off_part = o;
+  o += round256((size_t)batch * L * pl.W * 2 * N * 4);
+  pl.off_dA = o;
+  o += round256((size_t)batch * D * N * 4);
+  pl.off_dD = o;
+  o += round256((size_t)batch * D * 4);
+  pl.off_db = o;
+  o += round256((size_t)batch * D * 4);
+  pl.bytes = o;
+  return pl;
+}
+
+template <typename T, typename TG, int N>
+cudaError_t launch_bwd(const ssm::BwdParams& p, cudaStream_t st) {
+  auto kern = &ssm::scan_bwd_kernel<T, TG, N>;
+  constexpr int smem = ssm::bwd_smem_bytes<T, TG, N>();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  void* args[] = {const_cast<ssm::BwdParams*>(&p)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)p.W, (unsigned)p.batch), dim3(32), args,
+                          smem, st);
+}
+
+template <typename T, typename TG>
+cudaError_t launch_bwd_n(int64_t N, const ssm::BwdParams& p, cudaStream_t st) {
+  switch (N) {
+    case 4: return launch_bwd<T, TG, 4>(p, st);
+    case 8: return launch_bwd<T, TG, 8>(p, st);
+    default: return launch_bwd<T, TG, 16>(p, st);
+  }
+}
+
+template <typename TG>
+cudaError_t launch_bwd_reduce(const ssm::BwdParams& p, int64_t N, void* dB, void* dC, float* dA, float* dD,
+                              float* dbias, cudaStream_t st) {
+  const int64_t n = p.batch * p.L * N + p.D * N + p.D;
+  const float* part = p.part;
+  const float* dAp = p.dA_part;
+  const float* dDp = p.dD_part;
+  const float* dbp = p.dbias_part;
+  TG* b = static_cast<TG*>(dB);
+  TG* c = static_cast<TG*>(dC);
+  int64_t batch = p.batch, L = p.L, D = p.D;
+  int Ni = (int)N, W = p.W;
+  void* args[] = {&part, &dAp, &dDp, &dbp, &b, &c, &dA, &dD, &dbias, &batch, &L, &D, &Ni, &W};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::scan_bwd_reduce<TG>), dim3((unsigned)((n + 255) / 256)),
+                          dim3(256), args, 0, st);
+}
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N, size_t* bytes) {
+  if (!bytes) return SSM_ERR_NULL;
+  if (batch < 0 || L < 0 || D < 0 || N < 0) return SSM_ERR_SHAPE;
+  *bytes = 0;
+  if (batch == 0 || L == 0 || D == 0 || !n_supported(N)) return SSM_OK;
+  *bytes = plan_bwd(batch, L, D, N).bytes;
+  return SSM_OK;
+}
+
+ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                    const ssm_tensor_t* h0, const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
+                                    ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA, ssm_tensor_t* dB,
+                                    ssm_tensor_t* dC, ssm_tensor_t* dD, ssm_tensor_t* dz, ssm_tensor_t* dbias,
+                                    ssm_tensor_t* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return SSM_ERR_NULL;
+  if ((D != nullptr) != (dD != nullptr) || (z != nullptr) != (dz != nullptr) ||
+      (delta_bias != nullptr) != (dbias != nullptr))
+    return SSM_ERR_NULL;  // a gradient output exactly for each optional input
+  if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
+  const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
+  if (batch < 0 || L < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
+  ssm_status_t s;
+  const std::initializer_list<int64_t> sLD = {batch, L, Dm}, sLN = {batch, L, N}, sDN3 = {batch, Dm, N};
+  for (const ssm_tensor_t* t : {u, delta, dy, static_cast<const ssm_tensor_t*>(du),
+                                static_cast<const ssm_tensor_t*>(ddelta)})
+    if ((s = check_tensor(t, sLD)) != SSM_OK) return s;
+  if (z && ((s = check_tensor(z, sLD)) != SSM_OK || (s = check_tensor(dz, sLD)) != SSM_OK)) return s;
+  if ((s = check_tensor(A, {Dm, N})) != SSM_OK || (s = check_tensor(dA, {Dm, N})) != SSM_OK) return s;
+  for (const ssm_tensor_t* t : {B, C, static_cast<const ssm_tensor_t*>(dB), static_cast<const ssm_tensor_t*>(dC)})
+    if ((s = check_tensor(t, sLN)) != SSM_OK) return s;
+  if (D && ((s = check_tensor(D, {Dm})) != SSM_OK || (s = check_tensor(dD, {Dm})) != SSM_OK)) return s;
+  if (delta_bias && ((s = check_tensor(delta_bias, {Dm})) != SSM_OK || (s = check_tensor(dbias, {Dm})) != SSM_OK))
+    return s;
+  if (h0 && (s = check_tensor(h0, sDN3)) != SSM_OK) return s;
+  if (dlast && (s = check_tensor(dlast, sDN3)) != SSM_OK) return s;
+  if (dh0 && (s = check_tensor(dh0, sDN3)) != SSM_OK) return s;
+
+  const ssm_dtype_t io = u->dtype, gt = du->dtype;
+  if (delta->dtype != io || B->dtype != io || C->dtype != io || (z && z->dtype != io)) return SSM_ERR_DTYPE;
+  if (gt != io && gt != SSM_F32) return SSM_ERR_DTYPE;
+  if (dy->dtype != gt || ddelta->dtype != gt || dB->dtype != gt || dC->dtype != gt || (dz && dz->dtype != gt))
+    return SSM_ERR_DTYPE;
+  for (const ssm_tensor_t* t : {A, D, delta_bias, h0, dlast, static_cast<const ssm_tensor_t*>(dA),
+                                static_cast<const ssm_tensor_t*>(dD), static_cast<const ssm_tensor_t*>(dbias),
+                                static_cast<const ssm_tensor_t*>(dh0)})
+    if (t && t->dtype != SSM_F32) return SSM_ERR_DTYPE;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_UNSUPPORTED;
+  if (!n_supported(N)) return SSM_ERR_UNSUPPORTED;
+  if (batch > 65535) return SSM_ERR_UNSUPPORTED;
+
+  const ssm_tensor_t* ins[] = {u, delta, A, B, C, D, z, delta_bias, h0, dy, dlast};
+  const ssm_tensor_t* outs[] = {du, ddelta, dA, dB, dC, dD, dz, dbias, dh0};
+  for (const ssm_tensor_t* o : outs) {
+    for (const ssm_tensor_t* in : ins)
+      if (overlaps(o, in)) return SSM_ERR_LAYOUT;
+    for (const ssm_tensor_t* o2 : outs)
+      if (o != o2 && overlaps(o, o2)) return SSM_ERR_LAYOUT;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool empty = batch == 0 || L == 0 || Dm == 0;
+  const BwdPlan pl = empty ? BwdPlan{} : plan_bwd(batch, L, Dm, N);
+  if (!empty) {
+    if (!workspace) return SSM_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SSM_ERR_LAYOUT;
+    if (workspace_bytes < pl.bytes) return SSM_ERR_SHAPE;
+    ssm_tensor_t w{};
+    w.data = workspace;
+    w.dtype = SSM_F32;
+    w.ndim = 1;
+    w.shape[0] = (int64_t)(workspace_bytes / 4);
+    for (const ssm_tensor_t* t : ins)
+      if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
+    for (const ssm_tensor_t* t : outs)
+      if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
+  }
+
+  if (empty) {  // no steps: the sums are zero and dL/dh0 is dlast
+    auto zero = [&](ssm_tensor_t* t) {
+      return !t || numel(t) == 0 || cudaMemsetAsync(t->data, 0, (size_t)(numel(t) * elem_size(t->dtype)), st) == cudaSuccess;
+    };
+    bool ok = zero(dA) && zero(dD) && zero(dbias);
+    if (dh0 && numel(dh0) > 0)
+      ok = ok && (dlast ? cudaMemcpyAsync(dh0->data, dlast->data, (size_t)numel(dh0) * 4, cudaMemcpyDeviceToDevice, st) ==
+                              cudaSuccess
+                        : zero(dh0));
+    return ok ? SSM_OK : SSM_ERR_CUDA;
+  }
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  ssm::BwdParams p;
+  p.u = u->data;
+  p.delta = delta->data;
+  p.A = static_cast<const float*>(A->data);
+  p.B = B->data;
+  p.C = C->data;
+  p.Dskip = D ? static_cast<const float*>(D->data) : nullptr;
+  p.z = z ? z->data : nullptr;
+  p.delta_bias = delta_bias ? static_cast<const float*>(delta_bias->data) : nullptr;
+  p.delta_softplus = delta_softplus;
+  p.h0 = h0 ? static_cast<const float*>(h0->data) : nullptr;
+  p.dy = dy->data;
+  p.dlast = dlast ? static_cast<const float*>(dlast->data) : nullptr;
+  p.du = du->data;
+  p.ddelta = ddelta->data;
+  p.dz = dz ? dz->data : nullptr;
+  p.dh0 = dh0 ? static_cast<float*>(dh0->data) : nullptr;
+  p.ck = reinterpret_cast<float*>(ws + pl.off_ck);
+  p.part = reinterpret_cast<float*>(ws + pl.off_part);
+  p.dA_part = reinterpret_cast<float*>(ws + pl.off_dA);
+  p.dD_part = reinterpret_cast<float*>(ws + pl.off_dD);
+  p.dbias_part = reinterpret_cast<float*>(ws + pl.off_db);
+  p.batch = batch;
+  p.L = L;
+  p.D = Dm;
+  p.nc = pl.nc;
+  p.W = pl.W;
+  {  // cp.async staging needs every (batch, L, D) row and every chunk of B, C 16-byte aligned
+    const int64_t es = io == SSM_F32 ? 4 : 2, gs = gt == SSM_F32 ? 4 : 2;
+    bool ok = (Dm * es) % 16 == 0 && (Dm * gs) % 16 == 0 && (L * N * es) % 16 == 0;
+    for (const ssm_tensor_t* t : {u, delta, B, C, z, dy})
+      if (t && reinterpret_cast<uintptr_t>(t->data) % 16 != 0) ok = false;
+    p.async_ok = ok;
+  }
+
+  cudaError_t e;
+  if (io == SSM_F32)
+    e = launch_bwd_n<float, float>(N, p, st);
+  else if (gt == SSM_BF16)
+    e = launch_bwd_n<__nv_bfloat16, __nv_bfloat16>(N, p, st);
+  else
+    e = launch_bwd_n<__nv_bfloat16, float>(N, p, st);
+  if (e != cudaSuccess) return SSM_ERR_CUDA;
+  float* dAp = static_cast<float*>(dA->data);
+  float* dDp = dD ? static_cast<float*>(dD->data) : nullptr;
+  float* dbp = dbias ? static_cast<float*>(dbias->data) : nullptr;
+  e = gt == SSM_BF16 ? launch_bwd_reduce<__nv_bfloat16>(p, N, dB->data, dC->data, dAp, dDp, dbp, st)
+                     : launch_bwd_reduce<float>(p, N, dB->data, dC->data, dAp, dDp, dbp, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status_t ssm_device_error(void* stream, int32_t* code) {

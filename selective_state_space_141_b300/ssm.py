@@ -69,6 +69,11 @@ def load_library(path: str | None = None):
                                                             ctypes.c_size_t, ctypes.c_void_p]
     lib.ssm_conv_state_update.restype = ctypes.c_int
     lib.ssm_conv_state_update.argtypes = [_P] * 12 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
+    lib.ssm_selective_scan_bwd.restype = ctypes.c_int
+    lib.ssm_selective_scan_bwd.argtypes = [_P] * 8 + [ctypes.c_int] + [_P] * 12 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                                                ctypes.c_void_p]
+    lib.ssm_selective_scan_bwd_workspace_size.restype = ctypes.c_int
+    lib.ssm_selective_scan_bwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_state_update_ex.restype = ctypes.c_int
     lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -169,6 +174,50 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     if st != 0:
         raise SsmError(st, "ssm_selective_scan_fwd_ws")
     return y, last_state
+
+
+def bwd_workspace_size(batch, L, D, N) -> int:
+    """Bytes of workspace ``ssm_selective_scan_bwd`` needs for this shape."""
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.ssm_selective_scan_bwd_workspace_size(int(batch), int(L), int(D), int(N), ctypes.byref(n))
+    if st != 0:
+        raise SsmError(st, "ssm_selective_scan_bwd_workspace_size")
+    return int(n.value)
+
+
+def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True, h0=None,
+                       dlast=None, want_dh0=False, workspace=None, stream=None):
+    """Backward pass (``ssm_selective_scan_bwd``): gradients of sum(dy * y) +
+    sum(dlast * last_state). dy's dtype (the I/O dtype or fp32) is the dtype of du,
+    ddelta, dz, dB, dC; dA, dD, dbias, dh0 are fp32. Returns a dict with du, ddelta, dA,
+    dB, dC and, for the optional inputs given, dD, dz, dbias (dh0 when h0 is given or
+    ``want_dh0``)."""
+    lib = load_library()
+    batch, L, Dm = u.shape
+    N = A.shape[-1]
+    dev, gt = u.device, dy.dtype
+    f32 = torch.float32
+    g = dict(du=torch.empty(u.shape, dtype=gt, device=dev), ddelta=torch.empty(u.shape, dtype=gt, device=dev),
+             dA=torch.empty(A.shape, dtype=f32, device=dev), dB=torch.empty(B.shape, dtype=gt, device=dev),
+             dC=torch.empty(C.shape, dtype=gt, device=dev))
+    g["dD"] = torch.empty(D.shape, dtype=f32, device=dev) if D is not None else None
+    g["dz"] = torch.empty(z.shape, dtype=gt, device=dev) if z is not None else None
+    g["dbias"] = torch.empty(delta_bias.shape, dtype=f32, device=dev) if delta_bias is not None else None
+    g["dh0"] = torch.empty((batch, Dm, N), dtype=f32, device=dev) if (h0 is not None or want_dh0) else None
+    if workspace is None:
+        nbytes = bwd_workspace_size(batch, L, Dm, N)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+    ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
+    ins = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    rest = [describe(t) for t in (h0, dy, dlast, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"],
+                                  g["dbias"], g["dh0"])]
+    st = lib.ssm_selective_scan_bwd(*[_ref(d) for d in ins], int(bool(delta_softplus)), *[_ref(d) for d in rest],
+                                    ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes), _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_selective_scan_bwd")
+    return {k: v for k, v in g.items() if v is not None}
 
 
 def conv_selective_scan_fwd(x, conv_weight, delta, A, B, C, conv_bias=None, conv_state=None, D=None, z=None,

@@ -264,3 +264,53 @@ def test_conv_decode_validation(lib):
     assert call(T((3, 8, 2)), w) == 2
     assert call(cs, T((8, 5), ssm.SSM_F32)) == 2
     assert call(T((3, 8, 3), addr=a["state"].data), w) == 4
+
+
+def bwd_args(b=2, L=5, D=8, N=16, io=ssm.SSM_BF16, gt=None):
+    gt = io if gt is None else gt
+    a = fwd_args(b, L, D, N, io)
+    a.update(dy=T((b, L, D), gt), du=T((b, L, D), gt), ddelta=T((b, L, D), gt), dA=T((D, N), ssm.SSM_F32),
+             dB=T((b, L, N), gt), dC=T((b, L, N), gt), dD=T((D,), ssm.SSM_F32), dz=T((b, L, D), gt),
+             dbias=T((D,), ssm.SSM_F32), ws=T((1 << 16,), ssm.SSM_F32))
+    return a
+
+
+def call_bwd(lib, a, ws_bytes=None, ws_addr=None):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    n = ctypes.c_size_t(0)
+    assert lib.ssm_selective_scan_bwd_workspace_size(a["u"].shape[0], a["u"].shape[1], a["u"].shape[2],
+                                                      a["A"].shape[1], ctypes.byref(n)) == 0
+    wb = n.value if ws_bytes is None else ws_bytes
+    wa = ((a["ws"].data + 255) // 256 * 256) if ws_addr is None else ws_addr
+    return lib.ssm_selective_scan_bwd(r("u"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("bias"), 1, None,
+                                      r("dy"), None, r("du"), r("ddelta"), r("dA"), r("dB"), r("dC"), r("dD"), r("dz"),
+                                      r("dbias"), None, ctypes.c_void_p(wa), ctypes.c_size_t(wb), None)
+
+
+def test_bwd_validation(lib):
+    for k in ("dD", "dz", "dbias"):        # a gradient output for each optional input given
+        a = bwd_args()
+        a[k] = None
+        assert call_bwd(lib, a) == 1, k
+    a = bwd_args()
+    a["D"] = None                           # and none for an absent one
+    assert call_bwd(lib, a) == 1
+    a = bwd_args()
+    assert call_bwd(lib, a, ws_addr=0, ws_bytes=1024) == 1           # no workspace
+    assert call_bwd(lib, a, ws_bytes=16) == 2                         # too small
+    assert call_bwd(lib, a, ws_addr=a["ws"].data + 256 + 16) == 4     # not 256-byte aligned
+    a = bwd_args()
+    a["du"].dtype = ssm.SSM_F32                                       # gradient types must agree with dy
+    assert call_bwd(lib, a) == 3
+    a = bwd_args()
+    a["dA"].dtype = ssm.SSM_BF16
+    assert call_bwd(lib, a) == 3
+    a = bwd_args()
+    a["du"] = T((2, 5, 8), addr=a["u"].data)                          # an output over an input
+    assert call_bwd(lib, a) == 4
+    a = bwd_args()
+    a["dC"] = T((2, 5, 16), addr=a["dB"].data)                        # two outputs overlapping
+    assert call_bwd(lib, a) == 4
+    a = bwd_args()
+    a["dB"] = T((2, 5, 8))
+    assert call_bwd(lib, a) == 2

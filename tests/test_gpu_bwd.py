@@ -1,0 +1,82 @@
+"""GPU backward pass vs the fp64 oracle's backward (itself pinned to finite differences
+of the forward pass), called through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL_BF16, TOL_F32, check
+from selective_state_space_141_b300 import inputs, ssm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def case(b, L, D, N, dtype, seed, full=True, softplus=True):
+    d = inputs.random_fwd(b, L, D, N, dtype, DEV, seed=seed, has_bias=full, has_D=full, has_z=full,
+                          delta_softplus=softplus)
+    g = torch.Generator(device="cpu").manual_seed(seed + 500)
+    if not softplus:
+        d["delta"] = (torch.rand(b, L, D, generator=g) * 0.5 + 0.01).to(dtype).to(DEV)
+    d["h0"] = torch.randn(b, D, N, generator=g).to(DEV) if full else None
+    d["dlast"] = torch.randn(b, D, N, generator=g).to(DEV) if full else None
+    d["dy"] = torch.randn(b, L, D, generator=g).to(DEV)
+    return d
+
+
+def run(d, grad_dtype, want_dh0=True):
+    g = ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["dy"].to(grad_dtype), D=d["D"], z=d["z"],
+                               delta_bias=d["delta_bias"], delta_softplus=d["delta_softplus"], h0=d["h0"],
+                               dlast=d["dlast"], want_dh0=want_dh0)
+    torch.cuda.synchronize()
+    return g
+
+
+def ref(d, grad_dtype):
+    return oracle.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["dy"].to(grad_dtype), D=d["D"],
+                                     z=d["z"], delta_bias=d["delta_bias"], delta_softplus=d["delta_softplus"],
+                                     h0=d["h0"] if d["h0"] is not None else np.zeros((d["u"].shape[0],
+                                                                                      d["u"].shape[2],
+                                                                                      d["A"].shape[1])),
+                                     dlast=d["dlast"])
+
+
+@pytest.mark.parametrize("shape", [(2, 77, 100, 16), (3, 45, 64, 8), (1, 33, 40, 4), (2, 16, 32, 16)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("full", [True, False], ids=["all-inputs", "bare"])
+def test_bwd_vs_oracle(shape, dtype, full):
+    b, L, D, N = shape
+    d = case(b, L, D, N, dtype, seed=81 + L, full=full, softplus=full)
+    r = ref(d, torch.float32)
+    g = run(d, torch.float32)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    for k, v in r.items():
+        check(g[k], v, tol, False, k)
+    if dtype == torch.bfloat16:  # bf16 gradients: the same values rounded once
+        gb = run(d, torch.bfloat16)
+        rb = ref(d, torch.bfloat16)
+        for k in ("du", "ddelta", "dB", "dC") + (("dz",) if full else ()):
+            check(gb[k], rb[k], TOL_BF16, True, k + " (bf16)")
+
+
+def test_bwd_medium_shape():
+    """Several chunks, warps and a ragged tail, every gradient against the oracle."""
+    d = case(2, 333, 200, 16, torch.bfloat16, seed=91)
+    r = ref(d, torch.float32)
+    g = run(d, torch.float32)
+    for k, v in r.items():
+        check(g[k], v, TOL_BF16, False, k)
+
+
+def test_bwd_is_deterministic():
+    d = case(2, 100, 256, 16, torch.bfloat16, seed=92)
+    g1, g2 = run(d, torch.float32), run(d, torch.float32)
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+
+
+def test_bwd_empty_sequence():
+    d = case(2, 0, 64, 16, torch.bfloat16, seed=93)
+    g = run(d, torch.float32)
+    assert torch.count_nonzero(g["dA"]) == 0 and torch.count_nonzero(g["dD"]) == 0
+    assert torch.equal(g["dh0"], d["dlast"])
