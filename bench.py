@@ -329,6 +329,8 @@ def run_ours(args, w, ws, rank, local):
         result["e2e"] = e2e(w, d, args, ssm, torch, stream)
     if not args.no_decode:
         result["decode"] = decode_bench(args, ssm, torch, inputs, dev, hbm_peak)
+    if not args.no_bwd:
+        result["backward"] = backward_bench(args, ssm, torch, w, d, dev, launch_ms)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
     if rank == 0:
@@ -370,6 +372,37 @@ def e2e(w, d, args, ssm, torch, stream):
     sec = e0.elapsed_time(e1) / 1e3 / n
     return {"value": w.compulsory_bytes() / sec / 1e9, "unit": "GB/s", "ms_per_step": sec * 1e3,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def backward_bench(args, ssm, torch, w, d, dev, fwd_launch_ms):
+    """The backward pass (all gradients) on the same workload, bf16 dy, CUDA events around
+    each call (two launches: the sweep kernel and the fixed-order reduction)."""
+    g = torch.Generator(device=dev).manual_seed(5)
+    dy = torch.randn(d["u"].shape, generator=g, device=dev).to(d["u"].dtype)
+    nbytes = ssm.bwd_workspace_size(w.batch, w.L, w.D, w.N)
+    wsp = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def call():
+        return ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, D=d["D"], z=d["z"],
+                                      delta_bias=d["delta_bias"], delta_softplus=True, workspace=wsp)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.bwd_steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    if ssm.device_error() != 0:
+        raise RuntimeError("device error word set during the backward pass")
+    m = statistics.median(ms)
+    return {"workload": w.name, "ms": m, "ratio_to_forward": m / fwd_launch_ms, "elem_per_s": w.elems / (m / 1e3),
+            "calls": args.bwd_steps, "workspace_bytes": nbytes, "launches_per_call": 2,
+            "gradients": "du, ddelta, dA, dB, dC, dD, dz, dbias (bf16 dy; fp32 accumulation)"}
 
 
 def decode_bench(args, ssm, torch, inputs, dev, hbm_peak):
@@ -424,6 +457,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=5)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     args = ap.parse_args()

@@ -277,8 +277,10 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
   const int64_t threads = p.batch * p.D * (N / 4);
   dim3 grid((unsigned)((threads + 255) / 256)), block(256);
   void* args[] = {const_cast<DecodeParams*>(&p)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::state_update_kernel<T, TY, N>), grid, block, args,
-                          0, st);
+  const bool ext = p.delta_bias || p.delta_softplus || p.zoh || p.conv_w;
+  const void* kern = ext ? reinterpret_cast<const void*>(&ssm::state_update_kernel<T, TY, N, true>)
+                         : reinterpret_cast<const void*>(&ssm::state_update_kernel<T, TY, N, false>);
+  return cudaLaunchKernel(kern, grid, block, args, 0, st);
 }
 
 template <typename T, typename TY>

@@ -39,7 +39,10 @@ struct DecodeParams {
 
 // One thread per (b, d, group of 4 states); the N/4 lanes of a channel are adjacent
 // in the warp and combine their partial C.h with xor-shuffles.
-template <typename T, typename TY, int N>
+// kExt: the step-size map, the zero-order hold and the conv prologue are compiled in;
+// the plain step (all of them off) keeps the lean kernel (fewer registers, more resident
+// threads for this latency-bound update).
+template <typename T, typename TY, int N, bool kExt>
 __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p) {
   constexpr int LPC = N / 4;
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
     const T* Bp = static_cast<const T*>(p.B) + b * N + g * 4;
     const T* Cp = static_cast<const T*>(p.C) + b * N + g * 4;
     x = to_f32(xp[bd]);
-    if (p.conv_w) {  // the block's causal conv + SiLU over (cs0, cs1, cs2, x)
+    if (kExt && p.conv_w) {  // the block's causal conv + SiLU over (cs0, cs1, cs2, x)
       const T* cs = static_cast<const T*>(p.conv_state) + bd * 3;
       const float* w = p.conv_w + d * 4;
       float c = p.conv_b ? p.conv_b[d] : 0.f;
@@ -68,8 +71,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
       x = silu_precise(c);
     }
     float dt = to_f32(dp[bd]);
-    if (p.delta_bias) dt += p.delta_bias[d];
-    if (p.delta_softplus) dt = softplus_precise(dt);
+    if (kExt && p.delta_bias) dt += p.delta_bias[d];
+    if (kExt && p.delta_softplus) dt = softplus_precise(dt);
     const float dx = dt * x;
     float4* sp = reinterpret_cast<float4*>(p.state + bd * N + g * 4);
     s = *sp;
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float a = decay<sizeof(T) == 4>(dt, av[k], av[k] * kLog2e);
-      const float bx = p.zoh ? zoh_factor<sizeof(T) == 4>(dt, av[k]) * x : dx;  // B-bar u = bx B
+      const float bx = (kExt && p.zoh) ? zoh_factor<sizeof(T) == 4>(dt, av[k]) * x : dx;  // B-bar u = bx B
       sv[k] = fmaf(a, sv[k], bx * to_f32(Bp[k]));
       acc = fmaf(to_f32(Cp[k]), sv[k], acc);
     }
@@ -87,8 +90,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
   }
 #pragma unroll
   for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  __syncwarp();  // every lane of a channel has read the conv state before it is shifted
-  if (v && g == 0 && p.conv_w) {
+  if (kExt) __syncwarp();  // every lane of a channel has read the conv state before it is shifted
+  if (kExt && v && g == 0 && p.conv_w) {
     T* cs = static_cast<T*>(p.conv_state) + bd * 3;
     const T c1 = cs[1], c2 = cs[2];
     cs[0] = c1;
