@@ -78,6 +78,8 @@ class Oracle:
         lib.ssm_oracle_conv1d_silu.argtypes = [_i64, _i64, _i64] + [_dp] * 5
         lib.ssm_oracle_bwd.restype = ctypes.c_int
         lib.ssm_oracle_bwd.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12
+        lib.ssm_oracle_ssd_fwd.restype = ctypes.c_int
+        lib.ssm_oracle_ssd_fwd.argtypes = [_i64] * 6 + [_dp] * 7 + [ctypes.c_int, _dp, _dp, _dp]
         lib.ssm_oracle_fwd_ex.restype = ctypes.c_int
         lib.ssm_oracle_fwd_ex.argtypes = [_i64, _i64, _i64, _i64] + [_dp] * 8 + [ctypes.c_int, ctypes.c_int, _dp, _dp,
                                                                                  _dp, ctypes.c_int]
@@ -150,6 +152,29 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("ssm_oracle_bwd rejected its arguments")
         return {k: v for k, v in out.items() if v is not None}
+
+    def ssd_fwd(self, x, delta, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None):
+        """Mamba-2 SSD forward (sequential). x: (batch, L, H, P); delta: (batch, L, H);
+        A, D, dt_bias: (H); B, C: (batch, L, G, N); h0: (batch, H, P, N). Returns
+        (y (batch, L, H, P), last_state (batch, H, P, N)) as fp64 arrays."""
+        x = _f64(x)
+        batch, L, H, P = x.shape
+        B = _f64(B)
+        G, N = B.shape[2], B.shape[3]
+        delta = _f64(delta, (batch, L, H))
+        A = _f64(A, (H,))
+        C = _f64(C, (batch, L, G, N))
+        D = _f64(D, (H,))
+        dt_bias = _f64(dt_bias, (H,))
+        h0 = _f64(h0, (batch, H, P, N))
+        y = np.empty((batch, L, H, P))
+        last = np.empty((batch, H, P, N))
+        rc = self.lib.ssm_oracle_ssd_fwd(batch, L, H, P, N, G, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                         _ptr(D), _ptr(dt_bias), int(bool(dt_softplus)), _ptr(h0), _ptr(y),
+                                         _ptr(last))
+        if rc != 0:
+            raise RuntimeError("ssm_oracle_ssd_fwd rejected its arguments")
+        return y, last
 
     def conv1d_silu(self, x, w, bias=None, conv_state=None):
         """u = silu(causal depthwise conv of width 4 (+ bias)) as an fp64 array.
@@ -236,6 +261,10 @@ def conv1d_silu(*args, **kwargs):
 
 def selective_scan_bwd(*args, **kwargs):
     return default().selective_scan_bwd(*args, **kwargs)
+
+
+def ssd_fwd(*args, **kwargs):
+    return default().ssd_fwd(*args, **kwargs)
 
 
 def conv_selective_scan_fwd(*args, **kwargs):

@@ -346,3 +346,48 @@ int ssm_oracle_bwd(int64_t batch, int64_t L, int64_t D, int64_t N,
   free(hs); free(dts); free(rs); free(g);
   return 0;
 }
+
+/* Mamba-2 SSD recurrence (scalar decay per head): for every batch row b and head h, with
+ * the (P x N) state S starting at h0 (or 0) and g = h / (H / G) the B/C group:
+ *   dt  = delta[b,t,h] + dt_bias[h], then softplus when dt_softplus
+ *   S   = exp(dt A[h]) S + dt x[b,t,h,:] B[b,t,g,:]^T
+ *   y[b,t,h,:] = S C[b,t,g,:] + D[h] x[b,t,h,:]
+ * ("8.7 State Space Models (Mamba)" and "Mamba and State Space Models", "Mamba-2 and
+ * State Space Duality": A-bar_t = a_t I per head; B-bar = Delta B as in Mamba). */
+int ssm_oracle_ssd_fwd(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                       const double* x, const double* delta, const double* A, const double* B,
+                       const double* C, const double* Dskip, const double* dt_bias, int dt_softplus,
+                       const double* h0, double* y, double* last_state) {
+  if (batch < 0 || L < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return -1;
+  if (batch * H == 0) return 0;
+  if (!A || (L > 0 && (!x || !delta || !B || !C || !y))) return -1;
+  double* S = (double*)malloc(sizeof(double) * (size_t)(P * N));
+  if (!S) return -1;
+  for (int64_t b = 0; b < batch; ++b) {
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t g = h / (H / G);
+      for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[(b * H + h) * P * N + i] : 0.0;
+      for (int64_t t = 0; t < L; ++t) {
+        double r = delta[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+        const double dt = dt_softplus ? ssm_oracle_softplus(r) : r;
+        const double a = exp(dt * A[h]);
+        const double* xt = &x[((b * L + t) * H + h) * P];
+        const double* Bt = &B[((b * L + t) * G + g) * N];
+        const double* Ct = &C[((b * L + t) * G + g) * N];
+        double* yt = &y[((b * L + t) * H + h) * P];
+        for (int64_t p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (int64_t n = 0; n < N; ++n) {
+            S[p * N + n] = a * S[p * N + n] + dt * xt[p] * Bt[n];
+            acc += S[p * N + n] * Ct[n];
+          }
+          yt[p] = acc + (Dskip ? Dskip[h] * xt[p] : 0.0);
+        }
+      }
+      if (last_state)
+        for (int64_t i = 0; i < P * N; ++i) last_state[(b * H + h) * P * N + i] = S[i];
+    }
+  }
+  free(S);
+  return 0;
+}

@@ -116,6 +116,18 @@ int ssm_oracle_bwd(int64_t batch, int64_t L, int64_t D, int64_t N,
                    double* du, double* ddelta, double* dA, double* dB, double* dC,
                    double* dD, double* dz, double* dbias, double* dh0);
 
+/*
+ * Mamba-2 SSD (scalar decay per head, P x N state per head), sequential:
+ *   x, y : (batch, L, H, P)   delta : (batch, L, H)   A, Dskip, dt_bias : (H)
+ *   B, C : (batch, L, G, N), head h uses group h / (H / G)
+ *   h0, last_state : (batch, H, P, N), nullable
+ * Returns 0, or -1 on bad arguments.
+ */
+int ssm_oracle_ssd_fwd(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                       const double* x, const double* delta, const double* A, const double* B,
+                       const double* C, const double* Dskip, const double* dt_bias, int dt_softplus,
+                       const double* h0, double* y, double* last_state);
+
 #ifdef __cplusplus
 }
 #endif

@@ -430,7 +430,48 @@ def pin_backward_finite_differences(o, seed=12):
                 assert abs(fd - g[idx]) <= 1e-6 * (1 + abs(fd)), (k, idx, fd, g[idx])
 
 
+def pin_ssd_duality_and_mamba1(o, seed=13):
+    """Mamba-2 SSD ("Mamba and State Space Models", "Mamba-2 and State Space Duality"):
+    (1) the recurrence equals the masked quadratic form Y = tril(C B^T o M) (dt X) + D X
+    with M_ji = prod_{k=i+1..j} a_k, computed here by brute force with explicit products;
+    (2) with P = 1 every (head, p) is a Mamba-1 channel whose N states share the head's A,
+    so the result equals the (separately pinned) Mamba-1 oracle on those channels."""
+    rng = np.random.default_rng(seed)
+    b, L, H, P, N, G = 2, 9, 4, 3, 5, 2
+    x = rng.standard_normal((b, L, H, P))
+    raw = rng.standard_normal((b, L, H)) * 0.5
+    A = -rng.uniform(0.2, 2.0, H)
+    B = rng.standard_normal((b, L, G, N))
+    C = rng.standard_normal((b, L, G, N))
+    Dk = rng.standard_normal(H)
+    bias = rng.uniform(-0.5, 0.5, H)
+    h0 = rng.standard_normal((b, H, P, N))
+    y, last = o.ssd_fwd(x, raw, A, B, C, D=Dk, dt_bias=bias, dt_softplus=True, h0=h0)
+    dt = _softplus(raw + bias)
+    for bi in range(b):
+        for h in range(H):
+            g = h // (H // G)
+            a = np.exp(dt[bi, :, h] * A[h])
+            Yr = np.zeros((L, P))
+            for j in range(L):
+                pre = np.prod(a[:j + 1])                      # decay of h0 up to step j
+                Yr[j] += (h0[bi, h] @ C[bi, j, g]) * pre
+                for i in range(j + 1):
+                    m = np.prod(a[i + 1:j + 1])               # M_ji
+                    Yr[j] += (C[bi, j, g] @ B[bi, i, g]) * m * dt[bi, i, h] * x[bi, i, h]
+                Yr[j] += Dk[h] * x[bi, j, h]
+            assert _rel(y[bi, :, h], Yr) < 1e-13
+    # P = 1: Mamba-1 channels with a per-head A repeated over the N states
+    x1 = x[..., :1]
+    y1, l1 = o.ssd_fwd(x1, raw, A, B, C, D=Dk, dt_bias=bias, dt_softplus=True)
+    for g in range(G):
+        hs = list(range(g * (H // G), (g + 1) * (H // G)))
+        ym, lm = o.selective_scan_fwd(x1[:, :, hs, 0], raw[:, :, hs], np.repeat(A[hs, None], N, axis=1),
+                                      B[:, :, g], C[:, :, g], D=Dk[hs], delta_bias=bias[hs], delta_softplus=True)
+        assert _rel(y1[:, :, hs, 0], ym) < 1e-13 and _rel(l1[:, hs, 0, :], lm) < 1e-13
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_delta_zero_holds_state, pin_scalar_closed_form,
             pin_bruteforce_unrolling, pin_large_delta_reset, pin_stability_bound, pin_decode_matches_forward,
             pin_softplus_silu, pin_scan_operator, pin_decode_step_map, pin_zoh_solves_the_ode, pin_zoh_limits,
-            pin_conv_prologue, pin_backward_finite_differences]
+            pin_conv_prologue, pin_backward_finite_differences, pin_ssd_duality_and_mamba1]
