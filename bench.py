@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"] if os.path.exists(
     os.path.join(ROOT, "BASELINE.json")) else "selective-scan fwd GB/s & elem/s (B·L·D) on 1 B300; % of roofline"
 
-FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "sm_max_mhz": 2032.0, "source": "fallback"}
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "sm_max_mhz": 2032.0, "source": "fallback"}
 SM_COUNT = 148
 EX2_PER_CLK_SM = 32       # measured on B300: MUFU.EX2 32 lanes/clk/SM
 FP32_PER_CLK_SM = 128     # FFMA lanes/clk/SM
@@ -331,6 +331,8 @@ def run_ours(args, w, ws, rank, local):
         result["decode"] = decode_bench(args, ssm, torch, inputs, dev, hbm_peak)
     if not args.no_bwd:
         result["backward"] = backward_bench(args, ssm, torch, w, d, dev, launch_ms)
+    if not args.no_ssd:
+        result["ssd"] = ssd_bench(args, ssm, torch, inputs, dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
     if rank == 0:
@@ -405,6 +407,42 @@ def backward_bench(args, ssm, torch, w, d, dev, fwd_launch_ms):
             "gradients": "du, ddelta, dA, dB, dC, dD, dz, dbias (bf16 dy; fp32 accumulation)"}
 
 
+def ssd_bench(args, ssm, torch, inputs, dev, peaks):
+    """The Mamba-2 SSD workload (chunked, tensor cores): CUDA events around each call."""
+    w = inputs.SSD_M2
+    d = inputs.ssd_inputs(w, dev)
+    y = torch.empty_like(d["x"])
+    ls = torch.empty(w.batch, w.H, w.P, w.N, dtype=torch.float32, device=dev)
+
+    def call():
+        ssm.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], dt_bias=d["dt_bias"], dt_softplus=True,
+                    y=y, last_state=ls)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.ssd_steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    m = statistics.median(ms)
+    tf = w.flops() / (m / 1e3) / 1e12
+    tpk = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    gbs = w.compulsory_bytes() / (m / 1e3) / 1e9
+    hpk = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"workload": w.name, "ms": m, "tokens_per_s": w.tokens / (m / 1e3),
+            "roofline": {"bound": "tensor" if w.flops() / (tpk * 1e12) > w.compulsory_bytes() / (hpk * 1e9) else "hbm",
+                         "tensor": {"achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
+                                    "flops_per_call": w.flops()},
+                         "hbm": {"achieved_gbs": gbs, "peak_gbs": hpk, "frac": gbs / hpk,
+                                 "algorithmic_bytes": w.compulsory_bytes()}},
+            "calls": args.ssd_steps, "kernel": "mma.sync m16n8k16 bf16 (fp32 accumulate), one CTA per (batch, head)"}
+
+
 def decode_bench(args, ssm, torch, inputs, dev, hbm_peak):
     """The decode workload: 1024 single-token steps captured in one CUDA graph."""
     w = inputs.DECODE
@@ -459,6 +497,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=5)
+    ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--ssd-steps", type=int, default=10)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     args = ap.parse_args()

@@ -14,6 +14,8 @@
  *                            the same two with the block's causal width-4 depthwise
  *                            conv + SiLU (the step before the SSM) fused in front
  *   ssm_selective_scan_bwd   the backward pass of the forward pass (all gradients)
+ *   ssm_ssd_fwd              the Mamba-2 SSD forward pass (scalar decay per head,
+ *                            chunked, tensor cores)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -356,6 +358,39 @@ SSM_API ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_ten
  * partials of dA, dD, dbias. SSM_ERR_NULL (bytes == NULL) or SSM_ERR_SHAPE (negative). */
 SSM_API ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N,
                                                           size_t* bytes);
+
+/*
+ * ssm_ssd_fwd -- Mamba-2 SSD forward pass: the selective SSM with a scalar decay per head
+ * and a P x N matrix state per head ("Mamba and State Space Models", "Mamba-2 and State
+ * Space Duality"; "8.7 State Space Models (Mamba)", Mamba-2). For batch row b, head h,
+ * group g = h / (H / groups):
+ *   dt  = delta[b,t,h] + dt_bias[h], then softplus(dt) when dt_softplus
+ *   S   = exp(dt A[h]) S + dt x[b,t,h,:] B[b,t,g,:]^T        (S: P x N, from h0 or 0)
+ *   y[b,t,h,:] = S C[b,t,g,:] + D[h] x[b,t,h,:]
+ * computed in chunks of 64 steps: inside a chunk as the masked quadratic form
+ * tril(C B^T o decay) (dt X) plus the carried state read out, across chunks by carrying
+ * S on chip; the four contractions per chunk run on the tensor cores (bf16 operands,
+ * fp32 accumulation, fp32 state).
+ *
+ * Descriptors are 3-D views (the last two dimensions of each tensor flattened):
+ *   groups       number of B/C groups G (divides H)
+ *   x            (batch, L, H*P)   bf16    head h, channel p at h*P + p
+ *   delta        (batch, L, H)     bf16    raw step size
+ *   A            (H)               f32     decay rate per head (negative)
+ *   B, C         (batch, L, G*N)   bf16
+ *   D, dt_bias   (H)               f32, nullable
+ *   dt_softplus  0 or 1
+ *   h0           (batch, H, P*N)   f32, nullable   start state (row p, column n at p*N + n)
+ *   y            (batch, L, H*P)   bf16 or f32, written
+ *   last_state   (batch, H, P*N)   f32, nullable, written
+ * P = H*P / H and N = G*N / G must each be 64 or 128 (SSM_ERR_UNSUPPORTED otherwise); x,
+ * B, C 16-byte aligned. One CTA per (batch, head): batch <= 65535.
+ */
+SSM_API ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor_t* delta,
+                                 const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
+                                 const ssm_tensor_t* D, const ssm_tensor_t* dt_bias, int dt_softplus,
+                                 const ssm_tensor_t* h0, ssm_tensor_t* y, ssm_tensor_t* last_state,
+                                 void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

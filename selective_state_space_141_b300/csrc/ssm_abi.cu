@@ -18,6 +18,7 @@
 #include "scan_fwd.cuh"
 #include "scan_bwd.cuh"
 #include "scan_fwd_chan.cuh"
+#include "ssd_fwd.cuh"
 #include "state_update.cuh"
 
 namespace {
@@ -841,6 +842,97 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   float* dbp = dbias ? static_cast<float*>(dbias->data) : nullptr;
   e = gt == SSM_BF16 ? launch_bwd_reduce<__nv_bfloat16>(p, N, dB->data, dC->data, dAp, dDp, dbp, st)
                      : launch_bwd_reduce<float>(p, N, dB->data, dC->data, dAp, dDp, dbp, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+template <int P, int N>
+cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
+  constexpr int smem = ssm::ssd_smem_bytes<P, N>();
+  const void* kern = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, float>)
+                           : reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, __nv_bfloat16>);
+  const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  void* args[] = {const_cast<ssm::SsdParams*>(&p)};
+  return cudaLaunchKernel(kern, dim3((unsigned)p.H, (unsigned)p.batch), dim3(ssm::kSsdThreads), args, smem, st);
+}
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                         const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                         const ssm_tensor_t* dt_bias, int dt_softplus, const ssm_tensor_t* h0, ssm_tensor_t* y,
+                         ssm_tensor_t* last_state, void* stream) {
+  if (!x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+  if (x->ndim != 3 || A->ndim != 1 || B->ndim != 3) return SSM_ERR_SHAPE;
+  const int64_t batch = x->shape[0], L = x->shape[1], HP = x->shape[2], H = A->shape[0], GN = B->shape[2];
+  if (batch < 0 || L < 0 || HP < 0 || H <= 0 || groups <= 0 || H % groups != 0 || HP % H != 0 || GN % groups != 0)
+    return SSM_ERR_SHAPE;
+  const int64_t P = HP / H, N = GN / groups;
+  ssm_status_t s;
+  if ((s = check_tensor(x, {batch, L, HP})) != SSM_OK) return s;
+  if ((s = check_tensor(delta, {batch, L, H})) != SSM_OK) return s;
+  if ((s = check_tensor(A, {H})) != SSM_OK) return s;
+  if ((s = check_tensor(B, {batch, L, GN})) != SSM_OK) return s;
+  if ((s = check_tensor(C, {batch, L, GN})) != SSM_OK) return s;
+  if (D && (s = check_tensor(D, {H})) != SSM_OK) return s;
+  if (dt_bias && (s = check_tensor(dt_bias, {H})) != SSM_OK) return s;
+  if (h0 && (s = check_tensor(h0, {batch, H, P * N})) != SSM_OK) return s;
+  if ((s = check_tensor(y, {batch, L, HP})) != SSM_OK) return s;
+  if (last_state && (s = check_tensor(last_state, {batch, H, P * N})) != SSM_OK) return s;
+  if (x->dtype != SSM_BF16 || delta->dtype != SSM_BF16 || B->dtype != SSM_BF16 || C->dtype != SSM_BF16)
+    return SSM_ERR_DTYPE;
+  if (y->dtype != SSM_BF16 && y->dtype != SSM_F32) return SSM_ERR_DTYPE;
+  for (const ssm_tensor_t* t : {A, D, dt_bias, h0, static_cast<const ssm_tensor_t*>(last_state)})
+    if (t && t->dtype != SSM_F32) return SSM_ERR_DTYPE;
+  if (dt_softplus != 0 && dt_softplus != 1) return SSM_ERR_UNSUPPORTED;
+  if ((P != 64 && P != 128) || (N != 64 && N != 128) || batch > 65535 || H > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  for (const ssm_tensor_t* t : {x, B, C})  // 16-byte vector loads
+    if (numel(t) > 0 && reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return SSM_ERR_LAYOUT;
+  const ssm_tensor_t* ins[] = {x, delta, A, B, C, D, dt_bias, h0};
+  for (const ssm_tensor_t* in : ins) {
+    if (overlaps(y, in)) return SSM_ERR_LAYOUT;
+    if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
+  }
+  if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (batch == 0) return SSM_OK;
+  if (L == 0) {
+    if (!last_state) return SSM_OK;
+    const size_t bytes = (size_t)numel(last_state) * 4;
+    const cudaError_t e = h0 ? cudaMemcpyAsync(last_state->data, h0->data, bytes, cudaMemcpyDeviceToDevice, st)
+                             : cudaMemsetAsync(last_state->data, 0, bytes, st);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  }
+  ssm::SsdParams p;
+  p.x = static_cast<const __nv_bfloat16*>(x->data);
+  p.delta = static_cast<const __nv_bfloat16*>(delta->data);
+  p.A = static_cast<const float*>(A->data);
+  p.B = static_cast<const __nv_bfloat16*>(B->data);
+  p.C = static_cast<const __nv_bfloat16*>(C->data);
+  p.Dskip = D ? static_cast<const float*>(D->data) : nullptr;
+  p.dt_bias = dt_bias ? static_cast<const float*>(dt_bias->data) : nullptr;
+  p.dt_softplus = dt_softplus;
+  p.h0 = h0 ? static_cast<const float*>(h0->data) : nullptr;
+  p.y = y->data;
+  p.last_state = last_state ? static_cast<float*>(last_state->data) : nullptr;
+  p.batch = batch;
+  p.L = L;
+  p.H = H;
+  p.G = groups;
+  const bool yf = y->dtype == SSM_F32;
+  cudaError_t e;
+  if (P == 64 && N == 64)
+    e = launch_ssd<64, 64>(p, yf, st);
+  else if (P == 64)
+    e = launch_ssd<64, 128>(p, yf, st);
+  else if (N == 64)
+    e = launch_ssd<128, 64>(p, yf, st);
+  else
+    e = launch_ssd<128, 128>(p, yf, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

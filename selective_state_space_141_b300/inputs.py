@@ -178,3 +178,55 @@ def random_fwd(batch, L, D, N, dtype=torch.float32, device="cpu", seed=0, has_bi
     if not has_z:
         d["z"] = None
     return d
+
+
+# ---- Mamba-2 SSD ------------------------------------------------------------------------
+@dataclass(frozen=True)
+class SsdWorkload:
+    name: str
+    batch: int
+    L: int
+    H: int
+    P: int
+    N: int
+    G: int
+    seed: int
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.L
+
+    def flops(self, Q: int = 64) -> int:
+        """Tensor-core work of the chunked algorithm per call: per chunk and head the
+        contractions C B^T (2 Q^2 N), W X (2 Q^2 P), C S^T (2 Q N P) and X^T (w B) (2 Q N P),
+        i.e. 2 Q N + 2 Q P + 4 N P per token and head (a ragged last chunk counted whole)."""
+        chunks = (self.L + Q - 1) // Q
+        return self.batch * self.H * chunks * (2 * Q * Q * self.N + 2 * Q * Q * self.P + 4 * Q * self.N * self.P)
+
+    def compulsory_bytes(self) -> int:
+        """x and y (bf16), delta (bf16), B and C (bf16), A, D, dt_bias (fp32), last_state (fp32)."""
+        b, L, H, P, N, G = self.batch, self.L, self.H, self.P, self.N, self.G
+        return 2 * (2 * b * L * H * P + b * L * H + 2 * b * L * G * N) + 4 * 3 * H + 4 * b * H * P * N
+
+
+# A Mamba-2 layer in the pages' shape: "24 heads x 128 dims" per head; d_state 128 (the pages
+# give none for Mamba-2; the common choice), one B/C group.
+SSD_M2 = SsdWorkload("Mamba-2 layer SSD (4x4096, 24 heads x P=128, N=128, G=1)", 4, 4096, 24, 128, 128, 1, 7)
+
+
+def ssd_inputs(w: SsdWorkload, device="cpu", seed: int | None = None) -> dict:
+    """SSD tensors: x, B, C ~ N(0,1) and D ~ N(0,1) as for the Mamba-1 workloads; raw step
+    size ~ N(-2, 0.5) plus a bias ~ U(log(e^0.001 - 1), log(e^0.1 - 1)) through softplus;
+    A per head ~ -U(1, 16). bf16 x, delta, B, C; fp32 A, D, bias."""
+    g = _gen(device, w.seed if seed is None else seed)
+    b, L, H, P, N, G = w.batch, w.L, w.H, w.P, w.N, w.G
+    f32, bf = torch.float32, torch.bfloat16
+    x = torch.randn(b, L, H, P, generator=g, device=device, dtype=f32)
+    delta = torch.randn(b, L, H, generator=g, device=device, dtype=f32) * 0.5 - 2.0
+    B = torch.randn(b, L, G, N, generator=g, device=device, dtype=f32)
+    C = torch.randn(b, L, G, N, generator=g, device=device, dtype=f32)
+    D = torch.randn(H, generator=g, device=device, dtype=f32)
+    bias = torch.rand(H, generator=g, device=device, dtype=f32) * (BIAS_HI - BIAS_LO) + BIAS_LO
+    A = -(torch.rand(H, generator=g, device=device, dtype=f32) * 15.0 + 1.0)
+    return dict(x=x.to(bf).contiguous(), delta=delta.to(bf).contiguous(), A=A, B=B.to(bf).contiguous(),
+                C=C.to(bf).contiguous(), D=D, dt_bias=bias, dt_softplus=True)

@@ -74,6 +74,8 @@ def load_library(path: str | None = None):
                                                                                 ctypes.c_void_p]
     lib.ssm_selective_scan_bwd_workspace_size.restype = ctypes.c_int
     lib.ssm_selective_scan_bwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_ssd_fwd.restype = ctypes.c_int
+    lib.ssm_ssd_fwd.argtypes = [ctypes.c_int64] + [_P] * 7 + [ctypes.c_int, _P, _P, _P, ctypes.c_void_p]
     lib.ssm_state_update_ex.restype = ctypes.c_int
     lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -218,6 +220,28 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, d
     if st != 0:
         raise SsmError(st, "ssm_selective_scan_bwd")
     return {k: v for k, v in g.items() if v is not None}
+
+
+def ssd_fwd(x, delta, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None, y=None, last_state=None,
+            return_last_state=True, y_dtype=None, stream=None):
+    """Mamba-2 SSD forward (``ssm_ssd_fwd``). x: (batch, L, H, P) bf16; delta: (batch, L, H)
+    bf16; A, D, dt_bias: (H) fp32; B, C: (batch, L, G, N) bf16; h0: (batch, H, P, N) fp32.
+    Returns (y (batch, L, H, P), last_state (batch, H, P, N))."""
+    lib = load_library()
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    v3 = lambda t, shape: None if t is None else t.view(shape)
+    ds = [describe(t) for t in (v3(x, (b, L, H * P)), delta, A, v3(B, (b, L, G * N)), v3(C, (b, L, G * N)), D, dt_bias)]
+    st = lib.ssm_ssd_fwd(ctypes.c_int64(G), *[_ref(d) for d in ds], int(bool(dt_softplus)),
+                         _ref(describe(v3(h0, (b, H, P * N)))), _ref(describe(v3(y, (b, L, H * P)))),
+                         _ref(describe(v3(last_state, (b, H, P * N)))), _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_ssd_fwd")
+    return y, last_state
 
 
 def conv_selective_scan_fwd(x, conv_weight, delta, A, B, C, conv_bias=None, conv_state=None, D=None, z=None,

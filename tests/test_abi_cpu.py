@@ -314,3 +314,19 @@ def test_bwd_validation(lib):
     a = bwd_args()
     a["dB"] = T((2, 5, 8))
     assert call_bwd(lib, a) == 2
+
+
+def test_ssd_validation(lib):
+    b, L, H, P, N, G = 2, 5, 4, 64, 64, 2
+    x, dl, A = T((b, L, H * P)), T((b, L, H)), T((H,), ssm.SSM_F32)
+    Bm, Cm, y = T((b, L, G * N)), T((b, L, G * N)), T((b, L, H * P))
+    call = lambda g, x_=x, A_=A, B_=Bm, C_=Cm, y_=y, sp=1: lib.ssm_ssd_fwd(
+        ctypes.c_int64(g), ctypes.byref(x_), ctypes.byref(dl), ctypes.byref(A_), ctypes.byref(B_), ctypes.byref(C_),
+        None, None, sp, None, ctypes.byref(y_), None, None)
+    assert call(3) == 2                                              # groups must divide H
+    assert call(G, A_=T((3,), ssm.SSM_F32)) == 2                     # H must divide H*P
+    assert call(G, B_=T((b, L, G * 32)), C_=T((b, L, G * 32))) == 5  # N = 32 is not supported
+    assert call(G, x_=T((b, L, H * P), ssm.SSM_F32)) == 3            # bf16 inputs
+    assert call(G, y_=T((b, L, H * P), addr=x.data)) == 4            # y over x
+    assert call(G, x_=T((b, L, H * P), addr=x.data + 2)) == 4        # x not 16-byte aligned
+    assert call(G, sp=2) == 5
