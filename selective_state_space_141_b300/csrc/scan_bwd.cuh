@@ -13,14 +13,15 @@
 // of the states that "Hardware-Aware Parallel Scan" describes ("8.7 State Space Models
 // (Mamba)", section 4.1: the same (a, b) recurrence run backwards).
 //
-// Layout: one lane = one channel with all N states in registers (as the forward's
-// channel kernel), one warp per CTA. A forward sweep stores the state before every
+// Layout: two lanes per channel, each holding half of its N states in registers (a warp
+// covers 16 channels; one warp per CTA, several CTAs per SM), so that twice as many warps
+// hide the latency of the per-step dependency chains. A forward sweep stores the state before every
 // chunk of kBwdK steps (checkpoints); the reverse sweep recomputes a chunk's states into
 // shared memory, then walks it backwards. Each chunk's inputs are staged into shared
 // memory with asynchronous copies (cp.async), double-buffered: the next chunk streams
 // in while the current one is computed, and B, C are read as shared-memory broadcasts.
 // dB and dC are sums over channels: each warp
-// reduces its 32 lanes with a transpose-reduce butterfly (shuffles) and writes one
+// reduces its 16 channels with a transpose-reduce butterfly (shuffles) and writes one
 // partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over warps, and
 // dA, dD, dbias over batch rows, in a fixed order (deterministic, no atomics).
 #pragma once
@@ -58,22 +59,24 @@ struct BwdParams {
 };
 
 constexpr int kBwdK = 16;
+constexpr int kBwdCh = 16;  // channels per warp (two lanes per channel)
 
-// Sum over the 32 lanes of a warp of each of v[0..N-1]; lane l ends with the sum of
-// v[(l >> (5 - log2 N)) & (N - 1)] (two or more lanes hold each n). Each round halves
-// the values a lane holds: the lanes with the round's bit set keep the upper half and
-// send the lower, the others the reverse.
-template <int N>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
-  constexpr int kLogN = N == 16 ? 4 : N == 8 ? 3 : 2;
-  int m = N;
+// Sum over the warp's 16 channels (lanes of equal parity: lane = 2 * channel + half) of
+// each of v[0..NH-1]; lane l ends with the sum of v[(l >> (5 - log2 NH)) & (NH - 1)] of
+// its half. Each round halves the values a lane holds: the lanes with the round's bit set
+// keep the upper half and send the lower, the others the reverse; bit 0 (the half) is
+// never summed.
+template <int NH>
+__device__ __forceinline__ float pair_transpose_reduce(float (&v)[NH], int lane) {
+  constexpr int kLog = NH == 8 ? 3 : NH == 4 ? 2 : 1;
+  int m = NH;
 #pragma unroll
-  for (int r = 0; r < kLogN; ++r) {
+  for (int r = 0; r < kLog; ++r) {
     const int o = 16 >> r;
     const bool upper = (lane & o) != 0;
     const int half = m / 2;
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
+    for (int i = 0; i < NH / 2; ++i) {
       if (i < half) {
         const float send = upper ? v[i] : v[i + half];
         const float keep = upper ? v[i + half] : v[i];
@@ -84,7 +87,7 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
   }
   float s = v[0];
 #pragma unroll
-  for (int o = 16 >> kLogN; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  for (int o = 16 >> kLog; o >= 2; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
 }
 
@@ -100,21 +103,21 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Raw inputs of one chunk of kBwdK steps for the 32 channels of this warp.
 template <typename T, typename TG, int N>
 struct BwdStage {
-  T u[kBwdK][32];
-  T dl[kBwdK][32];
-  T z[kBwdK][32];
-  TG dy[kBwdK][32];
+  T u[kBwdK][kBwdCh];
+  T dl[kBwdK][kBwdCh];
+  T z[kBwdK][kBwdCh];
+  TG dy[kBwdK][kBwdCh];
   T B[kBwdK * N];
   T C[kBwdK * N];
 };
 
-// One (kBwdK x 32) tile of a (batch, L, D) tensor into smem. Asynchronous 16-byte copies
+// One (kBwdK x kBwdCh) tile of a (batch, L, D) tensor into smem. Asynchronous 16-byte copies
 // when every row start is 16-byte aligned (zero-filled past L and D), else plain loads.
 template <typename E>
-__device__ __forceinline__ void stage_rows(E (*dst)[32], const E* src, int64_t b, int64_t t0, int64_t L, int64_t D,
-                                           int64_t d0, bool async_ok, int lane) {
+__device__ __forceinline__ void stage_rows(E (*dst)[kBwdCh], const E* src, int64_t b, int64_t t0, int64_t L,
+                                           int64_t D, int64_t d0, bool async_ok, int lane) {
   if (async_ok) {
-    constexpr int kPieces = 32 * (int)sizeof(E) / 16;  // 16-byte pieces per row
+    constexpr int kPieces = kBwdCh * (int)sizeof(E) / 16;  // 16-byte pieces per row
     const int64_t valid_row = (D - d0) * (int64_t)sizeof(E);
     for (int q = lane; q < kBwdK * kPieces; q += 32) {
       const int k = q / kPieces, j = q % kPieces;
@@ -125,9 +128,10 @@ __device__ __forceinline__ void stage_rows(E (*dst)[32], const E* src, int64_t b
       cp_async16(reinterpret_cast<unsigned char*>(&dst[k][0]) + j * 16, g, (int)nb);
     }
   } else {
-    for (int k = 0; k < kBwdK; ++k) {
-      const int64_t t = t0 + k, d = d0 + lane;
-      dst[k][lane] = (t < L && d < D) ? src[(b * L + t) * D + d] : E(0.f);
+    for (int i = lane; i < kBwdK * kBwdCh; i += 32) {
+      const int k = i / kBwdCh, cc = i % kBwdCh;
+      const int64_t t = t0 + k, d = d0 + cc;
+      dst[k][cc] = (t < L && d < D) ? src[(b * L + t) * D + d] : E(0.f);
     }
   }
 }
@@ -177,44 +181,45 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
   return make_float2(ex2(x.x), ex2(x.y));
 }
 
-// grid (W = ceil(D / 32), batch), block 32 (one warp); dynamic shared memory:
-//   hs  [kBwdK + 1][N][32] f32   states h_{t0-1} .. h_{t0+K-1} of the chunk being walked
-//   bc  [kBwdK][2N]        f32   the chunk's B | C rows
-//   dts [kBwdK][32]        f32   its step sizes
-//   vs  [kBwdK][32]        f32   its read-outs C.h + D u (before the gate)
-//   stage[2]                     raw inputs of the current and the next chunk
+// grid (W = ceil(D / 16), batch), block 32 (one warp: 16 channels x two halves of the
+// states); dynamic shared memory:
+//   hs  [kBwdK + 1][N/2][32] f32  each lane's states h_{t0-1} .. h_{t0+K-1} of the chunk
+//   bc  [kBwdK][2N]          f32  the chunk's B | C rows
+//   dts [kBwdK][32]          f32  step sizes (both lanes of a channel hold the same)
+//   vs  [kBwdK][32]          f32  read-outs C.h + D u (before the gate)
+//   stage[2]                      raw inputs of the current and the next chunk
 template <typename T, typename TG, int N>
 constexpr int bwd_smem_bytes() {
-  return ((kBwdK + 1) * N * 32 + kBwdK * 2 * N + 2 * kBwdK * 32) * 4 + 2 * (int)sizeof(BwdStage<T, TG, N>);
+  return ((kBwdK + 1) * (N / 2) * 32 + kBwdK * 2 * N + 2 * kBwdK * 32) * 4 + 2 * (int)sizeof(BwdStage<T, TG, N>);
 }
 
 template <typename T, typename TG, int N>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
-  constexpr int P = N / 2;  // state pairs (packed f32x2 arithmetic)
+  constexpr int NH = N / 2;   // states per lane
+  constexpr int P2 = NH / 2;  // packed pairs per lane
   extern __shared__ __align__(16) float sm[];
   float* hs = sm;
-  float* bc = hs + (kBwdK + 1) * N * 32;
+  float* bc = hs + (kBwdK + 1) * NH * 32;
   float* dts = bc + kBwdK * 2 * N;
   float* vs = dts + kBwdK * 32;
   BwdStage<T, TG, N>* stg = reinterpret_cast<BwdStage<T, TG, N>*>(vs + kBwdK * 32);
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x, ch = lane >> 1, half = lane & 1, nb = half * NH;
   const int w = blockIdx.x;
   const int64_t b = blockIdx.y;
   const int64_t L = p.L, D = p.D;
-  const int64_t d0 = (int64_t)w * 32, d = d0 + lane;
+  const int64_t d0 = (int64_t)w * kBwdCh, d = d0 + ch;
   const bool vd = d < D;
   constexpr bool kAccurate = sizeof(T) == 4;
   const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
 
-  float2 Av[P], A2[P], h[P];
+  float2 Av[P2], A2[P2], h[P2];
 #pragma unroll
-  for (int q = 0; q < P; ++q) {
-    Av[q] = vd ? make_float2(p.A[d * N + 2 * q], p.A[d * N + 2 * q + 1]) : make_float2(0.f, 0.f);
+  for (int q = 0; q < P2; ++q) {
+    Av[q] = vd ? make_float2(p.A[d * N + nb + 2 * q], p.A[d * N + nb + 2 * q + 1]) : make_float2(0.f, 0.f);
     A2[q] = __fmul2_rn(Av[q], make_float2(kLog2e, kLog2e));
-    h[q] = (vd && p.h0) ? make_float2(p.h0[(b * D + d) * N + 2 * q], p.h0[(b * D + d) * N + 2 * q + 1])
+    h[q] = (vd && p.h0) ? make_float2(p.h0[(b * D + d) * N + nb + 2 * q], p.h0[(b * D + d) * N + nb + 2 * q + 1])
                         : make_float2(0.f, 0.f);
   }
-  // Converts the staged B (and C) of a chunk to fp32 for broadcast reads.
   auto convert_bc = [&](const BwdStage<T, TG, N>& sg, bool with_c) {
     for (int i = lane; i < kBwdK * N; i += 32) {
       const int k = i / N, n = i % N;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     __syncwarp();
   };
   auto step_dt = [&](const BwdStage<T, TG, N>& sg, int k, float* r_out) {
-    const float r = to_f32(sg.dl[k][lane]) + bias;
+    const float r = to_f32(sg.dl[k][ch]) + bias;
     if (r_out) *r_out = r;
     if (!p.delta_softplus) return r;
     if (kAccurate) return softplus_precise(r);
@@ -236,9 +241,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   if (p.nc > 1) stage_chunk<T, TG, N>(stg[0], p, b, 0, d0, false, lane);
   for (int c = 0; c < p.nc; ++c) {
     if (vd) {
-      float4* ckp = reinterpret_cast<float4*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N);
+      float2* ckp = reinterpret_cast<float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
 #pragma unroll
-      for (int q = 0; q < P; q += 2) ckp[q / 2] = make_float4(h[q].x, h[q].y, h[q + 1].x, h[q + 1].y);
+      for (int q = 0; q < P2; ++q) ckp[q] = h[q];
     }
     if (c == p.nc - 1) break;  // the state after the last chunk is not needed
     cp_async_wait_all();
@@ -248,29 +253,30 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     if (c + 1 < p.nc - 1) stage_chunk<T, TG, N>(stg[(c + 1) & 1], p, b, c + 1, d0, false, lane);
     for (int k = 0; k < kBwdK; ++k) {  // chunks before the last are full
       const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
-      const float dx = dt * to_f32(sg.u[k][lane]);
+      const float dx = dt * to_f32(sg.u[k][ch]);
       const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
+      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
 #pragma unroll
-      for (int q = 0; q < P; ++q)
+      for (int q = 0; q < P2; ++q)
         h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
     }
     __syncwarp();
   }
 
   // ---- reverse sweep ----
-  float2 g[P], dA_acc[P];
+  float2 g[P2], dA_acc[P2];
 #pragma unroll
-  for (int q = 0; q < P; ++q) {
-    g[q] = (vd && p.dlast) ? make_float2(p.dlast[(b * D + d) * N + 2 * q], p.dlast[(b * D + d) * N + 2 * q + 1])
+  for (int q = 0; q < P2; ++q) {
+    g[q] = (vd && p.dlast) ? make_float2(p.dlast[(b * D + d) * N + nb + 2 * q], p.dlast[(b * D + d) * N + nb + 2 * q + 1])
                            : make_float2(0.f, 0.f);
     dA_acc[q] = make_float2(0.f, 0.f);
   }
   float dD_acc = 0.f, dbias_acc = 0.f;
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
-  constexpr int kLogN = N == 16 ? 4 : N == 8 ? 3 : 2;
-  const int n_red = (lane >> (5 - kLogN)) & (N - 1);
-  const bool writer = (lane & ((32 / N) - 1)) == 0;
+  constexpr int kLog = NH == 8 ? 3 : NH == 4 ? 2 : 1;
+  const int n_red = nb + ((lane >> (5 - kLog)) & (NH - 1));
+  const bool writer = (lane & (((1 << (5 - kLog)) - 1) & ~1)) == 0;
+  const bool lead = half == 0 && vd;  // writes the channel's per-step outputs
   TG* du = static_cast<TG*>(p.du) + b * L * D + d;
   TG* ddl = static_cast<TG*>(p.ddelta) + b * L * D + d;
   TG* dzp = p.dz ? static_cast<TG*>(p.dz) + b * L * D + d : nullptr;
@@ -287,35 +293,31 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     if (c > 0) stage_chunk<T, TG, N>(stg[(c - 1) & 1], p, b, c - 1, d0, true, lane);
     // recompute the chunk's states and read-outs
     {
-      const float4* ckp = reinterpret_cast<const float4*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N);
+      const float2* ckp = reinterpret_cast<const float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
 #pragma unroll
-      for (int q = 0; q < P; q += 2) {
-        const float4 v4 = vd ? ckp[q / 2] : make_float4(0.f, 0.f, 0.f, 0.f);
-        h[q] = make_float2(v4.x, v4.y);
-        h[q + 1] = make_float2(v4.z, v4.w);
-      }
-#pragma unroll
-      for (int q = 0; q < P; ++q) {
+      for (int q = 0; q < P2; ++q) {
+        h[q] = vd ? ckp[q] : make_float2(0.f, 0.f);
         hs[(2 * q) * 32 + lane] = h[q].x;
         hs[(2 * q + 1) * 32 + lane] = h[q].y;
       }
       for (int k = 0; k < kc; ++k) {
         const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
-        const float x = to_f32(sg.u[k][lane]);
+        const float x = to_f32(sg.u[k][ch]);
         const float dx = dt * x;
         dts[k * 32 + lane] = dt;
         const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-        const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
-        const float2* c2 = b2 + P;
+        const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
+        const float2* c2 = reinterpret_cast<const float2*>(bc + k * 2 * N + N + nb);
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < P; ++q) {
+        for (int q = 0; q < P2; ++q) {
           h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
           acc = __ffma2_rn(c2[q], h[q], acc);
-          hs[((k + 1) * N + 2 * q) * 32 + lane] = h[q].x;
-          hs[((k + 1) * N + 2 * q + 1) * 32 + lane] = h[q].y;
+          hs[((k + 1) * NH + 2 * q) * 32 + lane] = h[q].x;
+          hs[((k + 1) * NH + 2 * q + 1) * 32 + lane] = h[q].y;
         }
-        vs[k * 32 + lane] = fmaf(Dk, x, acc.x + acc.y);
+        const float vp = acc.x + acc.y;
+        vs[k * 32 + lane] = fmaf(Dk, x, vp + __shfl_xor_sync(0xffffffffu, vp, 1));
       }
     }
     // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
@@ -324,24 +326,24 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       const float dt = dts[k * 32 + lane];
       float r = 0.f;
       if (vd) step_dt(sg, k, &r);
-      const float x = to_f32(sg.u[k][lane]), dyv = to_f32(sg.dy[k][lane]);
+      const float x = to_f32(sg.u[k][ch]), dyv = to_f32(sg.dy[k][ch]);
       const float v = vs[k * 32 + lane];
       float dv = dyv;
       if (dzp) {
-        const float zz = to_f32(sg.z[k][lane]);
+        const float zz = to_f32(sg.z[k][ch]);
         const float sgm = sigmoid(zz);
-        if (vd) dzp[t * D] = from_f32<TG>(dyv * v * (sgm * (1.f + zz * (1.f - sgm))));
+        if (lead) dzp[t * D] = from_f32<TG>(dyv * v * (sgm * (1.f + zz * (1.f - sgm))));
         dv = dyv * zz * sgm;
       }
       dD_acc = fmaf(dv, x, dD_acc);
       const float2 dv2 = make_float2(dv, dv), dt2 = make_float2(dt, dt), x2 = make_float2(x, x);
-      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N);
-      const float2* c2 = b2 + P;
+      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
+      const float2* c2 = reinterpret_cast<const float2*>(bc + k * 2 * N + N + nb);
       float2 dux2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
-      float vb[N], vc[N];
+      float vb[NH], vc[NH];
 #pragma unroll
-      for (int q = 0; q < P; ++q) {
-        const float2 hp = make_float2(hs[(k * N + 2 * q) * 32 + lane], hs[(k * N + 2 * q + 1) * 32 + lane]);
+      for (int q = 0; q < P2; ++q) {
+        const float2 hp = make_float2(hs[(k * NH + 2 * q) * 32 + lane], hs[(k * NH + 2 * q + 1) * 32 + lane]);
         const float2 a = decay2<kAccurate>(dt2, Av[q], A2[q]);
         const float2 B2 = b2[q];
         g[q] = __ffma2_rn(dv2, c2[q], g[q]);                 // g = dL/dh_t
@@ -359,15 +361,18 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
         vc[2 * q] = cv.x;
         vc[2 * q + 1] = cv.y;
       }
-      const float dux = fmaf(dv, Dk, dux2.x + dux2.y), ddt = ddt2.x + ddt2.y;
+      float dux = dux2.x + dux2.y, ddt = ddt2.x + ddt2.y;
+      dux += __shfl_xor_sync(0xffffffffu, dux, 1);          // the channel's other half
+      ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
+      dux = fmaf(dv, Dk, dux);
       const float dr = p.delta_softplus ? ddt * sigmoid(r) : ddt;
       dbias_acc += dr;
-      if (vd) {
+      if (lead) {
         du[t * D] = from_f32<TG>(dux);
         ddl[t * D] = from_f32<TG>(dr);
       }
-      const float sb = warp_transpose_reduce<N>(vb, lane);
-      const float sc = warp_transpose_reduce<N>(vc, lane);
+      const float sb = pair_transpose_reduce<NH>(vb, lane);
+      const float sc = pair_transpose_reduce<NH>(vc, lane);
       if (writer) {
         float* pp = part + t * p.W * 2 * N;
         pp[n_red] = sb;
@@ -379,17 +384,19 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
 
   if (vd) {
 #pragma unroll
-    for (int q = 0; q < P; ++q) {
-      p.dA_part[(b * D + d) * N + 2 * q] = dA_acc[q].x;
-      p.dA_part[(b * D + d) * N + 2 * q + 1] = dA_acc[q].y;
+    for (int q = 0; q < P2; ++q) {
+      p.dA_part[(b * D + d) * N + nb + 2 * q] = dA_acc[q].x;
+      p.dA_part[(b * D + d) * N + nb + 2 * q + 1] = dA_acc[q].y;
     }
-    p.dD_part[b * D + d] = dD_acc;
-    p.dbias_part[b * D + d] = dbias_acc;
+    if (half == 0) {
+      p.dD_part[b * D + d] = dD_acc;
+      p.dbias_part[b * D + d] = dbias_acc;
+    }
     if (p.dh0) {
 #pragma unroll
-      for (int q = 0; q < P; ++q) {
-        p.dh0[(b * D + d) * N + 2 * q] = g[q].x;
-        p.dh0[(b * D + d) * N + 2 * q + 1] = g[q].y;
+      for (int q = 0; q < P2; ++q) {
+        p.dh0[(b * D + d) * N + nb + 2 * q] = g[q].x;
+        p.dh0[(b * D + d) * N + nb + 2 * q + 1] = g[q].y;
       }
     }
   }

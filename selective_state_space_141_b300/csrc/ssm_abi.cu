@@ -646,7 +646,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 BwdPlan plan_bwd(int64_t batch, int64_t L, int64_t D, int64_t N) {
   BwdPlan pl;
   pl.nc = (int)((L + ssm::kBwdK - 1) / ssm::kBwdK);
-  pl.W = (int)((D + 31) / 32);
+  pl.W = (int)((D + ssm::kBwdCh - 1) / ssm::kBwdCh);
   size_t o = 0;
   pl.off_ck = o;
   o += round256((size_t)batch * pl.nc * D * N * 4);
