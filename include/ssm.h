@@ -383,14 +383,24 @@ SSM_API ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_
  *   h0           (batch, H, P*N)   f32, nullable   start state (row p, column n at p*N + n)
  *   y            (batch, L, H*P)   bf16 or f32, written
  *   last_state   (batch, H, P*N)   f32, nullable, written
+ *   workspace    at least ssm_ssd_fwd_workspace_size bytes, 256-byte aligned, overlapping
+ *                no tensor: the chunk-parallel schedule (every chunk's state contribution
+ *                computed at once, a carry over chunks, then every chunk's outputs);
+ *                NULL / too small: one CTA per (batch, head) walks the chunks in order
+ *                with the state on chip. Same arithmetic either way.
  * P = H*P / H and N = G*N / G must each be 64 or 128 (SSM_ERR_UNSUPPORTED otherwise); x,
- * B, C 16-byte aligned. One CTA per (batch, head): batch <= 65535.
+ * B, C 16-byte aligned; batch <= 65535.
  */
 SSM_API ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor_t* delta,
                                  const ssm_tensor_t* A, const ssm_tensor_t* B, const ssm_tensor_t* C,
                                  const ssm_tensor_t* D, const ssm_tensor_t* dt_bias, int dt_softplus,
                                  const ssm_tensor_t* h0, ssm_tensor_t* y, ssm_tensor_t* last_state,
-                                 void* stream);
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace for the chunk-parallel ssm_ssd_fwd schedule (0 for an empty problem):
+ * batch x ceil(L/64) x H x P x N x 6 bytes plus the chunk decays. SSM_ERR_NULL / SSM_ERR_SHAPE. */
+SSM_API ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
+                                                size_t* bytes);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

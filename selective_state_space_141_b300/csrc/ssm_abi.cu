@@ -848,6 +848,48 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* d
 }  // extern "C"
 
 namespace {
+// Workspace of the chunk-parallel SSD schedule: per (b, c, h) the chunk's state
+// contribution (fp32 P x N) and entering state (bf16 P x N), and per (b, h, c) its decay.
+struct SsdPlan {
+  size_t off_S = 0, off_H = 0, off_dec = 0, bytes = 0;
+};
+SsdPlan ssd_plan(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+  SsdPlan pl;
+  if (batch <= 0 || L <= 0 || H <= 0 || P <= 0 || N <= 0) return pl;
+  const size_t nc = (size_t)((L + ssm::kSsdQ - 1) / ssm::kSsdQ), e = (size_t)batch * nc * H * P * N;
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  pl.off_S = 0;
+  pl.off_H = r256(e * 4);
+  pl.off_dec = pl.off_H + r256(e * 2);
+  pl.bytes = pl.off_dec + r256((size_t)batch * H * nc * 4);
+  return pl;
+}
+
+template <int P, int N>
+cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
+  void* args[] = {const_cast<ssm::SsdParams*>(&p)};
+  const dim3 cgrid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.batch);
+  {
+    constexpr int smem = ssm::ssd_state_smem_bytes<P, N>();
+    const void* k = reinterpret_cast<const void*>(&ssm::ssd_chunk_state_kernel<P, N>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaLaunchKernel(k, cgrid, dim3(ssm::kSsdThreads), args, smem, st);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const int64_t n = p.batch * p.H * (int64_t)P * N;
+    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::ssd_state_pass_kernel<P, N>),
+                                           dim3((unsigned)((n + 255) / 256)), dim3(256), args, 0, st);
+    if (e != cudaSuccess) return e;
+  }
+  constexpr int smem = ssm::ssd_scan_smem_bytes<P, N>();
+  const void* k = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, float>)
+                        : reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, __nv_bfloat16>);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaLaunchKernel(k, cgrid, dim3(ssm::kSsdThreads), args, smem, st);
+  return e;
+}
+
 template <int P, int N>
 cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
   constexpr int smem = ssm::ssd_smem_bytes<P, N>();
@@ -862,10 +904,18 @@ cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
 
 extern "C" {
 
+ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, size_t* bytes) {
+  if (!bytes) return SSM_ERR_NULL;
+  if (batch < 0 || L < 0 || H < 0 || P < 0 || N < 0) return SSM_ERR_SHAPE;
+  *bytes = ssd_plan(batch, L, H, P, N).bytes;
+  return SSM_OK;
+}
+
 ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor_t* delta, const ssm_tensor_t* A,
                          const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
                          const ssm_tensor_t* dt_bias, int dt_softplus, const ssm_tensor_t* h0, ssm_tensor_t* y,
-                         ssm_tensor_t* last_state, void* stream) {
+                         ssm_tensor_t* last_state, void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace_bytes > 0 && !workspace) return SSM_ERR_NULL;
   if (!x || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (x->ndim != 3 || A->ndim != 1 || B->ndim != 3) return SSM_ERR_SHAPE;
   const int64_t batch = x->shape[0], L = x->shape[1], HP = x->shape[2], H = A->shape[0], GN = B->shape[2];
@@ -898,6 +948,19 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
     if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
   }
   if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
+  const SsdPlan plan = ssd_plan(batch, L, H, P, N);
+  const bool chunked = workspace && workspace_bytes >= plan.bytes && plan.bytes > 0 && H <= 65535;
+  if (chunked) {
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SSM_ERR_LAYOUT;
+    ssm_tensor_t w{};
+    w.data = workspace;
+    w.dtype = SSM_F32;
+    w.ndim = 1;
+    w.shape[0] = (int64_t)(workspace_bytes / 4);
+    const ssm_tensor_t* all[] = {x, delta, A, B, C, D, dt_bias, h0, y, last_state};
+    for (const ssm_tensor_t* t : all)
+      if (overlaps(&w, t)) return SSM_ERR_LAYOUT;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (batch == 0) return SSM_OK;
   if (L == 0) {
@@ -924,15 +987,25 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
   p.H = H;
   p.G = groups;
   const bool yf = y->dtype == SSM_F32;
+  p.nc = (int)((L + ssm::kSsdQ - 1) / ssm::kSsdQ);
+  p.ws_S = nullptr;
+  p.ws_H = nullptr;
+  p.ws_dec = nullptr;
+  if (chunked) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    p.ws_S = reinterpret_cast<float*>(ws + plan.off_S);
+    p.ws_H = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_H);
+    p.ws_dec = reinterpret_cast<float*>(ws + plan.off_dec);
+  }
   cudaError_t e;
   if (P == 64 && N == 64)
-    e = launch_ssd<64, 64>(p, yf, st);
+    e = chunked ? launch_ssd_chunked<64, 64>(p, yf, st) : launch_ssd<64, 64>(p, yf, st);
   else if (P == 64)
-    e = launch_ssd<64, 128>(p, yf, st);
+    e = chunked ? launch_ssd_chunked<64, 128>(p, yf, st) : launch_ssd<64, 128>(p, yf, st);
   else if (N == 64)
-    e = launch_ssd<128, 64>(p, yf, st);
+    e = chunked ? launch_ssd_chunked<128, 64>(p, yf, st) : launch_ssd<128, 64>(p, yf, st);
   else
-    e = launch_ssd<128, 128>(p, yf, st);
+    e = chunked ? launch_ssd_chunked<128, 128>(p, yf, st) : launch_ssd<128, 128>(p, yf, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

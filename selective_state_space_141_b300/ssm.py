@@ -75,7 +75,10 @@ def load_library(path: str | None = None):
     lib.ssm_selective_scan_bwd_workspace_size.restype = ctypes.c_int
     lib.ssm_selective_scan_bwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_ssd_fwd.restype = ctypes.c_int
-    lib.ssm_ssd_fwd.argtypes = [ctypes.c_int64] + [_P] * 7 + [ctypes.c_int, _P, _P, _P, ctypes.c_void_p]
+    lib.ssm_ssd_fwd.argtypes = [ctypes.c_int64] + [_P] * 7 + [ctypes.c_int, _P, _P, _P, ctypes.c_void_p,
+                                                              ctypes.c_size_t, ctypes.c_void_p]
+    lib.ssm_ssd_fwd_workspace_size.restype = ctypes.c_int
+    lib.ssm_ssd_fwd_workspace_size.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_state_update_ex.restype = ctypes.c_int
     lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -222,14 +225,32 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, d
     return {k: v for k, v in g.items() if v is not None}
 
 
+def ssd_workspace_size(batch, L, H, P, N) -> int:
+    """Bytes of workspace for the chunk-parallel ``ssm_ssd_fwd`` schedule."""
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.ssm_ssd_fwd_workspace_size(int(batch), int(L), int(H), int(P), int(N), ctypes.byref(n))
+    if st != 0:
+        raise SsmError(st, "ssm_ssd_fwd_workspace_size")
+    return int(n.value)
+
+
 def ssd_fwd(x, delta, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None, y=None, last_state=None,
-            return_last_state=True, y_dtype=None, stream=None):
+            return_last_state=True, y_dtype=None, stream=None, workspace=None, use_workspace=True):
     """Mamba-2 SSD forward (``ssm_ssd_fwd``). x: (batch, L, H, P) bf16; delta: (batch, L, H)
     bf16; A, D, dt_bias: (H) fp32; B, C: (batch, L, G, N) bf16; h0: (batch, H, P, N) fp32.
-    Returns (y (batch, L, H, P), last_state (batch, H, P, N))."""
+    With ``use_workspace`` (default) a workspace of ``ssd_workspace_size`` bytes is passed
+    (allocated here unless given): the chunk-parallel schedule; without, one CTA per
+    (batch, head). Returns (y (batch, L, H, P), last_state (batch, H, P, N))."""
     lib = load_library()
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
+    if workspace is None and use_workspace:
+        nbytes = ssd_workspace_size(b, L, H, P, N)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    ws_ptr = workspace.data_ptr() if use_workspace and workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
     if y is None:
         y = torch.empty(x.shape, dtype=y_dtype or x.dtype, device=x.device)
     if last_state is None and return_last_state:
@@ -238,7 +259,8 @@ def ssd_fwd(x, delta, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None, 
     ds = [describe(t) for t in (v3(x, (b, L, H * P)), delta, A, v3(B, (b, L, G * N)), v3(C, (b, L, G * N)), D, dt_bias)]
     st = lib.ssm_ssd_fwd(ctypes.c_int64(G), *[_ref(d) for d in ds], int(bool(dt_softplus)),
                          _ref(describe(v3(h0, (b, H, P * N)))), _ref(describe(v3(y, (b, L, H * P)))),
-                         _ref(describe(v3(last_state, (b, H, P * N)))), _stream(stream))
+                         _ref(describe(v3(last_state, (b, H, P * N)))), ctypes.c_void_p(ws_ptr),
+                         ctypes.c_size_t(ws_bytes), _stream(stream))
     if st != 0:
         raise SsmError(st, "ssm_ssd_fwd")
     return y, last_state

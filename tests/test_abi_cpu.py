@@ -322,7 +322,7 @@ def test_ssd_validation(lib):
     Bm, Cm, y = T((b, L, G * N)), T((b, L, G * N)), T((b, L, H * P))
     call = lambda g, x_=x, A_=A, B_=Bm, C_=Cm, y_=y, sp=1: lib.ssm_ssd_fwd(
         ctypes.c_int64(g), ctypes.byref(x_), ctypes.byref(dl), ctypes.byref(A_), ctypes.byref(B_), ctypes.byref(C_),
-        None, None, sp, None, ctypes.byref(y_), None, None)
+        None, None, sp, None, ctypes.byref(y_), None, None, ctypes.c_size_t(0), None)
     assert call(3) == 2                                              # groups must divide H
     assert call(G, A_=T((3,), ssm.SSM_F32)) == 2                     # H must divide H*P
     assert call(G, B_=T((b, L, G * 32)), C_=T((b, L, G * 32))) == 5  # N = 32 is not supported
@@ -330,3 +330,6 @@ def test_ssd_validation(lib):
     assert call(G, y_=T((b, L, H * P), addr=x.data)) == 4            # y over x
     assert call(G, x_=T((b, L, H * P), addr=x.data + 2)) == 4        # x not 16-byte aligned
     assert call(G, sp=2) == 5
+    n = ctypes.c_size_t(0)
+    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 64, 64, ctypes.byref(n)) == 0 and n.value > 0
+    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 64, 64, None) == 1

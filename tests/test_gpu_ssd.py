@@ -15,9 +15,9 @@ def case(b, L, H, P, N, G, seed):
     return inputs.ssd_inputs(inputs.SsdWorkload("t", b, L, H, P, N, G, seed), DEV)
 
 
-def gpu(d, h0=None, y_dtype=None):
+def gpu(d, h0=None, y_dtype=None, use_workspace=True):
     y, last = ssm.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], dt_bias=d["dt_bias"],
-                          dt_softplus=d["dt_softplus"], h0=h0, y_dtype=y_dtype)
+                          dt_softplus=d["dt_softplus"], h0=h0, y_dtype=y_dtype, use_workspace=use_workspace)
     torch.cuda.synchronize()
     return y, last
 
@@ -29,16 +29,18 @@ def ref(d, h0=None):
 
 @pytest.mark.parametrize("shape", [(2, 200, 3, 128, 128, 1), (1, 130, 4, 64, 64, 2), (2, 64, 2, 64, 128, 1),
                                    (1, 257, 2, 128, 64, 2), (1, 5, 2, 64, 64, 1)])
-def test_ssd_vs_oracle(shape):
+@pytest.mark.parametrize("schedule", ["chunk-parallel", "sequential"])
+def test_ssd_vs_oracle(shape, schedule):
     b, L, H, P, N, G = shape
     d = case(b, L, H, P, N, G, seed=101 + L)
     g = torch.Generator(device="cpu").manual_seed(102)
     h0 = torch.randn(b, H, P, N, generator=g).to(DEV)
     yr, lr = ref(d, h0)
-    y32, last = gpu(d, h0, y_dtype=torch.float32)
+    ws = schedule == "chunk-parallel"
+    y32, last = gpu(d, h0, y_dtype=torch.float32, use_workspace=ws)
     check(y32, yr, TOL_BF16, False, "y (fp32 output)")
     check(last, lr, TOL_BF16, False, "last_state")
-    y, _ = gpu(d, h0)
+    y, _ = gpu(d, h0, use_workspace=ws)
     check(y, yr, TOL_BF16, True, "y (bf16)")
 
 
@@ -66,10 +68,14 @@ def test_ssd_empty_sequence():
 
 
 def test_ssd_workload_sampled_heads():
-    """The bench's Mamba-2 layer, two sampled (batch, head) pairs vs the oracle."""
+    """The bench's Mamba-2 layer, two sampled (batch, head) pairs vs the oracle, and the
+    two schedules against each other over the whole output."""
     w = inputs.SSD_M2
     d = inputs.ssd_inputs(w, DEV)
     y, last = gpu(d, y_dtype=torch.float32)
+    y_s, last_s = gpu(d, y_dtype=torch.float32, use_workspace=False)
+    check(y, y_s, TOL_BF16, False, "chunk-parallel vs sequential y")
+    check(last, last_s, TOL_BF16, False, "chunk-parallel vs sequential last_state")
     for bi, h in ((0, 5), (3, 23)):
         sub = dict(x=d["x"][bi:bi + 1, :, h:h + 1], delta=d["delta"][bi:bi + 1, :, h:h + 1], A=d["A"][h:h + 1],
                    B=d["B"][bi:bi + 1], C=d["C"][bi:bi + 1], D=d["D"][h:h + 1], dt_bias=d["dt_bias"][h:h + 1],
