@@ -384,10 +384,11 @@ SSM_API ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_
  *   y            (batch, L, H*P)   bf16 or f32, written
  *   last_state   (batch, H, P*N)   f32, nullable, written
  *   workspace    at least ssm_ssd_fwd_workspace_size bytes, 256-byte aligned, overlapping
- *                no tensor: the chunk-parallel schedule (every chunk's state contribution
- *                computed at once, a carry over chunks, then every chunk's outputs);
- *                NULL / too small: one CTA per (batch, head) walks the chunks in order
- *                with the state on chip. Same arithmetic either way.
+ *                no tensor, H <= 65535: the chunk-parallel schedule (step sizes and the
+ *                chunks' C B^T first; then the state walked over the chunks by blocks of
+ *                32 state rows, writing every chunk's entering state; then every chunk's
+ *                outputs at once); NULL / too small: one CTA per (batch, head) walks the
+ *                chunks in order with the state on chip. Same arithmetic either way.
  * P = H*P / H and N = G*N / G must each be 64 or 128 (SSM_ERR_UNSUPPORTED otherwise); x,
  * B, C 16-byte aligned; batch <= 65535.
  */
@@ -398,9 +399,12 @@ SSM_API ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ss
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace for the chunk-parallel ssm_ssd_fwd schedule (0 for an empty problem):
- * batch x ceil(L/64) x H x P x N x 6 bytes plus the chunk decays. SSM_ERR_NULL / SSM_ERR_SHAPE. */
-SSM_API ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
-                                                size_t* bytes);
+ * batch x ceil(L/64) x H x (P x N x 2 + 512) bytes (per chunk and head: the entering state
+ * in bf16, the step sizes and decay exponents in fp32) plus batch x ceil(L/64) x groups x
+ * 16 KiB (C B^T of each chunk and group), each part rounded up to 256 bytes.
+ * SSM_ERR_NULL / SSM_ERR_SHAPE (negative sizes, groups < 1). */
+SSM_API ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t groups, int64_t P,
+                                                int64_t N, size_t* bytes);
 
 /* Human-readable name of a status code (static string, never NULL). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

@@ -36,12 +36,15 @@ struct SsdParams {
   void* y;                     // (batch, L, H, P), bf16 or f32
   float* last_state;           // (batch, H, P, N), nullable
   int64_t batch, L, H, G;
-  // chunk-parallel schedule (workspace): per (b, c, h) the chunk's own state
-  // contribution S_c (fp32, P x N), the state entering the chunk (bf16, P x N), and the
-  // chunk's decay exp(sum dt A)
-  float* ws_S;
+  // chunk-parallel schedule (workspace): per (b, c, h) the state entering the chunk
+  // (bf16 P x N in tensor-core fragment order: [P/8][N/16][32 lanes][2] pairs, the pair
+  // (row 8 j + lane / 4, columns 16 k + 2 (lane % 4) (+ 1)) and the same 8 columns on), its
+  // step sizes dt and cumulative decay exponents cs (fp32, Q each); per (b, c, g) C B^T of
+  // the chunk (fp32, Q x Q)
   __nv_bfloat16* ws_H;
-  float* ws_dec;
+  float* ws_dt;
+  float* ws_cs;
+  float* ws_CB;
   int nc;
 };
 
@@ -56,7 +59,7 @@ constexpr int ssd_smem_bytes() {
 }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
@@ -324,27 +327,134 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ssd_fwd_kernel(const SsdParams
 }
 
 // ---- chunk-parallel schedule ----------------------------------------------------------
-// Pass 1 (grid (nc, H, batch)): the state each chunk adds from zero, S_c = X^T diag(w) B,
-// and its decay exp(cs_end). Pass 2 (element-wise): H_0 = h0, H_{c+1} = dec_c H_c + S_c,
-// storing every entering state H_c (bf16: the operand of the read-out) and the final
-// state. Pass 3 (grid (nc, H, batch)): Y = W X + diag(exp(cs)) C H_c^T + D X. The same
-// per-chunk arithmetic as ssd_fwd_kernel, spread over every chunk at once.
+// Pass 0 (block per (b, c)): dt_t = softplus(delta + dt_bias) and cs_t = sum_{k<=t} dt_k A
+//   for every head of the chunk (dt = 0 past L), and C B^T of the chunk for every group
+//   (shared by the group's heads).
+// Pass 1 (CTA per (b, h, block of 32 state columns)): the state walk. The block's columns
+//   of S stay in tensor-core accumulators (fp32) from chunk to chunk:
+//     H_c -> workspace (bf16, the operand of the read-out),  S <- exp(cs_end) S + X^T (w B),
+//   w_t = exp(cs_end - cs_t) dt_t; the final S is last_state. Only the states the read-out
+//   needs leave the chip; each chunk's inputs arrive by cp.async while the previous chunk
+//   is computed.
+// Pass 2 (persistent, item = (b, c, h)): Y = W X + diag(exp(cs)) C H_c^T + D X, with W the
+//   group's C B^T masked to j >= i and decayed by exp(cs_j - cs_i) dt_i for this head.
+//   One CTA of 8 warps per SM walks the items (h fastest, so CTAs working at the same time
+//   share C B^T and C in L2); each item's inputs arrive by cp.async into a 2-stage ring
+//   while the previous item is computed.
+// Fragments come from shared memory by ldmatrix (transposed where the contraction runs
+// over time); w B and W reach the tensor cores as bf16 high + low pairs.
 
+__device__ __forceinline__ uint32_t ssd_saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const __nv_bfloat16* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(ssd_saddr(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const __nv_bfloat16* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(ssd_saddr(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const __nv_bfloat16* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(ssd_saddr(p))
+               : "memory");
+}
+// 16-byte global -> shared copy; zero fill when !valid (src must still be a mapped address)
+__device__ __forceinline__ void ssd_cp16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ssd_saddr(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void ssd_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void ssd_cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+// (lo, hi) bf16 halves of a fragment register as floats (lo = the lower index)
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t r) {
+  return make_float2(__uint_as_float(r << 16), __uint_as_float(r & 0xffff0000u));
+}
+// v -> (high, low) bf16 pairs with high + low = v to ~16 significant bits
+__device__ __forceinline__ void split_bf16x2(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v.x, v.y);
+  const float2 h = bf16x2_to_f2(hi);
+  lo = pack_bf16(v.x - h.x, v.y - h.y);
+}
+
+// Q rows of W 16-byte chunks each, row t of a (batch, L, ...) tensor at src + t * pitch,
+// zero past rows_valid, into dst with row stride ld (elements).
+template <int W>
+__device__ __forceinline__ void ssd_stage_rows(__nv_bfloat16* dst, int ld, const __nv_bfloat16* src, int64_t pitch,
+                                               int64_t rows_valid, const __nv_bfloat16* any, int tid) {
+  for (int i = tid; i < kSsdQ * W; i += kSsdThreads) {
+    const int t = i / W, k = i % W;
+    const bool v = t < rows_valid;
+    ssd_cp16(dst + t * ld + 8 * k, v ? src + t * pitch + 8 * k : any, v);
+  }
+}
+// dt and cs of item it (Q floats each) into a stage.
+__device__ __forceinline__ void ssd_stage_floats(unsigned char* st, const SsdParams& p, int64_t it, int off_dt,
+                                                 int off_cs, int tid) {
+  if (tid < 2 * (kSsdQ / 4)) {
+    const int k = tid % (kSsdQ / 4);
+    const float* src = (tid < kSsdQ / 4 ? p.ws_dt : p.ws_cs) + it * kSsdQ + 4 * k;
+    ssd_cp16(st + (tid < kSsdQ / 4 ? off_dt : off_cs) + 16 * k, src, true);
+  }
+}
+
+constexpr int kSsdNB = 32;  // state columns per CTA of the state walk
+
+template <int P>
+struct SsdWalkStage {
+  static constexpr int LP = P + kSsdPad, LB = kSsdNB + kSsdPad;
+  static constexpr int kX = 0, kB = kX + kSsdQ * LP * 2, kDt = kB + kSsdQ * LB * 2, kCs = kDt + kSsdQ * 4;
+  static constexpr int kBytes = kCs + kSsdQ * 4, kStages = 2;
+  static constexpr int kWB = kStages * kBytes;  // (w B) high and low, two buffers: [2][2][Q][LB] bf16
+  static_assert(kBytes % 16 == 0, "stage layout");
+};
 template <int P, int N>
-constexpr int ssd_state_smem_bytes() {
-  constexpr int LQ = kSsdQ + kSsdPad;
-  return 2 * (P * LQ + 2 * N * LQ + kSsdQ * (N + kSsdPad)) + 4 * 2 * kSsdQ;
+struct SsdScanStage {
+  static constexpr int LN = N + kSsdPad, LP = P + kSsdPad, LW = kSsdQ + 4, LQ = kSsdQ + kSsdPad;
+  static constexpr int kC = 0, kW = kC + kSsdQ * LN * 2, kX = kW + kSsdQ * LW * 4, kH = kX + kSsdQ * LP * 2;
+  static constexpr int kDt = kH + P * N * 2, kCs = kDt + kSsdQ * 4, kBytes = kCs + kSsdQ * 4, kStages = 2;
+  static constexpr int kWhl = kStages * kBytes;  // W high and low parts, [Q][LQ] bf16 each
+  static_assert(kBytes % 16 == 0, "stage layout");
+};
+template <int P>
+constexpr int ssd_walk_smem_bytes() {
+  return SsdWalkStage<P>::kWB + 4 * kSsdQ * SsdWalkStage<P>::LB * 2;
 }
 template <int P, int N>
 constexpr int ssd_scan_smem_bytes() {
-  constexpr int LQ = kSsdQ + kSsdPad, LN = N + kSsdPad;
-  return 2 * (P * LQ + 2 * kSsdQ * LN + 2 * kSsdQ * LQ + P * LN) + 4 * 2 * kSsdQ;
+  return SsdScanStage<P, N>::kWhl + 2 * kSsdQ * SsdScanStage<P, N>::LQ * 2;
 }
 
-// cs_j = sum_{k <= j} dt_k A over the chunk (warp 0; dt = 0 on padded steps).
-__device__ __forceinline__ void ssd_cumsum(const float* dts, float* cs, float Ah, int warp, int lane) {
-  if (warp == 0) {
-    const float v0 = dts[2 * lane] * Ah, v1 = dts[2 * lane + 1] * Ah;
+// Pass 0. grid (nc, batch), block 256. (a) warp w takes heads w, w + 8, ...; lane l steps
+// 2l, 2l + 1. (b) per group g: CB = C B^T of the chunk (fp32, Q x Q, zero rows and columns
+// past L); warp w computes rows 16 (w & 3) .. + 15, columns 32 (w >> 2) .. + 31.
+template <int N>
+__global__ void __launch_bounds__(256) ssd_prep_kernel(const SsdParams p) {
+  constexpr int Q = kSsdQ, LN = N + kSsdPad;
+  __shared__ __align__(16) __nv_bfloat16 Cs[Q * LN], Bs[Q * LN];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3, c = blockIdx.x;
+  const int64_t b = blockIdx.y, t0 = (int64_t)c * Q, t = t0 + 2 * lane;
+  for (int64_t h = warp; h < p.H; h += 8) {
+    const float bias = p.dt_bias ? p.dt_bias[h] : 0.f, Ah = p.A[h];
+    float d[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      d[k] = 0.f;
+      if (t + k < p.L) {
+        const float r = __bfloat162float(p.delta[(b * p.L + t + k) * p.H + h]) + bias;
+        d[k] = p.dt_softplus ? softplus_precise(r) : r;
+      }
+    }
+    const float v0 = d[0] * Ah, v1 = d[1] * Ah;
     float s = v0 + v1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -352,206 +462,332 @@ __device__ __forceinline__ void ssd_cumsum(const float* dts, float* cs, float Ah
       if (lane >= o) s += up;
     }
     const float ex = s - (v0 + v1);
-    cs[2 * lane] = ex + v0;
-    cs[2 * lane + 1] = ex + v0 + v1;
+    const int64_t o = ((b * p.nc + c) * p.H + h) * Q + 2 * lane;
+    *reinterpret_cast<float2*>(p.ws_dt + o) = make_float2(d[0], d[1]);
+    *reinterpret_cast<float2*>(p.ws_cs + o) = make_float2(ex + v0, ex + v0 + v1);
   }
-}
-
-template <int P, int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdParams p) {
-  constexpr int Q = kSsdQ, LQ = Q + kSsdPad, LN = N + kSsdPad;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* XT = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [P][LQ]
-  __nv_bfloat16* wBT = XT + P * LQ;                                 // [N][LQ] high
-  __nv_bfloat16* wBL = wBT + N * LQ;                                // [N][LQ] low
-  __nv_bfloat16* Bs = wBL + N * LQ;                                 // [Q][LN]
-  float* dts = reinterpret_cast<float*>(Bs + Q * LN);
-  float* cs = dts + Q;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int c = blockIdx.x;
-  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G), t0 = (int64_t)c * Q;
-  {
-    SsdChunkRegs<P, N> r;
-    ssd_fetch<P, N, false>(r, p, b, h, g, t0, tid);  // C is not needed here
-    ssd_store<P, N, false>(r, XT, Bs, nullptr, dts, tid);
-  }
-  __syncthreads();
-  ssd_cumsum(dts, cs, p.A[h], warp, lane);
-  __syncthreads();
-  const float cs_end = cs[Q - 1];
-  for (int i = tid; i < Q * N; i += kSsdThreads) {
-    const int t = i % Q, n = i / Q;
-    const float v = __bfloat162float(Bs[t * LN + n]) * __expf(cs_end - cs[t]) * dts[t];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    wBT[n * LQ + t] = hi;
-    wBL[n * LQ + t] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  }
-  __syncthreads();
-  constexpr int MT = P / 16, WPM = 8 / MT, NTW = (N / 8) / WPM;
-  const int mt = warp % MT, nq = warp / MT;
-  float acc[NTW][4] = {};
-#pragma unroll
-  for (int k0 = 0; k0 < Q; k0 += 16) {
-    uint32_t a[4];
-    frag_a(a, XT, LQ, mt * 16, k0, lane);
-#pragma unroll
-    for (int nt = 0; nt < NTW; ++nt) {
-      uint32_t bb[2];
-      frag_b(bb, wBT, LQ, (nq * NTW + nt) * 8, k0, lane);
-      mma_16816(acc[nt], a, bb);
-      frag_b(bb, wBL, LQ, (nq * NTW + nt) * 8, k0, lane);
-      mma_16816(acc[nt], a, bb);
+  const int64_t rv = p.L - t0;
+  const int mt = warp & 3, n0 = (warp >> 2) * 32;
+  for (int64_t g = 0; g < p.G; ++g) {
+    __syncthreads();  // the previous group's tiles are no longer read
+    for (int i = tid; i < Q * (N / 8); i += 256) {
+      const int r = i / (N / 8), k = i % (N / 8);
+      const int64_t o = ((b * p.L + t0 + r) * p.G + g) * N + 8 * k;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(Cs + r * LN + 8 * k) = r < rv ? *reinterpret_cast<const uint4*>(p.C + o) : z;
+      *reinterpret_cast<uint4*>(Bs + r * LN + 8 * k) = r < rv ? *reinterpret_cast<const uint4*>(p.B + o) : z;
     }
-  }
-  float* S = p.ws_S + (((b * p.nc + c) * p.H + h) * P) * N;
-#pragma unroll
-  for (int nt = 0; nt < NTW; ++nt) {
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int pr = mt * 16 + gq + 8 * hf, nc0 = (nq * NTW + nt) * 8 + 2 * tq;
-      *reinterpret_cast<float2*>(S + pr * N + nc0) = make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
-    }
-  }
-  if (tid == 0) p.ws_dec[(b * p.H + h) * p.nc + c] = __expf(cs_end);
-}
-
-// One thread per (b, h, state element): the carry over chunks.
-template <int P, int N>
-__global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdParams p) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over batch * H * P * N
-  constexpr int64_t PN = (int64_t)P * N;
-  if (i >= p.batch * p.H * PN) return;
-  const int64_t e = i % PN, bh = i / PN, h = bh % p.H, b = bh / p.H;
-  float st = p.h0 ? p.h0[bh * PN + e] : 0.f;
-  const float* dec = p.ws_dec + bh * p.nc;
-  const int64_t cstride = p.H * PN;  // from one chunk's entry to the next
-  const float* S = p.ws_S + ((b * p.nc) * p.H + h) * PN + e;
-  __nv_bfloat16* Ho = p.ws_H + ((b * p.nc) * p.H + h) * PN + e;
-  // Eight chunks' contributions are loaded before any of them is used (the stores of the
-  // entering states would otherwise keep each load behind the previous store).
-  for (int c0 = 0; c0 < p.nc; c0 += 8) {
-    float sv[8], dv[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      sv[k] = c0 + k < p.nc ? __ldg(S + (c0 + k) * cstride) : 0.f;
-      dv[k] = c0 + k < p.nc ? __ldg(dec + c0 + k) : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (c0 + k < p.nc) {
-        Ho[(c0 + k) * cstride] = __float2bfloat16_rn(st);
-        st = fmaf(dv[k], st, sv[k]);
-      }
-    }
-  }
-  if (p.last_state) p.last_state[bh * PN + e] = st;
-}
-
-template <int P, int N, typename TY>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdParams p) {
-  constexpr int Q = kSsdQ, LQ = Q + kSsdPad, LN = N + kSsdPad;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* XT = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [P][LQ]
-  __nv_bfloat16* Bs = XT + P * LQ;                                  // [Q][LN]
-  __nv_bfloat16* Cs = Bs + Q * LN;                                  // [Q][LN]
-  __nv_bfloat16* Ws = Cs + Q * LN;                                  // [Q][LQ] high
-  __nv_bfloat16* WsL = Ws + Q * LQ;                                 // [Q][LQ] low
-  __nv_bfloat16* Hb = WsL + Q * LQ;                                 // [P][LN] entering state
-  float* dts = reinterpret_cast<float*>(Hb + P * LN);
-  float* cs = dts + Q;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int c = blockIdx.x;
-  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G), t0 = (int64_t)c * Q;
-  const int tc = (int)((p.L - t0) < Q ? (p.L - t0) : Q);
-  const float Dh = p.Dskip ? p.Dskip[h] : 0.f;
-  {
-    SsdChunkRegs<P, N> r;
-    ssd_fetch<P, N>(r, p, b, h, g, t0, tid);
-    ssd_store<P, N>(r, XT, Bs, Cs, dts, tid);
-    const __nv_bfloat16* Hg = p.ws_H + (((b * p.nc + c) * p.H + h) * P) * N;
-    for (int i = tid; i < P * N / 8; i += kSsdThreads) {
-      const int pr = (i * 8) / N, n0 = (i * 8) % N;
-      *reinterpret_cast<uint4*>(Hb + pr * LN + n0) = *reinterpret_cast<const uint4*>(Hg + pr * N + n0);
-    }
-  }
-  __syncthreads();
-  ssd_cumsum(dts, cs, p.A[h], warp, lane);
-  __syncthreads();
-  {
-    const int mt = warp & 3, nh = warp >> 2;
+    __syncthreads();
     float acc[4][4] = {};
 #pragma unroll
-    for (int k0 = 0; k0 < N; k0 += 16) {
+    for (int ks = 0; ks < N / 16; ++ks) {
       uint32_t a[4];
-      frag_a(a, Cs, LN, mt * 16, k0, lane);
+      ldsm_x4(a, Cs + (mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LN + ks * 16 + (lane >> 4) * 8);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        uint32_t bb[2];
-        frag_b(bb, Bs, LN, nh * 32 + nt * 8, k0, lane);
-        mma_16816(acc[nt], a, bb);
+      for (int np = 0; np < 2; ++np) {
+        uint32_t bb[4];
+        ldsm_x4(bb, Bs + (n0 + np * 16 + (lane & 7) + (lane >> 4) * 8) * LN + ks * 16 + ((lane >> 3) & 1) * 8);
+        const uint32_t b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
+        mma_16816(acc[2 * np], a, b0);
+        mma_16816(acc[2 * np + 1], a, b1);
       }
     }
+    float* CB = p.ws_CB + ((b * p.nc + c) * p.G + g) * Q * Q;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int j = mt * 16 + gq + 8 * hf, i0 = nh * 32 + nt * 8 + 2 * tq;
-        const float w0 = j >= i0 ? acc[nt][2 * hf] * __expf(cs[j] - cs[i0]) * dts[i0] : 0.f;
-        const float w1 = j >= i0 + 1 ? acc[nt][2 * hf + 1] * __expf(cs[j] - cs[i0 + 1]) * dts[i0 + 1] : 0.f;
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
-        *reinterpret_cast<__nv_bfloat162*>(Ws + j * LQ + i0) = hi;
-        *reinterpret_cast<uint32_t*>(WsL + j * LQ + i0) = pack_bf16(w0 - __low2float(hi), w1 - __high2float(hi));
+      for (int hf = 0; hf < 2; ++hf)
+        *reinterpret_cast<float2*>(CB + (mt * 16 + gq + 8 * hf) * Q + n0 + nt * 8 + 2 * tq) =
+            make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
+  }
+}
+
+// Pass 1. grid (N / 32, H, batch), block 256: the CTA holds state columns 32 bx .. + 31 and
+// all P rows; warp w holds rows 16 (w % MT) .. + 15 (MT = P / 16 row tiles) and NTW column
+// tiles of 8 starting at 8 NTW (w / MT). Per chunk, w B of the CTA's columns is formed once
+// in shared memory (bf16 high + low); X^T comes straight from the staged X by ldmatrix.
+template <int P, int N>
+__global__ void __launch_bounds__(kSsdThreads, 3) ssd_state_walk_kernel(const SsdParams p) {
+  using St = SsdWalkStage<P>;
+  constexpr int Q = kSsdQ, S = St::kStages, LP = St::LP, LB = St::LB, NB = kSsdNB;
+  constexpr int MT = P / 16, WPM = 8 / MT, NTW = (NB / 8) / WPM;
+  static_assert(MT * WPM == 8 && NTW % 2 == 0, "warp tiling");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* wBbuf = reinterpret_cast<__nv_bfloat16*>(smem_raw + St::kWB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const int nb0 = blockIdx.x * NB;
+  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G);
+  const int row0 = (warp % MT) * 16, col0 = (warp / MT) * NTW * 8;  // within the CTA's block
+  const int nc = p.nc;
+  auto load = [&](int s, int c) {
+    unsigned char* st = smem_raw + s * St::kBytes;
+    const int64_t t0 = (int64_t)c * Q, rv = p.L - t0;
+    ssd_stage_rows<P / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kX), LP, p.x + ((b * p.L + t0) * p.H + h) * P,
+                          p.H * P, rv, p.x, tid);
+    ssd_stage_rows<NB / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kB), LB,
+                           p.B + ((b * p.L + t0) * p.G + g) * N + nb0, p.G * N, rv, p.B, tid);
+    ssd_stage_floats(st, p, (b * nc + c) * p.H + h, St::kDt, St::kCs, tid);
+  };
+  // acc[nt]: rows row0 + gq (+ 8), columns nb0 + col0 + 8 nt + 2 tq (+ 1)
+  const int64_t sbase = ((b * p.H + h) * P + row0 + gq) * N + nb0 + col0 + 2 * tq;
+  float acc[NTW][4];
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const float2 v = p.h0 ? *reinterpret_cast<const float2*>(p.h0 + sbase + 8 * hf * N + 8 * nt)
+                            : make_float2(0.f, 0.f);
+      acc[nt][2 * hf] = v.x;
+      acc[nt][2 * hf + 1] = v.y;
+    }
+#pragma unroll
+  for (int k = 0; k < S - 1; ++k) {
+    if (k < nc) load(k, k);
+    ssd_cp_commit();
+  }
+  for (int c = 0; c < nc; ++c) {
+    ssd_cp_wait<S - 2>();  // chunk c has landed (this thread's copies)
+    __syncthreads();       // ... everyone's; and every warp is done with chunk c - 1
+    if (c + S - 1 < nc) load((c + S - 1) % S, c + S - 1);
+    ssd_cp_commit();
+    const unsigned char* st = smem_raw + (c % S) * St::kBytes;
+    const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(st + St::kX);  // [t][p]
+    const __nv_bfloat16* Bs = reinterpret_cast<const __nv_bfloat16*>(st + St::kB);  // [t][n of the block]
+    const float* dts = reinterpret_cast<const float*>(st + St::kDt);
+    const float* css = reinterpret_cast<const float*>(st + St::kCs);
+    __nv_bfloat16* wbh = wBbuf + (c & 1) * 2 * Q * LB;  // [t][n] high
+    __nv_bfloat16* wbl = wbh + Q * LB;                   // [t][n] low
+    const float cs_end = css[Q - 1];
+    static_assert(NB == 32, "w B rows: half a warp per row");
+    for (int e = tid; e < Q * NB / 2; e += kSsdThreads) {
+      // a warp covers rows t and t + 4 (80-byte pitch: disjoint banks)
+      const int q = e >> 5, l = e & 31, t = (q >> 2) * 8 + (q & 3) + (l >> 4) * 4, n = 2 * (l & 15);
+      const float w = __expf(cs_end - css[t]) * dts[t];
+      const float2 v = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(Bs + t * LB + n));
+      uint32_t hi, lo;
+      split_bf16x2(make_float2(v.x * w, v.y * w), hi, lo);
+      *reinterpret_cast<uint32_t*>(wbh + t * LB + n) = hi;
+      *reinterpret_cast<uint32_t*>(wbl + t * LB + n) = lo;
+    }
+    // the state entering chunk c, for the read-out, in fragment order (256 contiguous bytes
+    // per warp store)
+    uint2* Ho = reinterpret_cast<uint2*>(p.ws_H + ((b * nc + c) * p.H + h) * (int64_t)P * N) + lane;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int kp = 0; kp < NTW / 2; ++kp)
+        Ho[((row0 / 8 + hf) * (N / 16) + (nb0 + col0) / 16 + kp) * 32] =
+            make_uint2(pack_bf16(acc[2 * kp][2 * hf], acc[2 * kp][2 * hf + 1]),
+                       pack_bf16(acc[2 * kp + 1][2 * hf], acc[2 * kp + 1][2 * hf + 1]));
+    const float dec = __expf(cs_end);
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][e] *= dec;
+    __syncthreads();  // w B is complete
+#pragma unroll
+    for (int ks = 0; ks < Q / 16; ++ks) {
+      const int k0 = ks * 16;
+      uint32_t a[4];  // (X^T)[p][t] fragment, from X stored [t][p]
+      ldsm_x4_t(a, Xs + (k0 + (lane & 7) + (lane >> 4) * 8) * LP + row0 + ((lane >> 3) & 1) * 8);
+      uint32_t bh[NTW / 2][4], bl[NTW / 2][4];
+#pragma unroll
+      for (int np = 0; np < NTW / 2; ++np) {
+        const int o = (k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * LB + col0 + np * 16 + (lane >> 4) * 8;
+        ldsm_x4_t(bh[np], wbh + o);
+        ldsm_x4_t(bl[np], wbl + o);
+      }
+#pragma unroll
+      for (int np = 0; np < NTW / 2; ++np) {
+        const uint32_t b0[2] = {bh[np][0], bh[np][1]}, b1[2] = {bh[np][2], bh[np][3]};
+        mma_16816(acc[2 * np], a, b0);
+        mma_16816(acc[2 * np + 1], a, b1);
+      }
+#pragma unroll
+      for (int np = 0; np < NTW / 2; ++np) {
+        const uint32_t b0[2] = {bl[np][0], bl[np][1]}, b1[2] = {bl[np][2], bl[np][3]};
+        mma_16816(acc[2 * np], a, b0);
+        mma_16816(acc[2 * np + 1], a, b1);
       }
     }
   }
-  __syncthreads();
-  {
-    constexpr int NT = P / 16;
-    const int mt = warp & 3, nh = warp >> 2;
-    float ad[NT][4] = {}, ao[NT][4] = {};
+  if (p.last_state) {
 #pragma unroll
-    for (int k0 = 0; k0 < Q; k0 += 16) {
-      uint32_t a[4], al[4];
-      frag_a(a, Ws, LQ, mt * 16, k0, lane);
-      frag_a(al, WsL, LQ, mt * 16, k0, lane);
+    for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        uint32_t bb[2];
-        frag_b(bb, XT, LQ, nh * (P / 2) + nt * 8, k0, lane);
-        mma_16816(ad[nt], a, bb);
-        mma_16816(ad[nt], al, bb);
+      for (int hf = 0; hf < 2; ++hf)
+        *reinterpret_cast<float2*>(p.last_state + sbase + 8 * hf * N + 8 * nt) =
+            make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
+  }
+  ssd_cp_wait<0>();
+}
+
+// Item (b, c, h) of the persistent read-out pass.
+struct SsdItem {
+  int64_t b, c, h, g, t0;
+};
+__device__ __forceinline__ SsdItem ssd_item(const SsdParams& p, int64_t it) {
+  SsdItem r;
+  r.h = it % p.H;
+  r.c = (it / p.H) % p.nc;
+  r.b = it / (p.H * p.nc);
+  r.g = r.h / (p.H / p.G);
+  r.t0 = r.c * kSsdQ;
+  return r;
+}
+
+// Pass 2. W is built once per item in shared memory; the causal work of a row block grows
+// with its index, so warp (mp, pq) takes row blocks mp and 3 - mp (rows 16 m .. 16 m + 15)
+// and columns pq P/4 .. + P/4 - 1: every warp does the same number of tensor-core operations.
+template <int P, int N, typename TY>
+__global__ void __launch_bounds__(kSsdThreads, 1) ssd_chunk_scan_kernel(const SsdParams p) {
+  using St = SsdScanStage<P, N>;
+  constexpr int S = St::kStages, LN = St::LN, LP = St::LP, LW = St::LW, LQ = St::LQ, NQ = P / 32, Q = kSsdQ;
+  static_assert(NQ % 2 == 0, "two column tiles per ldmatrix");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* Wh = reinterpret_cast<__nv_bfloat16*>(smem_raw + St::kWhl);  // [j][i] high
+  __nv_bfloat16* Wl = Wh + Q * LQ;                                             // [j][i] low
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const int64_t items = p.batch * p.nc * p.H;
+  auto load = [&](int s, int64_t it) {
+    const SsdItem m = ssd_item(p, it);
+    unsigned char* st = smem_raw + s * St::kBytes;
+    const int64_t rv = p.L - m.t0;
+    ssd_stage_rows<N / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kC), LN,
+                          p.C + ((m.b * p.L + m.t0) * p.G + m.g) * N, p.G * N, rv, p.C, tid);
+    ssd_stage_rows<P / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kX), LP,
+                          p.x + ((m.b * p.L + m.t0) * p.H + m.h) * P, p.H * P, rv, p.x, tid);
+    const __nv_bfloat16* Hg = p.ws_H + it * (int64_t)P * N;  // fragment order, copied as is
+    for (int i = tid; i < P * N / 8; i += kSsdThreads) ssd_cp16(st + St::kH + 16 * i, Hg + 8 * i, true);
+    float* CBs = reinterpret_cast<float*>(st + St::kW);
+    const float* CBg = p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * Q;
+    for (int i = tid; i < Q * (Q / 4); i += kSsdThreads) {
+      const int r = i / (Q / 4), k = i % (Q / 4);
+      ssd_cp16(CBs + r * LW + 4 * k, CBg + r * Q + 4 * k, true);
+    }
+    ssd_stage_floats(st, p, it, St::kDt, St::kCs, tid);
+  };
+#pragma unroll
+  for (int k = 0; k < S - 1; ++k) {
+    const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+    if (it < items) load(k, it);
+    ssd_cp_commit();
+  }
+  const int mp = warp & 1, pc0 = (warp >> 1) * (P / 4);
+  const int mrow[2] = {mp, 3 - mp};
+  for (int k = 0;; ++k) {
+    const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+    if (it >= items) break;
+    {
+      const int64_t nx = it + (int64_t)(S - 1) * gridDim.x;
+      if (nx < items) load((k + S - 1) % S, nx);
+      ssd_cp_commit();
+    }
+    const SsdItem m = ssd_item(p, it);
+    const float Dh = p.Dskip ? p.Dskip[m.h] : 0.f;
+    ssd_cp_wait<S - 1>();
+    __syncthreads();
+    const unsigned char* st = smem_raw + (k % S) * St::kBytes;
+    const __nv_bfloat16* Cs = reinterpret_cast<const __nv_bfloat16*>(st + St::kC);  // [t][n]
+    const float* CBs = reinterpret_cast<const float*>(st + St::kW);                 // [j][i] C B^T
+    const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(st + St::kX);  // [t][p]
+    const uint2* Hs = reinterpret_cast<const uint2*>(st + St::kH) + lane;  // fragment order
+    const float* dts = reinterpret_cast<const float*>(st + St::kDt);
+    const float* css = reinterpret_cast<const float*>(st + St::kCs);
+
+    // W_ji = (C B^T)_ji exp(cs_j - cs_i) dt_i for j >= i (else 0), as bf16 high + low
+    for (int e = tid; e < Q * Q / 2; e += kSsdThreads) {
+      const int j = e / (Q / 2), i = 2 * (e % (Q / 2));
+      const float2 cb = *reinterpret_cast<const float2*>(CBs + j * LW + i);
+      const float cj = css[j];
+      const float2 v = make_float2(j >= i ? cb.x * __expf(cj - css[i]) * dts[i] : 0.f,
+                                   j >= i + 1 ? cb.y * __expf(cj - css[i + 1]) * dts[i + 1] : 0.f);
+      uint32_t hi, lo;
+      split_bf16x2(v, hi, lo);
+      *reinterpret_cast<uint32_t*>(Wh + j * LQ + i) = hi;
+      *reinterpret_cast<uint32_t*>(Wl + j * LQ + i) = lo;
+    }
+
+    float acc[2][NQ][4] = {};
+    // C H^T
+#pragma unroll
+    for (int ks = 0; ks < N / 16; ++ks) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        ldsm_x4(a[r], Cs + (mrow[r] * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LN + ks * 16 + (lane >> 4) * 8);
+#pragma unroll
+#pragma unroll
+      for (int nt = 0; nt < NQ; ++nt) {
+        const uint2 hv = Hs[((pc0 / 8 + nt) * (N / 16) + ks) * 32];  // H^T fragment of column tile
+        const uint32_t bb[2] = {hv.x, hv.y};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) mma_16816(acc[r][nt], a[r], bb);
       }
     }
 #pragma unroll
-    for (int k0 = 0; k0 < N; k0 += 16) {
-      uint32_t a[4];
-      frag_a(a, Cs, LN, mt * 16, k0, lane);
+    for (int r = 0; r < 2; ++r) {
+      const float e0 = __expf(css[mrow[r] * 16 + gq]), e1 = __expf(css[mrow[r] * 16 + gq + 8]);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        uint32_t bb[2];
-        frag_b(bb, Hb, LN, nh * (P / 2) + nt * 8, k0, lane);
-        mma_16816(ao[nt], a, bb);
+      for (int nt = 0; nt < NQ; ++nt) {
+        acc[r][nt][0] *= e0;
+        acc[r][nt][1] *= e0;
+        acc[r][nt][2] *= e1;
+        acc[r][nt][3] *= e1;
       }
     }
+    __syncthreads();  // W is complete
+    // W X over the row blocks' causal column blocks
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int j = mt * 16 + gq + 8 * hf;
-      if (j < tc) {
-        const float e = __expf(cs[j]);
-        TY* yrow = static_cast<TY*>(p.y) + ((b * p.L + t0 + j) * p.H + h) * P;
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks > mrow[1] && ks > mrow[0]) continue;
+      uint32_t xb[NQ / 2][4];  // X[t][p] fragments of column tiles (pc0 + 16 np) and (+ 8)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int pc = nh * (P / 2) + nt * 8 + 2 * tq;
-          const float v0 = ad[nt][2 * hf] + e * ao[nt][2 * hf] + Dh * __bfloat162float(XT[pc * LQ + j]);
-          const float v1 = ad[nt][2 * hf + 1] + e * ao[nt][2 * hf + 1] + Dh * __bfloat162float(XT[(pc + 1) * LQ + j]);
-          if (sizeof(TY) == 2)
-            *reinterpret_cast<uint32_t*>(yrow + pc) = pack_bf16(v0, v1);
-          else
-            *reinterpret_cast<float2*>(yrow + pc) = make_float2(v0, v1);
+      for (int np = 0; np < NQ / 2; ++np)
+        ldsm_x4_t(xb[np], Xs + (ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LP + pc0 + np * 16 + (lane >> 4) * 8);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (ks > mrow[r]) continue;
+        uint32_t wh[4], wl[4];
+        const int wo = (mrow[r] * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LQ + ks * 16 + (lane >> 4) * 8;
+        ldsm_x4(wh, Wh + wo);
+        ldsm_x4(wl, Wl + wo);
+#pragma unroll
+        for (int np = 0; np < NQ / 2; ++np) {
+          const uint32_t b0[2] = {xb[np][0], xb[np][1]}, b1[2] = {xb[np][2], xb[np][3]};
+          mma_16816(acc[r][2 * np], wh, b0);
+          mma_16816(acc[r][2 * np + 1], wh, b1);
+        }
+#pragma unroll
+        for (int np = 0; np < NQ / 2; ++np) {
+          const uint32_t b0[2] = {xb[np][0], xb[np][1]}, b1[2] = {xb[np][2], xb[np][3]};
+          mma_16816(acc[r][2 * np], wl, b0);
+          mma_16816(acc[r][2 * np + 1], wl, b1);
         }
       }
     }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int j = mrow[r] * 16 + gq + 8 * hf;
+        if (m.t0 + j < p.L) {
+          TY* yrow = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + j) * p.H + m.h) * P;
+#pragma unroll
+          for (int nt = 0; nt < NQ; ++nt) {
+            const int pc = pc0 + nt * 8 + 2 * tq;
+            const float2 xv = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(Xs + j * LP + pc));
+            const float v0 = fmaf(Dh, xv.x, acc[r][nt][2 * hf]), v1 = fmaf(Dh, xv.y, acc[r][nt][2 * hf + 1]);
+            if (sizeof(TY) == 2)
+              *reinterpret_cast<uint32_t*>(yrow + pc) = pack_bf16(v0, v1);
+            else
+              *reinterpret_cast<float2*>(yrow + pc) = make_float2(v0, v1);
+          }
+        }
+      }
+    __syncthreads();  // this stage and W are refilled next iteration
   }
+  ssd_cp_wait<0>();
 }
 
 }  // namespace ssm

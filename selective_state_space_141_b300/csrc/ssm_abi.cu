@@ -851,42 +851,56 @@ namespace {
 // Workspace of the chunk-parallel SSD schedule: per (b, c, h) the chunk's state
 // contribution (fp32 P x N) and entering state (bf16 P x N), and per (b, h, c) its decay.
 struct SsdPlan {
-  size_t off_S = 0, off_H = 0, off_dec = 0, bytes = 0;
+  size_t off_H = 0, off_dt = 0, off_cs = 0, off_CB = 0, bytes = 0;
 };
-SsdPlan ssd_plan(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+SsdPlan ssd_plan(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t P, int64_t N) {
   SsdPlan pl;
-  if (batch <= 0 || L <= 0 || H <= 0 || P <= 0 || N <= 0) return pl;
-  const size_t nc = (size_t)((L + ssm::kSsdQ - 1) / ssm::kSsdQ), e = (size_t)batch * nc * H * P * N;
+  if (batch <= 0 || L <= 0 || H <= 0 || G <= 0 || P <= 0 || N <= 0) return pl;
+  const size_t nc = (size_t)((L + ssm::kSsdQ - 1) / ssm::kSsdQ), items = (size_t)batch * nc * H;
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
-  pl.off_S = 0;
-  pl.off_H = r256(e * 4);
-  pl.off_dec = pl.off_H + r256(e * 2);
-  pl.bytes = pl.off_dec + r256((size_t)batch * H * nc * 4);
+  pl.off_H = 0;
+  pl.off_dt = r256(items * P * N * 2);
+  pl.off_cs = pl.off_dt + r256(items * ssm::kSsdQ * 4);
+  pl.off_CB = pl.off_cs + r256(items * ssm::kSsdQ * 4);
+  pl.bytes = pl.off_CB + r256((size_t)batch * nc * G * ssm::kSsdQ * ssm::kSsdQ * 4);
   return pl;
+}
+
+// Persistent grid: as many CTAs as fit on the GPU at once, at most one per item.
+unsigned persistent_grid(const void* kern, int smem, int64_t items) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ssm::kSsdThreads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t n = (int64_t)(num_sms() > 0 ? num_sms() : 1) * per_sm;
+  if (n > items) n = items;
+  return (unsigned)(n > 0 ? n : 1);
 }
 
 template <int P, int N>
 cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
   void* args[] = {const_cast<ssm::SsdParams*>(&p)};
-  const dim3 cgrid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.batch);
   {
-    constexpr int smem = ssm::ssd_state_smem_bytes<P, N>();
-    const void* k = reinterpret_cast<const void*>(&ssm::ssd_chunk_state_kernel<P, N>);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = cudaLaunchKernel(k, cgrid, dim3(ssm::kSsdThreads), args, smem, st);
+    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::ssd_prep_kernel<N>),
+                                           dim3((unsigned)p.nc, (unsigned)p.batch), dim3(256), args, 0, st);
     if (e != cudaSuccess) return e;
   }
   {
-    const int64_t n = p.batch * p.H * (int64_t)P * N;
-    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::ssd_state_pass_kernel<P, N>),
-                                           dim3((unsigned)((n + 255) / 256)), dim3(256), args, 0, st);
+    constexpr int smem = ssm::ssd_walk_smem_bytes<P>();
+    const void* k = reinterpret_cast<const void*>(&ssm::ssd_state_walk_kernel<P, N>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaLaunchKernel(k, dim3(N / ssm::kSsdNB, (unsigned)p.H, (unsigned)p.batch), dim3(ssm::kSsdThreads), args,
+                           smem, st);
     if (e != cudaSuccess) return e;
   }
   constexpr int smem = ssm::ssd_scan_smem_bytes<P, N>();
   const void* k = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, float>)
                         : reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, __nv_bfloat16>);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess) e = cudaLaunchKernel(k, cgrid, dim3(ssm::kSsdThreads), args, smem, st);
+  if (e == cudaSuccess)
+    e = cudaLaunchKernel(k, dim3(persistent_grid(k, smem, p.batch * p.nc * p.H)), dim3(ssm::kSsdThreads), args, smem,
+                         st);
   return e;
 }
 
@@ -904,10 +918,11 @@ cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
 
 extern "C" {
 
-ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, size_t* bytes) {
+ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t groups, int64_t P, int64_t N,
+                                        size_t* bytes) {
   if (!bytes) return SSM_ERR_NULL;
-  if (batch < 0 || L < 0 || H < 0 || P < 0 || N < 0) return SSM_ERR_SHAPE;
-  *bytes = ssd_plan(batch, L, H, P, N).bytes;
+  if (batch < 0 || L < 0 || H < 0 || groups < 1 || P < 0 || N < 0) return SSM_ERR_SHAPE;
+  *bytes = ssd_plan(batch, L, H, groups, P, N).bytes;
   return SSM_OK;
 }
 
@@ -948,7 +963,7 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
     if (last_state && overlaps(last_state, in)) return SSM_ERR_LAYOUT;
   }
   if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
-  const SsdPlan plan = ssd_plan(batch, L, H, P, N);
+  const SsdPlan plan = ssd_plan(batch, L, H, groups, P, N);
   const bool chunked = workspace && workspace_bytes >= plan.bytes && plan.bytes > 0 && H <= 65535;
   if (chunked) {
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SSM_ERR_LAYOUT;
@@ -988,14 +1003,16 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
   p.G = groups;
   const bool yf = y->dtype == SSM_F32;
   p.nc = (int)((L + ssm::kSsdQ - 1) / ssm::kSsdQ);
-  p.ws_S = nullptr;
   p.ws_H = nullptr;
-  p.ws_dec = nullptr;
+  p.ws_dt = nullptr;
+  p.ws_cs = nullptr;
+  p.ws_CB = nullptr;
   if (chunked) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    p.ws_S = reinterpret_cast<float*>(ws + plan.off_S);
     p.ws_H = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_H);
-    p.ws_dec = reinterpret_cast<float*>(ws + plan.off_dec);
+    p.ws_dt = reinterpret_cast<float*>(ws + plan.off_dt);
+    p.ws_cs = reinterpret_cast<float*>(ws + plan.off_cs);
+    p.ws_CB = reinterpret_cast<float*>(ws + plan.off_CB);
   }
   cudaError_t e;
   if (P == 64 && N == 64)

@@ -78,7 +78,7 @@ def load_library(path: str | None = None):
     lib.ssm_ssd_fwd.argtypes = [ctypes.c_int64] + [_P] * 7 + [ctypes.c_int, _P, _P, _P, ctypes.c_void_p,
                                                               ctypes.c_size_t, ctypes.c_void_p]
     lib.ssm_ssd_fwd_workspace_size.restype = ctypes.c_int
-    lib.ssm_ssd_fwd_workspace_size.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_ssd_fwd_workspace_size.argtypes = [ctypes.c_int64] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_state_update_ex.restype = ctypes.c_int
     lib.ssm_state_update_ex.argtypes = [_P] * 9 + [ctypes.c_int, ctypes.c_uint32, _P, ctypes.c_void_p]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -225,11 +225,11 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, d
     return {k: v for k, v in g.items() if v is not None}
 
 
-def ssd_workspace_size(batch, L, H, P, N) -> int:
+def ssd_workspace_size(batch, L, H, P, N, groups=1) -> int:
     """Bytes of workspace for the chunk-parallel ``ssm_ssd_fwd`` schedule."""
     lib = load_library()
     n = ctypes.c_size_t(0)
-    st = lib.ssm_ssd_fwd_workspace_size(int(batch), int(L), int(H), int(P), int(N), ctypes.byref(n))
+    st = lib.ssm_ssd_fwd_workspace_size(int(batch), int(L), int(H), int(groups), int(P), int(N), ctypes.byref(n))
     if st != 0:
         raise SsmError(st, "ssm_ssd_fwd_workspace_size")
     return int(n.value)
@@ -246,7 +246,7 @@ def ssd_fwd(x, delta, A, B, C, D=None, dt_bias=None, dt_softplus=True, h0=None, 
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     if workspace is None and use_workspace:
-        nbytes = ssd_workspace_size(b, L, H, P, N)
+        nbytes = ssd_workspace_size(b, L, H, P, N, groups=G)
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     ws_ptr = workspace.data_ptr() if use_workspace and workspace is not None and workspace.numel() > 0 else None

@@ -331,5 +331,10 @@ def test_ssd_validation(lib):
     assert call(G, x_=T((b, L, H * P), addr=x.data + 2)) == 4        # x not 16-byte aligned
     assert call(G, sp=2) == 5
     n = ctypes.c_size_t(0)
-    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 64, 64, ctypes.byref(n)) == 0 and n.value > 0
-    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 64, 64, None) == 1
+    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 2, 64, 64, ctypes.byref(n)) == 0
+    # per (b, c, h): entering state (bf16 P x N) + dt, cs (64 floats each); per (b, c, g): C B^T
+    items, cbs = 2 * 2 * 4, 2 * 2 * 2
+    r256 = lambda v: (v + 255) // 256 * 256
+    assert n.value == r256(items * 64 * 64 * 2) + 2 * r256(items * 64 * 4) + r256(cbs * 64 * 64 * 4)
+    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 0, 64, 64, ctypes.byref(n)) == 2
+    assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 2, 64, 64, None) == 1
