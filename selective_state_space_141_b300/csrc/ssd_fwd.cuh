@@ -338,9 +338,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ssd_fwd_kernel(const SsdParams
 //   is computed.
 // Pass 2 (persistent, item = (b, c, h)): Y = W X + diag(exp(cs)) C H_c^T + D X, with W the
 //   group's C B^T masked to j >= i and decayed by exp(cs_j - cs_i) dt_i for this head.
-//   One CTA of 8 warps per SM walks the items (h fastest, so CTAs working at the same time
-//   share C B^T and C in L2); each item's inputs arrive by cp.async into a 2-stage ring
-//   while the previous item is computed.
+//   Two CTAs of 8 warps per SM walk the items (h fastest, so CTAs working at the same time
+//   share C B^T and C in L2); each CTA copies an item's inputs by cp.async, then computes
+//   it, so one CTA's copies overlap the other's arithmetic.
 // Fragments come from shared memory by ldmatrix (transposed where the contraction runs
 // over time); w B and W reach the tensor cores as bf16 high + low pairs.
 
@@ -421,7 +421,8 @@ template <int P, int N>
 struct SsdScanStage {
   static constexpr int LN = N + kSsdPad, LP = P + kSsdPad, LW = kSsdQ + 4, LQ = kSsdQ + kSsdPad;
   static constexpr int kC = 0, kW = kC + kSsdQ * LN * 2, kX = kW + kSsdQ * LW * 4, kH = kX + kSsdQ * LP * 2;
-  static constexpr int kDt = kH + P * N * 2, kCs = kDt + kSsdQ * 4, kBytes = kCs + kSsdQ * 4, kStages = 2;
+  // one stage: two CTAs per SM overlap one CTA's loads with the other's compute
+  static constexpr int kDt = kH + P * N * 2, kCs = kDt + kSsdQ * 4, kBytes = kCs + kSsdQ * 4, kStages = 1;
   static constexpr int kWhl = kStages * kBytes;  // W high and low parts, [Q][LQ] bf16 each
   static_assert(kBytes % 16 == 0, "stage layout");
 };
@@ -512,6 +513,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_state_walk_kernel(const Ss
   constexpr int Q = kSsdQ, S = St::kStages, LP = St::LP, LB = St::LB, NB = kSsdNB;
   constexpr int MT = P / 16, WPM = 8 / MT, NTW = (NB / 8) / WPM;
   static_assert(MT * WPM == 8 && NTW % 2 == 0, "warp tiling");
+  static_assert(S >= 2, "the ring waits for all but the newest S - 2 groups");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* wBbuf = reinterpret_cast<__nv_bfloat16*>(smem_raw + St::kWB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
@@ -640,7 +642,7 @@ __device__ __forceinline__ SsdItem ssd_item(const SsdParams& p, int64_t it) {
 // with its index, so warp (mp, pq) takes row blocks mp and 3 - mp (rows 16 m .. 16 m + 15)
 // and columns pq P/4 .. + P/4 - 1: every warp does the same number of tensor-core operations.
 template <int P, int N, typename TY>
-__global__ void __launch_bounds__(kSsdThreads, 1) ssd_chunk_scan_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const SsdParams p) {
   using St = SsdScanStage<P, N>;
   constexpr int S = St::kStages, LN = St::LN, LP = St::LP, LW = St::LW, LQ = St::LQ, NQ = P / 32, Q = kSsdQ;
   static_assert(NQ % 2 == 0, "two column tiles per ldmatrix");
