@@ -20,6 +20,8 @@
 #pragma once
 
 #include "common.cuh"
+#include "tma.cuh"
+#include "umma.cuh"
 
 namespace ssm {
 
@@ -622,6 +624,272 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_state_walk_kernel(const Ss
             make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
   }
   ssd_cp_wait<0>();
+}
+
+// Pass 1 on the 5th-generation tensor cores (P = 128). grid (N / 32, H,
+// batch), block 192: warps 0-3 are workers, warp 4's lane 0 issues the MMAs, warp 5's
+// lane 0 issues the copies. Per chunk c:
+//   copier: chunk c by TMA into stage c % 2 once the MMA of chunk c - 2 has released it
+//     (X as two 64 x 64 boxes with the 128-byte swizzle, B as one 32 x 64 box, dt and cs
+//     as bulk copies, all on one mbarrier);
+//   workers: form w B of chunk c (bf16 high + low) in stage c % 2 and signal full; then,
+//     for chunk c - 1, load its MMA result from TMEM (one
+//     state row per thread: warp w has TMEM lanes 32 w .. 32 w + 31), write the entering
+//     state (bf16, fragment order) for the read-out, update the fp32 state registers
+//     S <- exp(cs_end) S + S_c and release the TMEM buffer;
+//   MMA thread: S_c = X^T (w B) as 8 tcgen05.mma (M = 128 state rows, N = 32 state
+//     columns, K = 16 steps; high and low parts of w B) into TMEM buffer c % 2, then
+//     commit to the buffer's full barrier and to the stage's empty barrier.
+// So the MMA of chunk c runs while the workers finish chunk c - 1 and start chunk c + 1.
+// X is an MN-major operand with the 128-byte swizzle (a 128-byte row = 64 state rows of
+// one step; 8 steps per 1 KB atom; the descriptor's LBO is the distance between atoms along
+// M and its SBO the distance between atoms along K; measured on B300 against a host
+// product), so TMA moves 128-byte rows. w B is an MN-major operand without swizzle (16-byte
+// rows of 8 bf16 along the state columns, 8 steps per core matrix). Steps past L in a
+// batch row's last chunk are zeroed (X) or masked (w B) after the copy, so the next row's
+// data never enters. Every wait is bounded; one that runs out raises a CTA-wide abort flag
+// that ends every role's loop.
+constexpr int kTcP = 128;
+constexpr int kTcWorkers = 128;
+constexpr int kTcThreads = kTcWorkers + 64;
+template <int N>
+struct SsdTcWalk {
+  static constexpr int kX = 0;                            // X: [p half][t][64 p] swizzled, 16 KB
+  static constexpr int kB = kX + kSsdQ * kTcP * 2;        // raw B, [t][32 columns], 4 KB
+  static constexpr int kWh = kB + kSsdQ * kSsdNB * 2;     // w B high: 4 x 8 core matrices (n8, t8), 4 KB
+  static constexpr int kWl = kWh + kSsdQ * kSsdNB * 2;    // w B low
+  static constexpr int kDt = kWl + kSsdQ * kSsdNB * 2;    // dt [Q]
+  static constexpr int kCs = kDt + kSsdQ * 4;             // cs [Q]
+  static constexpr int kStage = (kCs + kSsdQ * 4 + 1023) / 1024 * 1024;  // swizzle atoms 1 KB aligned
+  static constexpr int kBar = 2 * kStage;                 // full, empty, tfull, tempty, loaded [2] each
+  static constexpr int kSlot = kBar + 10 * 8;             // TMEM address
+  static constexpr int kAbort = kSlot + 4;
+  static constexpr int kBytes = kAbort + 12 + 1024;       // + room to align the base to 1 KB
+  // operand strides (bytes): X atoms (64 p x 8 t, 1 KB) at p-half * 8192 + t8 * 1024; w B core
+  // matrix (n8, t8) at n8 * 128 + t8 * 512
+  static constexpr uint32_t kXlbo = 8192, kXsbo = 1024, kWlbo = 512, kWsbo = 128;
+};
+
+// Bounded wait on a barrier phase that also gives up once another role has aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - start > kWaitCycles) {
+      atomicCAS(&g_ssm_error, 0, (int)kErrWaitMma);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Barrier over n threads (id bar_id) that also returns the AND of every thread's v.
+__device__ __forceinline__ bool bar_and(bool v, int bar_id, int n) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.and.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(bar_id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <int N>
+__global__ void __launch_bounds__(kTcThreads)
+    ssd_state_walk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                             const SsdParams p) {
+  using L = SsdTcWalk<N>;
+  constexpr int Q = kSsdQ, P = kTcP, NB = kSsdNB;
+  constexpr uint32_t kIdesc = umma_idesc_bf16(P, NB, true, true);
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
+  unsigned char* smem_raw = smem_dyn + ((1024u - (umma_saddr(smem_dyn) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L::kBar);
+  uint64_t* empty = full + 2;
+  uint64_t* tfull = full + 4;
+  uint64_t* tempty = full + 6;
+  uint64_t* loaded = full + 8;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem_raw + L::kSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem_raw + L::kAbort);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb0 = blockIdx.x * NB;
+  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G);
+  const int nc = p.nc;
+  const int64_t item0 = (b * nc) * p.H + h;  // item of chunk c: item0 + c * H
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], kTcWorkers);
+      mbar_init(&empty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kTcWorkers);
+      mbar_init(&loaded[i], 1);
+    }
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_b);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(slot, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  // chunk c into stage s by TMA (X 16 KB, B 4 KB, dt and cs 256 B each)
+  auto load = [&](int s, int c) {
+    unsigned char* st = smem_raw + s * L::kStage;
+    const int32_t row = (int32_t)(b * p.L + (int64_t)c * Q);
+    mbar_arrive_expect_tx(&loaded[s], (uint32_t)(Q * P * 2 + Q * NB * 2 + 2 * Q * 4));
+    tma_load_3d_bar(st + L::kX, &tm_x, 0, (int32_t)h, row, &loaded[s]);
+    tma_load_3d_bar(st + L::kX + L::kXlbo, &tm_x, 64, (int32_t)h, row, &loaded[s]);
+    tma_load_2d(st + L::kB, &tm_b, (int32_t)(g * N + nb0), row, &loaded[s]);
+    const int64_t it = item0 + (int64_t)c * p.H;
+    bulk_load(st + L::kDt, p.ws_dt + it * Q, Q * 4, &loaded[s]);
+    bulk_load(st + L::kCs, p.ws_cs + it * Q, Q * 4, &loaded[s]);
+  };
+
+  if (warp == 5) {  // ---------------- copier ----------------
+    if (lane == 0) {
+      for (int c = 0; c < nc; ++c) {
+        // stage c % 2 last held chunk c - 2: wait until its MMA has read it
+        if (c >= 2 && !tc_wait(&empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1), abort)) break;
+        load(c & 1, c);
+      }
+    }
+  } else if (warp == 4) {  // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      for (int c = 0; c < nc; ++c) {
+        const int s = c & 1;
+        if (!tc_wait(&full[s], (uint32_t)((c >> 1) & 1), abort)) break;
+        if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort)) break;
+        tc_fence_after();
+        const unsigned char* st = smem_raw + s * L::kStage;
+        const uint32_t xa = umma_saddr(st + L::kX), wh = umma_saddr(st + L::kWh), wl = umma_saddr(st + L::kWl);
+        const uint32_t d = tmem + 32u * (uint32_t)s;
+#pragma unroll
+        for (int ks = 0; ks < Q / 16; ++ks) {
+          const uint64_t ad = umma_sdesc(xa + ks * 2 * L::kXsbo, L::kXlbo, L::kXsbo, 2);
+          umma_bf16(d, ad, umma_sdesc(wh + ks * 2 * L::kWlbo, L::kWlbo, L::kWsbo), kIdesc, ks > 0);
+          umma_bf16(d, ad, umma_sdesc(wl + ks * 2 * L::kWlbo, L::kWlbo, L::kWsbo), kIdesc, true);
+        }
+        umma_commit(&tfull[s]);
+        umma_commit(&empty[s]);
+      }
+    }
+  } else {  // ---------------- workers ----------------
+    const int prow = tid;  // this thread's state row (TMEM lane)
+    float S[NB];
+    {
+      const int64_t o = ((b * p.H + h) * P + prow) * N + nb0;
+#pragma unroll
+      for (int j = 0; j < NB; j += 4) {
+        const float4 v = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + o + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[j] = v.x;
+        S[j + 1] = v.y;
+        S[j + 2] = v.z;
+        S[j + 3] = v.w;
+      }
+    }
+    // chunk c's result -> entering state out, state update (dec = exp(cs_end) of chunk c);
+    // releases its TMEM buffer
+    auto epilogue = [&](int c, float dec) {
+      const int s = c & 1;
+      if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort)) return false;
+      tc_fence_after();
+      float Sc[NB];
+      {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 32u * (uint32_t)s, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) Sc[j] = v[j];
+        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 32u * (uint32_t)s + 16u, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) Sc[16 + j] = v[j];
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[s]);
+      // fragment order: this row's 32 columns are, per 16 columns, 4 consecutive
+      // (lane, pair) entries of 8 bytes
+      uint4* Ho = reinterpret_cast<uint4*>(reinterpret_cast<uint2*>(p.ws_H + (item0 + (int64_t)c * p.H) * P * N) +
+                                           ((prow >> 3) * (N / 16) + (nb0 >> 4)) * 32 + (prow & 7) * 4);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float* v = S + 16 * k;
+        uint4* o = Ho + k * 16;  // next column tile of 16: 32 (lane, pair) entries further
+        o[0] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[8], v[9]), pack_bf16(v[2], v[3]), pack_bf16(v[10], v[11]));
+        o[1] = make_uint4(pack_bf16(v[4], v[5]), pack_bf16(v[12], v[13]), pack_bf16(v[6], v[7]), pack_bf16(v[14], v[15]));
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) S[j] = fmaf(dec, S[j], Sc[j]);
+      return true;
+    };
+
+    bool ok = true;        // this thread's waits so far
+    float dec_prev = 0.f;  // exp(cs_end) of chunk c - 1
+    for (int c = 0; c < nc; ++c) {
+      const int s = c & 1;
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((c >> 1) & 1), abort)) ok = false;
+      const int rv = (int)((p.L - (int64_t)c * Q) < Q ? (p.L - (int64_t)c * Q) : Q);
+      if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
+        unsigned char* st = smem_raw + s * L::kStage;
+        for (int i = tid; i < (Q - rv) * (P / 8); i += kTcWorkers) {  // a step's row: 8 chunks per half
+          const int t = rv + i / (P / 8), k = i % (P / 8);
+          *reinterpret_cast<uint4*>(st + L::kX + (k >> 3) * L::kXlbo + t * 128 + (k & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // every worker's view of the stage; the workers leave the loop together if any wait
+      // ran out
+      if (!bar_and(ok, 1, kTcWorkers)) {
+        ok = false;
+        break;
+      }
+      float dec_cur;
+      {  // w B of chunk c (bf16 high + low), thread -> (t, 8 columns) x 2
+        unsigned char* st = smem_raw + s * L::kStage;
+        const float* dts = reinterpret_cast<const float*>(st + L::kDt);
+        const float* css = reinterpret_cast<const float*>(st + L::kCs);
+        const float cs_end = css[Q - 1];
+        dec_cur = __expf(cs_end);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int i = tid + r * kTcWorkers;
+          const int t = (i >> 5) * 8 + (i & 7), n8 = (i >> 3) & 3;
+          const float w = __expf(cs_end - css[t]) * dts[t];
+          const uint4 raw = *reinterpret_cast<const uint4*>(st + L::kB + t * (NB * 2) + n8 * 16);
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 v = bf16x2_to_f2(rw[k]);
+            split_bf16x2(t < rv ? make_float2(v.x * w, v.y * w) : make_float2(0.f, 0.f), hi[k], lo[k]);
+          }
+          const int off = n8 * L::kWsbo + (t >> 3) * L::kWlbo + (t & 7) * 16;
+          *reinterpret_cast<uint4*>(st + L::kWh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(st + L::kWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_smem_to_async();
+      mbar_arrive(&full[s]);
+      if (c >= 1 && !epilogue(c - 1, dec_prev)) ok = false;
+      dec_prev = dec_cur;
+    }
+    if (ok && nc >= 1) ok = epilogue(nc - 1, dec_prev);
+    if (p.last_state && ok) {
+      const int64_t o = ((b * p.H + h) * P + prow) * N + nb0;
+#pragma unroll
+      for (int j = 0; j < NB; j += 4)
+        *reinterpret_cast<float4*>(p.last_state + o + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
 }
 
 // Item (b, c, h) of the persistent read-out pass.

@@ -877,6 +877,39 @@ unsigned persistent_grid(const void* kern, int smem, int64_t items) {
   return (unsigned)(n > 0 ? n : 1);
 }
 
+// Tensor maps of the tcgen05 state walk (P = 128): x as (p, head, batch row x step) with
+// 64 x 64 boxes and the 128-byte swizzle (the MMA's operand layout); B as (group column,
+// batch row x step) with 32 x 64 boxes.
+template <int N>
+bool ssd_walk_maps(const ssm::SsdParams& p, CUtensorMap* tm) {
+  auto fn = encode_fn();
+  constexpr uint64_t P = ssm::kTcP;
+  if (!fn || (uint64_t)(p.batch * p.L) >= (1ull << 31)) return false;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t H = (uint64_t)p.H, G = (uint64_t)p.G, rows = (uint64_t)(p.batch * p.L);
+  {
+    cuuint64_t dims[3] = {P, H, rows};
+    cuuint64_t strides[2] = {P * 2, H * P * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)ssm::kSsdQ};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&tm[0], bf, 3, const_cast<void*>(static_cast<const void*>(p.x)), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    cuuint64_t dims[2] = {G * N, rows};
+    cuuint64_t strides[1] = {G * N * 2};
+    cuuint32_t box[2] = {(cuuint32_t)ssm::kSsdNB, (cuuint32_t)ssm::kSsdQ};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&tm[1], bf, 2, const_cast<void*>(static_cast<const void*>(p.B)), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 template <int P, int N>
 cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
   void* args[] = {const_cast<ssm::SsdParams*>(&p)};
@@ -885,7 +918,17 @@ cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t
                                            dim3((unsigned)p.nc, (unsigned)p.batch), dim3(256), args, 0, st);
     if (e != cudaSuccess) return e;
   }
-  {
+  CUtensorMap tm[2];
+  if (P == ssm::kTcP && ssd_walk_maps<N>(p, tm)) {  // the state walk on tcgen05, operands by TMA
+    constexpr int smem = ssm::SsdTcWalk<N>::kBytes;
+    const void* k = reinterpret_cast<const void*>(&ssm::ssd_state_walk_tc_kernel<N>);
+    void* targs[] = {&tm[0], &tm[1], const_cast<ssm::SsdParams*>(&p)};
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaLaunchKernel(k, dim3(N / ssm::kSsdNB, (unsigned)p.H, (unsigned)p.batch), dim3(ssm::kTcThreads), targs,
+                           smem, st);
+    if (e != cudaSuccess) return e;
+  } else {
     constexpr int smem = ssm::ssd_walk_smem_bytes<P>();
     const void* k = reinterpret_cast<const void*>(&ssm::ssd_state_walk_kernel<P, N>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -1,0 +1,89 @@
+// umma.cuh -- tcgen05 (5th-generation tensor core) helpers in inline PTX, sm_103a.
+//
+// Operands come from shared memory through 64-bit matrix descriptors, the accumulator
+// lives in tensor memory (TMEM), one thread issues the MMA and tcgen05.commit signals an
+// mbarrier when it has completed. Without swizzle an operand is a grid of "core matrices"
+// of 8 rows x 16 bytes (128 contiguous bytes, rows 16 bytes apart). For a K-major operand
+// a row runs along K (8 bf16 of one M/N index); for an MN-major operand a row runs along
+// M/N (8 bf16 of one K index). In both cases the descriptor's leading byte offset (LBO) is
+// the distance between core matrices adjacent along K, and its stride byte offset (SBO) the
+// distance between core matrices adjacent along M/N (measured on B300 with single MMAs
+// against a host product, every element exact). The 128-byte swizzle is described at
+// umma_sdesc.
+#pragma once
+
+#include <stdint.h>
+
+namespace ssm {
+
+__device__ __forceinline__ uint32_t umma_saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor: start address, LBO, SBO (bytes, multiples of 16, below
+// 256 KB), descriptor version 1, base offset 0, layout type (0: no swizzle, 2: 128-byte
+// swizzle with 1 KB atoms, which must start 1 KB aligned). With the 128-byte swizzle an
+// MN-major operand is made of atoms of 8 K-rows x 128 bytes (64 elements along M/N), the
+// 16-byte chunk c of row r stored at chunk c ^ r; there LBO is the distance between atoms
+// along M/N and SBO the distance between atoms along K (the reverse of the no-swizzle
+// roles; measured on B300 against a host product).
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation, M x N tile;
+// a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) = A B (+ D when accumulate), issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+
+// Arrive once on bar when every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(umma_saddr(bar))
+               : "memory");
+}
+
+// Warp-wide: allocate ncols TMEM columns (power of two, >= 32), address written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(umma_saddr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy shared-memory writes (stores, cp.async) -> visible to the tensor core.
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Warp-wide: 16 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the warp
+// gets row (lane quarter) * 32 + i); then wait for the load.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace ssm
