@@ -419,22 +419,9 @@ struct SsdWalkStage {
   static constexpr int kWB = kStages * kBytes;  // (w B) high and low, two buffers: [2][2][Q][LB] bf16
   static_assert(kBytes % 16 == 0, "stage layout");
 };
-template <int P, int N>
-struct SsdScanStage {
-  static constexpr int LN = N + kSsdPad, LP = P + kSsdPad, LW = kSsdQ + 4, LQ = kSsdQ + kSsdPad;
-  static constexpr int kC = 0, kW = kC + kSsdQ * LN * 2, kX = kW + kSsdQ * LW * 4, kH = kX + kSsdQ * LP * 2;
-  // one stage: two CTAs per SM overlap one CTA's loads with the other's compute
-  static constexpr int kDt = kH + P * N * 2, kCs = kDt + kSsdQ * 4, kBytes = kCs + kSsdQ * 4, kStages = 1;
-  static constexpr int kWhl = kStages * kBytes;  // W high and low parts, [Q][LQ] bf16 each
-  static_assert(kBytes % 16 == 0, "stage layout");
-};
 template <int P>
 constexpr int ssd_walk_smem_bytes() {
   return SsdWalkStage<P>::kWB + 4 * kSsdQ * SsdWalkStage<P>::LB * 2;
-}
-template <int P, int N>
-constexpr int ssd_scan_smem_bytes() {
-  return SsdScanStage<P, N>::kWhl + 2 * kSsdQ * SsdScanStage<P, N>::LQ * 2;
 }
 
 // Pass 0. grid (nc, batch), block 256. (a) warp w takes heads w, w + 8, ...; lane l steps
@@ -906,69 +893,98 @@ __device__ __forceinline__ SsdItem ssd_item(const SsdParams& p, int64_t it) {
   return r;
 }
 
-// Pass 2. W is built once per item in shared memory; the causal work of a row block grows
-// with its index, so warp (mp, pq) takes row blocks mp and 3 - mp (rows 16 m .. 16 m + 15)
-// and columns pq P/4 .. + P/4 - 1: every warp does the same number of tensor-core operations.
+// Pass 2. Per item the inputs arrive by TMA and bulk copies on one mbarrier (one thread
+// issues them): X and C as 64 x 64 boxes with the 128-byte swizzle (rows of 128 bytes; the
+// 16-byte chunk c of row r at chunk c ^ (r % 8), so that ldmatrix reads them without bank
+// conflicts), the entering state, C B^T, dt and cs as contiguous copies. W is built once
+// per item in shared memory; the causal work of a row block grows with its index, so warp
+// (mp, pq) takes row blocks mp and 3 - mp (rows 16 m .. 16 m + 15) and columns pq P/4 ..
+// + P/4 - 1: every warp does the same number of tensor-core operations. Two CTAs per SM:
+// one CTA's copies overlap the other's arithmetic.
+template <int P, int N>
+struct SsdScanSmem {
+  static constexpr int LQ = kSsdQ + kSsdPad;
+  static constexpr int kX = 0;                         // X: P / 64 halves of [Q][128 B], swizzled
+  static constexpr int kC = kX + kSsdQ * P * 2;         // C: N / 64 halves, swizzled
+  static constexpr int kH = kC + kSsdQ * N * 2;         // entering state, fragment order
+  static constexpr int kCB = kH + P * N * 2;            // C B^T, [Q][Q] fp32
+  static constexpr int kDt = kCB + kSsdQ * kSsdQ * 4;
+  static constexpr int kCs = kDt + kSsdQ * 4;
+  static constexpr int kW = kCs + kSsdQ * 4;            // W high, W low: [Q][LQ] bf16 each
+  static constexpr int kBar = kW + 2 * kSsdQ * LQ * 2;
+  static constexpr int kBytes = kBar + 16 + 1024;       // + room to align the base to 1 KB
+  static constexpr uint32_t kTx = kSsdQ * P * 2 + kSsdQ * N * 2 + P * N * 2 + kSsdQ * kSsdQ * 4 + 2 * kSsdQ * 4;
+  static_assert(kC % 1024 == 0 && kH % 1024 == 0, "swizzled boxes start 1 KB aligned");
+};
+template <int P, int N>
+constexpr int ssd_scan_smem_bytes() {
+  return SsdScanSmem<P, N>::kBytes;
+}
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled [rows][128 B] tile
+__device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
 template <int P, int N, typename TY>
-__global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const SsdParams p) {
-  using St = SsdScanStage<P, N>;
-  constexpr int S = St::kStages, LN = St::LN, LP = St::LP, LW = St::LW, LQ = St::LQ, NQ = P / 32, Q = kSsdQ;
+__global__ void __launch_bounds__(kSsdThreads, 2)
+    ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
+                          const SsdParams p) {
+  using Sm = SsdScanSmem<P, N>;
+  constexpr int LQ = Sm::LQ, NQ = P / 32, Q = kSsdQ;
   static_assert(NQ % 2 == 0, "two column tiles per ldmatrix");
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* Wh = reinterpret_cast<__nv_bfloat16*>(smem_raw + St::kWhl);  // [j][i] high
-  __nv_bfloat16* Wl = Wh + Q * LQ;                                             // [j][i] low
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
+  unsigned char* sm = smem_dyn + ((1024u - (umma_saddr(smem_dyn) & 1023u)) & 1023u);
+  __nv_bfloat16* Wh = reinterpret_cast<__nv_bfloat16*>(sm + Sm::kW);  // [j][i] high
+  __nv_bfloat16* Wl = Wh + Q * LQ;                                    // [j][i] low
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Sm::kBar);
+  const unsigned char* Xs = sm + Sm::kX;
+  const unsigned char* Cs = sm + Sm::kC;
+  const uint2* Hs = reinterpret_cast<const uint2*>(sm + Sm::kH);  // fragment order
+  const float* CBs = reinterpret_cast<const float*>(sm + Sm::kCB);
+  const float* dts = reinterpret_cast<const float*>(sm + Sm::kDt);
+  const float* css = reinterpret_cast<const float*>(sm + Sm::kCs);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int64_t items = p.batch * p.nc * p.H;
-  auto load = [&](int s, int64_t it) {
-    const SsdItem m = ssd_item(p, it);
-    unsigned char* st = smem_raw + s * St::kBytes;
-    const int64_t rv = p.L - m.t0;
-    ssd_stage_rows<N / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kC), LN,
-                          p.C + ((m.b * p.L + m.t0) * p.G + m.g) * N, p.G * N, rv, p.C, tid);
-    ssd_stage_rows<P / 8>(reinterpret_cast<__nv_bfloat16*>(st + St::kX), LP,
-                          p.x + ((m.b * p.L + m.t0) * p.H + m.h) * P, p.H * P, rv, p.x, tid);
-    const __nv_bfloat16* Hg = p.ws_H + it * (int64_t)P * N;  // fragment order, copied as is
-    for (int i = tid; i < P * N / 8; i += kSsdThreads) ssd_cp16(st + St::kH + 16 * i, Hg + 8 * i, true);
-    float* CBs = reinterpret_cast<float*>(st + St::kW);
-    const float* CBg = p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * Q;
-    for (int i = tid; i < Q * (Q / 4); i += kSsdThreads) {
-      const int r = i / (Q / 4), k = i % (Q / 4);
-      ssd_cp16(CBs + r * LW + 4 * k, CBg + r * Q + 4 * k, true);
-    }
-    ssd_stage_floats(st, p, it, St::kDt, St::kCs, tid);
-  };
-#pragma unroll
-  for (int k = 0; k < S - 1; ++k) {
-    const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
-    if (it < items) load(k, it);
-    ssd_cp_commit();
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_c);
+    mbar_fence_init();
   }
+  __syncthreads();
   const int mp = warp & 1, pc0 = (warp >> 1) * (P / 4);
   const int mrow[2] = {mp, 3 - mp};
+  bool ok = true;
   for (int k = 0;; ++k) {
     const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
     if (it >= items) break;
-    {
-      const int64_t nx = it + (int64_t)(S - 1) * gridDim.x;
-      if (nx < items) load((k + S - 1) % S, nx);
-      ssd_cp_commit();
-    }
     const SsdItem m = ssd_item(p, it);
+    if (tid == 0) {
+      const int32_t row = (int32_t)(m.b * p.L + m.t0);
+      mbar_arrive_expect_tx(bar, Sm::kTx);
+#pragma unroll
+      for (int hx = 0; hx < P / 64; ++hx) tma_load_3d_bar(sm + Sm::kX + hx * 8192, &tm_x, 64 * hx, (int32_t)m.h, row, bar);
+#pragma unroll
+      for (int hc = 0; hc < N / 64; ++hc)
+        tma_load_2d(sm + Sm::kC + hc * 8192, &tm_c, (int32_t)(m.g * N + 64 * hc), row, bar);
+      bulk_load(sm + Sm::kH, p.ws_H + it * (int64_t)P * N, P * N * 2, bar);
+      bulk_load(sm + Sm::kCB, p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * Q, Q * Q * 4, bar);
+      bulk_load(sm + Sm::kDt, p.ws_dt + it * Q, Q * 4, bar);
+      bulk_load(sm + Sm::kCs, p.ws_cs + it * Q, Q * 4, bar);
+    }
     const float Dh = p.Dskip ? p.Dskip[m.h] : 0.f;
-    ssd_cp_wait<S - 1>();
-    __syncthreads();
-    const unsigned char* st = smem_raw + (k % S) * St::kBytes;
-    const __nv_bfloat16* Cs = reinterpret_cast<const __nv_bfloat16*>(st + St::kC);  // [t][n]
-    const float* CBs = reinterpret_cast<const float*>(st + St::kW);                 // [j][i] C B^T
-    const __nv_bfloat16* Xs = reinterpret_cast<const __nv_bfloat16*>(st + St::kX);  // [t][p]
-    const uint2* Hs = reinterpret_cast<const uint2*>(st + St::kH) + lane;  // fragment order
-    const float* dts = reinterpret_cast<const float*>(st + St::kDt);
-    const float* css = reinterpret_cast<const float*>(st + St::kCs);
+    if (ok && !mbar_wait(bar, (uint32_t)(k & 1), kErrWaitFull)) ok = false;
+    const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
+    if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
+      for (int i = tid; i < (Q - rv) * (P / 8); i += kSsdThreads) {
+        const int t = rv + i / (P / 8), c = i % (P / 8);
+        *reinterpret_cast<uint4*>(sm + Sm::kX + (c >> 3) * 8192 + t * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (!__syncthreads_and(ok)) break;  // a copy that never landed stops every thread
 
     // W_ji = (C B^T)_ji exp(cs_j - cs_i) dt_i for j >= i (else 0), as bf16 high + low
     for (int e = tid; e < Q * Q / 2; e += kSsdThreads) {
       const int j = e / (Q / 2), i = 2 * (e % (Q / 2));
-      const float2 cb = *reinterpret_cast<const float2*>(CBs + j * LW + i);
+      const float2 cb = *reinterpret_cast<const float2*>(CBs + j * Q + i);
       const float cj = css[j];
       const float2 v = make_float2(j >= i ? cb.x * __expf(cj - css[i]) * dts[i] : 0.f,
                                    j >= i + 1 ? cb.y * __expf(cj - css[i + 1]) * dts[i + 1] : 0.f);
@@ -983,13 +999,15 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const Ss
 #pragma unroll
     for (int ks = 0; ks < N / 16; ++ks) {
       uint32_t a[2][4];
+      const int kc = 2 * ks + (lane >> 4);  // 16-byte chunk along n
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
-        ldsm_x4(a[r], Cs + (mrow[r] * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LN + ks * 16 + (lane >> 4) * 8);
-#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = mrow[r] * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        ldsm_x4(a[r], reinterpret_cast<const __nv_bfloat16*>(Cs + (kc >> 3) * 8192 + sw128(row, kc & 7)));
+      }
 #pragma unroll
       for (int nt = 0; nt < NQ; ++nt) {
-        const uint2 hv = Hs[((pc0 / 8 + nt) * (N / 16) + ks) * 32];  // H^T fragment of column tile
+        const uint2 hv = Hs[((pc0 / 8 + nt) * (N / 16) + ks) * 32 + lane];  // H^T fragment of column tile
         const uint32_t bb[2] = {hv.x, hv.y};
 #pragma unroll
         for (int r = 0; r < 2; ++r) mma_16816(acc[r][nt], a[r], bb);
@@ -1012,9 +1030,12 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const Ss
     for (int ks = 0; ks < 4; ++ks) {
       if (ks > mrow[1] && ks > mrow[0]) continue;
       uint32_t xb[NQ / 2][4];  // X[t][p] fragments of column tiles (pc0 + 16 np) and (+ 8)
+      const int t = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int np = 0; np < NQ / 2; ++np)
-        ldsm_x4_t(xb[np], Xs + (ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LP + pc0 + np * 16 + (lane >> 4) * 8);
+      for (int np = 0; np < NQ / 2; ++np) {
+        const int pc = (pc0 + np * 16) / 8 + (lane >> 4);  // 16-byte chunk along p
+        ldsm_x4_t(xb[np], reinterpret_cast<const __nv_bfloat16*>(Xs + (pc >> 3) * 8192 + sw128(t, pc & 7)));
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         if (ks > mrow[r]) continue;
@@ -1041,12 +1062,13 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const Ss
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int j = mrow[r] * 16 + gq + 8 * hf;
-        if (m.t0 + j < p.L) {
+        if (j < rv) {
           TY* yrow = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + j) * p.H + m.h) * P;
 #pragma unroll
           for (int nt = 0; nt < NQ; ++nt) {
             const int pc = pc0 + nt * 8 + 2 * tq;
-            const float2 xv = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(Xs + j * LP + pc));
+            const float2 xv = bf16x2_to_f2(
+                *reinterpret_cast<const uint32_t*>(Xs + (pc >> 6) * 8192 + sw128(j, (pc >> 3) & 7) + (pc & 7) * 2));
             const float v0 = fmaf(Dh, xv.x, acc[r][nt][2 * hf]), v1 = fmaf(Dh, xv.y, acc[r][nt][2 * hf + 1]);
             if (sizeof(TY) == 2)
               *reinterpret_cast<uint32_t*>(yrow + pc) = pack_bf16(v0, v1);
@@ -1055,9 +1077,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_chunk_scan_kernel(const Ss
           }
         }
       }
-    __syncthreads();  // this stage and W are refilled next iteration
+    fence_smem_to_async();  // this thread's stores into the stage come before the next copies
+    __syncthreads();        // the copies of the next item may overwrite every buffer
   }
-  ssd_cp_wait<0>();
 }
 
 }  // namespace ssm

@@ -877,32 +877,50 @@ unsigned persistent_grid(const void* kern, int smem, int64_t items) {
   return (unsigned)(n > 0 ? n : 1);
 }
 
-// Tensor maps of the tcgen05 state walk (P = 128): x as (p, head, batch row x step) with
-// 64 x 64 boxes and the 128-byte swizzle (the MMA's operand layout); B as (group column,
-// batch row x step) with 32 x 64 boxes.
-template <int N>
-bool ssd_walk_maps(const ssm::SsdParams& p, CUtensorMap* tm) {
+template <int P, int N>
+cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
+  constexpr int smem = ssm::ssd_smem_bytes<P, N>();
+  const void* kern = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, float>)
+                           : reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, __nv_bfloat16>);
+  const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  void* args[] = {const_cast<ssm::SsdParams*>(&p)};
+  return cudaLaunchKernel(kern, dim3((unsigned)p.H, (unsigned)p.batch), dim3(ssm::kSsdThreads), args, smem, st);
+}
+
+// Tensor maps of the chunk-parallel schedule: x as (p, head, batch row x step) and C as
+// (group column, batch row x step), both in 64 x 64 boxes with the 128-byte swizzle (the
+// read-out's ldmatrix layout and the tcgen05 walk's X operand); B as (group column, batch
+// row x step) in 32 x 64 boxes (the walk's raw B).
+bool ssd_maps(const ssm::SsdParams& p, int64_t P, int64_t N, CUtensorMap* tm_x, CUtensorMap* tm_c, CUtensorMap* tm_b) {
   auto fn = encode_fn();
-  constexpr uint64_t P = ssm::kTcP;
   if (!fn || (uint64_t)(p.batch * p.L) >= (1ull << 31)) return false;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t H = (uint64_t)p.H, G = (uint64_t)p.G, rows = (uint64_t)(p.batch * p.L);
+  const uint64_t H = (uint64_t)p.H, GN = (uint64_t)(p.G * N), rows = (uint64_t)(p.batch * p.L);
+  const cuuint32_t Q = (cuuint32_t)ssm::kSsdQ;
   {
-    cuuint64_t dims[3] = {P, H, rows};
-    cuuint64_t strides[2] = {P * 2, H * P * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)ssm::kSsdQ};
+    cuuint64_t dims[3] = {(uint64_t)P, H, rows};
+    cuuint64_t strides[2] = {(uint64_t)P * 2, H * P * 2};
+    cuuint32_t box[3] = {64, 1, Q};
     cuuint32_t estr[3] = {1, 1, 1};
-    if (fn(&tm[0], bf, 3, const_cast<void*>(static_cast<const void*>(p.x)), dims, strides, box, estr,
+    if (fn(tm_x, bf, 3, const_cast<void*>(static_cast<const void*>(p.x)), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  cuuint64_t dims[2] = {GN, rows};
+  cuuint64_t strides[1] = {GN * 2};
+  cuuint32_t estr[2] = {1, 1};
+  {
+    cuuint32_t box[2] = {64, Q};
+    if (fn(tm_c, bf, 2, const_cast<void*>(static_cast<const void*>(p.C)), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
   {
-    cuuint64_t dims[2] = {G * N, rows};
-    cuuint64_t strides[1] = {G * N * 2};
-    cuuint32_t box[2] = {(cuuint32_t)ssm::kSsdNB, (cuuint32_t)ssm::kSsdQ};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&tm[1], bf, 2, const_cast<void*>(static_cast<const void*>(p.B)), dims, strides, box, estr,
+    cuuint32_t box[2] = {(cuuint32_t)ssm::kSsdNB, Q};
+    if (fn(tm_b, bf, 2, const_cast<void*>(static_cast<const void*>(p.B)), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
@@ -918,11 +936,12 @@ cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t
                                            dim3((unsigned)p.nc, (unsigned)p.batch), dim3(256), args, 0, st);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap tm[2];
-  if (P == ssm::kTcP && ssd_walk_maps<N>(p, tm)) {  // the state walk on tcgen05, operands by TMA
+  CUtensorMap tm_x, tm_c, tm_b;
+  if (!ssd_maps(p, P, N, &tm_x, &tm_c, &tm_b)) return launch_ssd<P, N>(p, y_f32, st);  // no TMA: one CTA per head
+  if (P == ssm::kTcP) {  // the state walk on tcgen05, operands by TMA
     constexpr int smem = ssm::SsdTcWalk<N>::kBytes;
     const void* k = reinterpret_cast<const void*>(&ssm::ssd_state_walk_tc_kernel<N>);
-    void* targs[] = {&tm[0], &tm[1], const_cast<ssm::SsdParams*>(&p)};
+    void* targs[] = {&tm_x, &tm_b, const_cast<ssm::SsdParams*>(&p)};
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       e = cudaLaunchKernel(k, dim3(N / ssm::kSsdNB, (unsigned)p.H, (unsigned)p.batch), dim3(ssm::kTcThreads), targs,
@@ -940,23 +959,14 @@ cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t
   constexpr int smem = ssm::ssd_scan_smem_bytes<P, N>();
   const void* k = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, float>)
                         : reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, __nv_bfloat16>);
+  void* sargs[] = {&tm_x, &tm_c, const_cast<ssm::SsdParams*>(&p)};
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
-    e = cudaLaunchKernel(k, dim3(persistent_grid(k, smem, p.batch * p.nc * p.H)), dim3(ssm::kSsdThreads), args, smem,
-                         st);
+    e = cudaLaunchKernel(k, dim3(persistent_grid(k, smem, p.batch * p.nc * p.H)), dim3(ssm::kSsdThreads), sargs,
+                         smem, st);
   return e;
 }
 
-template <int P, int N>
-cudaError_t launch_ssd(const ssm::SsdParams& p, bool y_f32, cudaStream_t st) {
-  constexpr int smem = ssm::ssd_smem_bytes<P, N>();
-  const void* kern = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, float>)
-                           : reinterpret_cast<const void*>(&ssm::ssd_fwd_kernel<P, N, __nv_bfloat16>);
-  const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (attr != cudaSuccess) return attr;
-  void* args[] = {const_cast<ssm::SsdParams*>(&p)};
-  return cudaLaunchKernel(kern, dim3((unsigned)p.H, (unsigned)p.batch), dim3(ssm::kSsdThreads), args, smem, st);
-}
 }  // namespace
 
 extern "C" {
