@@ -83,3 +83,20 @@ def test_ssd_workload_sampled_heads():
         yr, lr = ref(sub)
         check(y[bi:bi + 1, :, h:h + 1], yr, TOL_BF16, False, f"y b={bi} h={h}")
         check(last[bi:bi + 1, h:h + 1], lr, TOL_BF16, False, f"last_state b={bi} h={h}")
+
+
+@pytest.mark.parametrize("shape", [(2, 70, 2, 128, 128, 1), (3, 77, 2, 128, 64, 2), (2, 70, 2, 64, 64, 1)])
+def test_ssd_ragged_chunk_ignores_next_row(shape):
+    """A batch row's last chunk is ragged; its copies reach into the next row (or past the
+    tensor). Filling the next row with inf must not change this row's outputs."""
+    b, L, H, P, N, G = shape
+    d = case(b, L, H, P, N, G, seed=105 + L)
+    inf = torch.tensor(float("inf"), dtype=torch.bfloat16, device=DEV)
+    for k in ("x", "B", "C", "delta"):
+        d[k][1:] = inf
+    y, last = gpu(d, y_dtype=torch.float32)
+    sub = {k: (v[:1] if k in ("x", "delta", "B", "C") else v) for k, v in d.items()}
+    yr, lr = ref(sub)
+    check(y[:1], yr, TOL_BF16, False, "y of row 0")
+    check(last[:1], lr, TOL_BF16, False, "last_state of row 0")
+    assert np.isfinite(y[:1].double().cpu().numpy()).all()
