@@ -401,7 +401,8 @@ SSM_API ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ss
 /* Bytes of workspace for the chunk-parallel ssm_ssd_fwd schedule (0 for an empty problem):
  * batch x ceil(L/64) x H x (P x N x 2 + 512) bytes (per chunk and head: the entering state
  * in bf16, the step sizes and decay exponents in fp32) plus batch x ceil(L/64) x groups x
- * 16 KiB (C B^T of each chunk and group), each part rounded up to 256 bytes.
+ * 18 KiB (C B^T of each chunk and group, rows padded to 72 floats), each part rounded up to
+ * 256 bytes.
  * SSM_ERR_NULL / SSM_ERR_SHAPE (negative sizes, groups < 1). */
 SSM_API ssm_status_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t groups, int64_t P,
                                                 int64_t N, size_t* bytes);

@@ -39,10 +39,12 @@ struct SsdParams {
   float* last_state;           // (batch, H, P, N), nullable
   int64_t batch, L, H, G;
   // chunk-parallel schedule (workspace): per (b, c, h) the state entering the chunk
-  // (bf16 P x N in tensor-core fragment order: [P/8][N/16][32 lanes][2] pairs, the pair
-  // (row 8 j + lane / 4, columns 16 k + 2 (lane % 4) (+ 1)) and the same 8 columns on), its
-  // step sizes dt and cumulative decay exponents cs (fp32, Q each); per (b, c, g) C B^T of
-  // the chunk (fp32, Q x Q)
+  // (bf16 P x N; for P = 128 a K-major tensor-core operand image: 8 x 8 core matrices
+  // (p / 8, n / 8) of 8 rows p x 16 bytes, (p8, n8) at p8 (N / 8) 128 + n8 128 bytes; for
+  // P = 64 mma.sync fragment order: [P/8][N/16][32 lanes][2] pairs, the pair (row 8 j +
+  // lane / 4, columns 16 k + 2 (lane % 4) (+ 1)) and the same 8 columns on), its step sizes
+  // dt and cumulative decay exponents cs (fp32, Q each); per (b, c, g) C B^T of the chunk
+  // (fp32, Q rows of kSsdCBPitch)
   __nv_bfloat16* ws_H;
   float* ws_dt;
   float* ws_cs;
@@ -51,6 +53,7 @@ struct SsdParams {
 };
 
 constexpr int kSsdQ = 64;
+constexpr int kSsdCBPitch = kSsdQ + 8;  // floats per row of C B^T in the workspace (bank-spread reads)
 constexpr int kSsdThreads = 256;
 constexpr int kSsdPad = 8;  // bf16 elements of row padding: conflict-free fragment loads
 
@@ -482,12 +485,12 @@ __global__ void __launch_bounds__(256) ssd_prep_kernel(const SsdParams p) {
         mma_16816(acc[2 * np + 1], a, b1);
       }
     }
-    float* CB = p.ws_CB + ((b * p.nc + c) * p.G + g) * Q * Q;
+    float* CB = p.ws_CB + ((b * p.nc + c) * p.G + g) * Q * kSsdCBPitch;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2*>(CB + (mt * 16 + gq + 8 * hf) * Q + n0 + nt * 8 + 2 * tq) =
+        *reinterpret_cast<float2*>(CB + (mt * 16 + gq + 8 * hf) * kSsdCBPitch + n0 + nt * 8 + 2 * tq) =
             make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
   }
 }
@@ -797,16 +800,15 @@ __global__ void __launch_bounds__(kTcThreads)
       }
       tc_fence_before();
       mbar_arrive(&tempty[s]);
-      // fragment order: this row's 32 columns are, per 16 columns, 4 consecutive
-      // (lane, pair) entries of 8 bytes
-      uint4* Ho = reinterpret_cast<uint4*>(reinterpret_cast<uint2*>(p.ws_H + (item0 + (int64_t)c * p.H) * P * N) +
-                                           ((prow >> 3) * (N / 16) + (nb0 >> 4)) * 32 + (prow & 7) * 4);
+      // K-major operand image for the read-out: this row's 32 columns are 4 core-matrix
+      // rows of 16 bytes, (p8, n8) at p8 (N / 8) 128 + n8 128 + (p % 8) 16 bytes
+      unsigned char* Ho = reinterpret_cast<unsigned char*>(p.ws_H + (item0 + (int64_t)c * p.H) * P * N) +
+                          (prow >> 3) * (N / 8) * 128 + (nb0 >> 3) * 128 + (prow & 7) * 16;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float* v = S + 16 * k;
-        uint4* o = Ho + k * 16;  // next column tile of 16: 32 (lane, pair) entries further
-        o[0] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[8], v[9]), pack_bf16(v[2], v[3]), pack_bf16(v[10], v[11]));
-        o[1] = make_uint4(pack_bf16(v[4], v[5]), pack_bf16(v[12], v[13]), pack_bf16(v[6], v[7]), pack_bf16(v[14], v[15]));
+      for (int q = 0; q < NB / 8; ++q) {
+        const float* v = S + 8 * q;
+        *reinterpret_cast<uint4*>(Ho + q * 128) =
+            make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
       }
 #pragma unroll
       for (int j = 0; j < NB; ++j) S[j] = fmaf(dec, S[j], Sc[j]);
@@ -908,12 +910,12 @@ struct SsdScanSmem {
   static constexpr int kC = kX + kSsdQ * P * 2;         // C: N / 64 halves, swizzled
   static constexpr int kH = kC + kSsdQ * N * 2;         // entering state, fragment order
   static constexpr int kCB = kH + P * N * 2;            // C B^T, [Q][Q] fp32
-  static constexpr int kDt = kCB + kSsdQ * kSsdQ * 4;
+  static constexpr int kDt = kCB + kSsdQ * kSsdCBPitch * 4;
   static constexpr int kCs = kDt + kSsdQ * 4;
   static constexpr int kW = kCs + kSsdQ * 4;            // W high, W low: [Q][LQ] bf16 each
   static constexpr int kBar = kW + 2 * kSsdQ * LQ * 2;
   static constexpr int kBytes = kBar + 16 + 1024;       // + room to align the base to 1 KB
-  static constexpr uint32_t kTx = kSsdQ * P * 2 + kSsdQ * N * 2 + P * N * 2 + kSsdQ * kSsdQ * 4 + 2 * kSsdQ * 4;
+  static constexpr uint32_t kTx = kSsdQ * P * 2 + kSsdQ * N * 2 + P * N * 2 + kSsdQ * kSsdCBPitch * 4 + 2 * kSsdQ * 4;
   static_assert(kC % 1024 == 0 && kH % 1024 == 0, "swizzled boxes start 1 KB aligned");
 };
 template <int P, int N>
@@ -966,7 +968,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
       for (int hc = 0; hc < N / 64; ++hc)
         tma_load_2d(sm + Sm::kC + hc * 8192, &tm_c, (int32_t)(m.g * N + 64 * hc), row, bar);
       bulk_load(sm + Sm::kH, p.ws_H + it * (int64_t)P * N, P * N * 2, bar);
-      bulk_load(sm + Sm::kCB, p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * Q, Q * Q * 4, bar);
+      bulk_load(sm + Sm::kCB, p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * kSsdCBPitch, Q * kSsdCBPitch * 4, bar);
       bulk_load(sm + Sm::kDt, p.ws_dt + it * Q, Q * 4, bar);
       bulk_load(sm + Sm::kCs, p.ws_cs + it * Q, Q * 4, bar);
     }
@@ -984,7 +986,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
     // W_ji = (C B^T)_ji exp(cs_j - cs_i) dt_i for j >= i (else 0), as bf16 high + low
     for (int e = tid; e < Q * Q / 2; e += kSsdThreads) {
       const int j = e / (Q / 2), i = 2 * (e % (Q / 2));
-      const float2 cb = *reinterpret_cast<const float2*>(CBs + j * Q + i);
+      const float2 cb = *reinterpret_cast<const float2*>(CBs + j * kSsdCBPitch + i);
       const float cj = css[j];
       const float2 v = make_float2(j >= i ? cb.x * __expf(cj - css[i]) * dts[i] : 0.f,
                                    j >= i + 1 ? cb.y * __expf(cj - css[i + 1]) * dts[i + 1] : 0.f);
@@ -1079,6 +1081,232 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
       }
     fence_smem_to_async();  // this thread's stores into the stage come before the next copies
     __syncthreads();        // the copies of the next item may overwrite every buffer
+  }
+}
+
+// Pass 2 on the 5th-generation tensor cores (P = 128): per item (b, c, h) the outputs as
+// their transpose, M = 128 head rows p by N = 64 steps t,
+//   Y^T = X^T W^T + (H C^T) diag(exp(cs)),   W_ti = (C B^T)_ti exp(cs_t - cs_i) dt_i (t >= i),
+// with D folded into W's diagonal (D x_t = sum_i x_i D [i == t]). Two TMEM accumulators per
+// item (double-buffered across items): D1 = X^T W^T (X an MN-major operand with the
+// 128-byte swizzle; W^T a K-major operand without swizzle, bf16 high + low, built by the
+// workers from C B^T) and D2 = H C^T (H the walk's K-major image; C a K-major operand with
+// the 128-byte swizzle, K-steps 32 bytes apart inside the swizzle atom). Warp-specialised
+// like the walk, with two stages: warp 9's lane 0 copies item k by TMA and bulk copies into
+// stage k % 2 once the MMAs of item k - 2 have read it; warps 0-7 zero the rows past L,
+// build W^T and exp(cs), and write the previous item's outputs (warp w: head rows 32 (w % 4)
+// .. + 31, one per thread, and steps 32 (w / 4) .. + 31; a warp stores 32 consecutive head
+// channels of a step); warp 8's lane 0 issues 8 + N / 16 MMAs per item.
+constexpr int kTcScanWorkers = 256;
+constexpr int kTcScanThreads = kTcScanWorkers + 64;
+template <int N>
+struct SsdTcScan {
+  static constexpr int Q = kSsdQ, P = kTcP;
+  // one stage (two per CTA: item k in stage k % 2)
+  static constexpr int kX = 0;                          // X: 2 halves [Q][128 B], swizzled
+  static constexpr int kC = kX + Q * P * 2;             // C: N / 64 halves [Q][128 B], swizzled
+  static constexpr int kH = kC + Q * N * 2;             // entering state, K-major image
+  static constexpr int kCB = kH + P * N * 2;            // C B^T, Q rows of kSsdCBPitch floats
+  static constexpr int kDt = kCB + Q * kSsdCBPitch * 4;
+  static constexpr int kCs = kDt + Q * 4;
+  static constexpr int kW = kCs + Q * 4;                // W^T high, then low: 8 x 8 core matrices each
+  static constexpr int kStage = (kW + 2 * Q * Q * 2 + 1023) / 1024 * 1024;
+  static constexpr int kEcs = 2 * kStage;               // exp(cs) of the last two items, [2][Q]
+  static constexpr int kBar = kEcs + 2 * Q * 4;         // loaded[2], empty[2], full[2], tfull[2], tempty[2]
+  static constexpr int kSlot = kBar + 10 * 8;
+  static constexpr int kAbort = kSlot + 4;
+  static constexpr int kBytes = kAbort + 12 + 1024;     // + room to align the base to 1 KB
+  static constexpr uint32_t kTx = Q * P * 2 + Q * N * 2 + P * N * 2 + Q * kSsdCBPitch * 4 + 2 * Q * 4;
+  static constexpr uint32_t kHsbo = (N / 8) * 128;      // H image: core matrices (p8, n8) at p8 kHsbo + n8 128
+  static_assert(kC % 1024 == 0 && kH % 1024 == 0 && kW % 16 == 0, "operand alignment");
+};
+
+template <int N, typename TY>
+__global__ void __launch_bounds__(kTcScanThreads, 1)
+    ssd_chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
+                             const SsdParams p) {
+  using L = SsdTcScan<N>;
+  constexpr int Q = kSsdQ, P = kTcP;
+  constexpr uint32_t kIdesc1 = umma_idesc_bf16(P, Q, true, false);   // X^T (MN-major) x W^T (K-major)
+  constexpr uint32_t kIdesc2 = umma_idesc_bf16(P, Q, false, false);  // H (K-major) x C^T (K-major)
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
+  unsigned char* sm = smem_dyn + ((1024u - (umma_saddr(smem_dyn) & 1023u)) & 1023u);
+  uint64_t* loaded = reinterpret_cast<uint64_t*>(sm + L::kBar);  // [2]
+  uint64_t* empty = loaded + 2;                                   // [2]
+  uint64_t* full = loaded + 4;                                    // [2]
+  uint64_t* tfull = loaded + 6;                                   // [2]
+  uint64_t* tempty = loaded + 8;                                  // [2]
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L::kSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  float* ecs = reinterpret_cast<float*>(sm + L::kEcs);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t items = p.batch * p.nc * p.H;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&loaded[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], kTcScanWorkers);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kTcScanWorkers);
+    }
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_c);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (warp == 9) {  // ---------------- copier ----------------
+    if (lane == 0) {
+      for (int k = 0;; ++k) {
+        const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+        if (it >= items) break;
+        const int s = k & 1;
+        // stage s last held item k - 2: wait until its MMAs have read it
+        if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort)) break;
+        unsigned char* st = sm + s * L::kStage;
+        const SsdItem m = ssd_item(p, it);
+        const int32_t row = (int32_t)(m.b * p.L + m.t0);
+        mbar_arrive_expect_tx(&loaded[s], L::kTx);
+        tma_load_3d_bar(st + L::kX, &tm_x, 0, (int32_t)m.h, row, &loaded[s]);
+        tma_load_3d_bar(st + L::kX + 8192, &tm_x, 64, (int32_t)m.h, row, &loaded[s]);
+#pragma unroll
+        for (int hc = 0; hc < N / 64; ++hc)
+          tma_load_2d(st + L::kC + hc * 8192, &tm_c, (int32_t)(m.g * N + 64 * hc), row, &loaded[s]);
+        bulk_load(st + L::kH, p.ws_H + it * (int64_t)P * N, P * N * 2, &loaded[s]);
+        bulk_load(st + L::kCB, p.ws_CB + ((m.b * p.nc + m.c) * p.G + m.g) * Q * kSsdCBPitch, Q * kSsdCBPitch * 4,
+                  &loaded[s]);
+        bulk_load(st + L::kDt, p.ws_dt + it * Q, Q * 4, &loaded[s]);
+        bulk_load(st + L::kCs, p.ws_cs + it * Q, Q * 4, &loaded[s]);
+      }
+    }
+  } else if (warp == 8) {  // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      for (int k = 0;; ++k) {
+        const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+        if (it >= items) break;
+        const int s = k & 1;
+        if (!tc_wait(&full[s], (uint32_t)((k >> 1) & 1), abort)) break;
+        if (k >= 2 && !tc_wait(&tempty[s], (uint32_t)(((k - 2) >> 1) & 1), abort)) break;
+        tc_fence_after();
+        const unsigned char* st = sm + s * L::kStage;
+        const uint32_t xa = umma_saddr(st + L::kX), ca = umma_saddr(st + L::kC), ha = umma_saddr(st + L::kH);
+        const uint32_t wh = umma_saddr(st + L::kW), wl = wh + Q * Q * 2;
+        const uint32_t d1 = tmem + 128u * (uint32_t)s, d2 = d1 + 64u;
+#pragma unroll
+        for (int ks = 0; ks < Q / 16; ++ks) {  // X^T W^T over the chunk's steps i
+          const uint64_t ad = umma_sdesc(xa + ks * 2048, 8192, 1024, 2);
+          umma_bf16(d1, ad, umma_sdesc(wh + ks * 256, 128, 1024), kIdesc1, ks > 0);
+          umma_bf16(d1, ad, umma_sdesc(wl + ks * 256, 128, 1024), kIdesc1, true);
+        }
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks)  // H C^T over the state columns n
+          umma_bf16(d2, umma_sdesc(ha + ks * 256, 128, L::kHsbo),
+                    umma_sdesc(ca + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, 2), kIdesc2, ks > 0);
+        umma_commit(&tfull[s]);
+        umma_commit(&empty[s]);
+      }
+    }
+  } else {  // ---------------- workers ----------------
+    const int q = warp & 3, th = warp >> 2;  // TMEM lane quarter, half of the steps
+    const int prow = 32 * q + lane;          // head row of this thread in the epilogue (TMEM lane)
+    // item k's outputs (y rows of its chunk; the MMA results in TMEM buffer k % 2)
+    auto epilogue = [&](int k) {
+      const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+      const SsdItem m = ssd_item(p, it);
+      const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
+      const int bsel = k & 1;
+      if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort)) return false;
+      tc_fence_after();
+      uint32_t v1[32], v2[32];
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)bsel + 32u * (uint32_t)th;
+      tmem_ld32_nowait(ta, v1);
+      tmem_ld32_nowait(ta + 64u, v2);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&tempty[bsel]);
+      const float* e = ecs + bsel * Q + 32 * th;
+      const int64_t ystride = p.H * P;
+      TY* yb = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + 32 * th) * p.H + m.h) * P + prow;
+      const int tn = rv - 32 * th;  // steps of this half inside the sequence
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (c < tn) *yb = from_f32<TY>(fmaf(e[c], __uint_as_float(v2[c]), __uint_as_float(v1[c])));
+        yb += ystride;
+      }
+      return true;
+    };
+    bool ok = true;
+    int k = 0;
+    for (;; ++k) {
+      const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
+      if (it >= items) break;
+      const int s = k & 1;
+      unsigned char* st = sm + s * L::kStage;
+      const SsdItem m = ssd_item(p, it);
+      const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort)) ok = false;
+      if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
+        for (int i = tid; i < (Q - rv) * (P / 8); i += kTcScanWorkers) {
+          const int t = rv + i / (P / 8), c = i % (P / 8);
+          *reinterpret_cast<uint4*>(st + L::kX + (c >> 3) * 8192 + t * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (!bar_and(ok, 1, kTcScanWorkers)) {
+        ok = false;
+        break;
+      }
+      {  // W^T (bf16 high + low, K-major core matrices (t / 8, i / 8)) and exp(cs) of item k
+        const float* CBs = reinterpret_cast<const float*>(st + L::kCB);
+        const float* dts = reinterpret_cast<const float*>(st + L::kDt);
+        const float* css = reinterpret_cast<const float*>(st + L::kCs);
+        const float Dh = p.Dskip ? p.Dskip[m.h] : 0.f;
+#pragma unroll
+        for (int r = 0; r < (Q * Q / 8) / kTcScanWorkers; ++r) {
+          // eight consecutive threads write one core matrix (rows t % 8 of columns i8)
+          const int u = tid + r * kTcScanWorkers;
+          const int t8 = u >> 6, t = t8 * 8 + (u & 7), i8 = (u >> 3) & 7;
+          const float ct = css[t];
+          const int off = (t >> 3) * 1024 + i8 * 128 + (t & 7) * 16;
+          uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
+          if (i8 <= t8) {  // blocks above the diagonal stay zero
+            const float4 cb0 = *reinterpret_cast<const float4*>(CBs + t * kSsdCBPitch + 8 * i8);
+            const float4 cb1 = *reinterpret_cast<const float4*>(CBs + t * kSsdCBPitch + 8 * i8 + 4);
+            const float cbv[8] = {cb0.x, cb0.y, cb0.z, cb0.w, cb1.x, cb1.y, cb1.z, cb1.w};
+            float w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int i = 8 * i8 + e;
+              w[e] = t >= i ? cbv[e] * __expf(ct - css[i]) * dts[i] : 0.f;
+              if (t == i) w[e] += Dh;
+            }
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(w[2 * e], w[2 * e + 1]), hi[e], lo[e]);
+            hv = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            lv = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+          *reinterpret_cast<uint4*>(st + L::kW + off) = hv;
+          *reinterpret_cast<uint4*>(st + L::kW + Q * Q * 2 + off) = lv;
+          if (i8 == 0) ecs[s * Q + t] = __expf(ct);
+        }
+      }
+      fence_smem_to_async();
+      mbar_arrive(&full[s]);
+      if (k >= 1 && !epilogue(k - 1)) ok = false;
+    }
+    if (ok && k >= 1) epilogue(k - 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 

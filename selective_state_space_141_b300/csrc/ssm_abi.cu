@@ -862,14 +862,14 @@ SsdPlan ssd_plan(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t P, int6
   pl.off_dt = r256(items * P * N * 2);
   pl.off_cs = pl.off_dt + r256(items * ssm::kSsdQ * 4);
   pl.off_CB = pl.off_cs + r256(items * ssm::kSsdQ * 4);
-  pl.bytes = pl.off_CB + r256((size_t)batch * nc * G * ssm::kSsdQ * ssm::kSsdQ * 4);
+  pl.bytes = pl.off_CB + r256((size_t)batch * nc * G * ssm::kSsdQ * ssm::kSsdCBPitch * 4);
   return pl;
 }
 
 // Persistent grid: as many CTAs as fit on the GPU at once, at most one per item.
-unsigned persistent_grid(const void* kern, int smem, int64_t items) {
+unsigned persistent_grid(const void* kern, int threads, int smem, int64_t items) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ssm::kSsdThreads, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   int64_t n = (int64_t)(num_sms() > 0 ? num_sms() : 1) * per_sm;
@@ -956,13 +956,24 @@ cudaError_t launch_ssd_chunked(const ssm::SsdParams& p, bool y_f32, cudaStream_t
                            smem, st);
     if (e != cudaSuccess) return e;
   }
+  void* sargs[] = {&tm_x, &tm_c, const_cast<ssm::SsdParams*>(&p)};
+  const int64_t items = p.batch * p.nc * p.H;
+  if (P == ssm::kTcP) {  // the read-out on tcgen05
+    constexpr int smem = ssm::SsdTcScan<N>::kBytes;
+    const void* k = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_tc_kernel<N, float>)
+                          : reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_tc_kernel<N, __nv_bfloat16>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaLaunchKernel(k, dim3(persistent_grid(k, ssm::kTcScanThreads, smem, items)), dim3(ssm::kTcScanThreads),
+                           sargs, smem, st);
+    return e;
+  }
   constexpr int smem = ssm::ssd_scan_smem_bytes<P, N>();
   const void* k = y_f32 ? reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, float>)
                         : reinterpret_cast<const void*>(&ssm::ssd_chunk_scan_kernel<P, N, __nv_bfloat16>);
-  void* sargs[] = {&tm_x, &tm_c, const_cast<ssm::SsdParams*>(&p)};
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
-    e = cudaLaunchKernel(k, dim3(persistent_grid(k, smem, p.batch * p.nc * p.H)), dim3(ssm::kSsdThreads), sargs,
+    e = cudaLaunchKernel(k, dim3(persistent_grid(k, ssm::kSsdThreads, smem, items)), dim3(ssm::kSsdThreads), sargs,
                          smem, st);
   return e;
 }

@@ -335,6 +335,6 @@ def test_ssd_validation(lib):
     # per (b, c, h): entering state (bf16 P x N) + dt, cs (64 floats each); per (b, c, g): C B^T
     items, cbs = 2 * 2 * 4, 2 * 2 * 2
     r256 = lambda v: (v + 255) // 256 * 256
-    assert n.value == r256(items * 64 * 64 * 2) + 2 * r256(items * 64 * 4) + r256(cbs * 64 * 64 * 4)
+    assert n.value == r256(items * 64 * 64 * 2) + 2 * r256(items * 64 * 4) + r256(cbs * 64 * 72 * 4)
     assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 0, 64, 64, ctypes.byref(n)) == 2
     assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 2, 64, 64, None) == 1
