@@ -1092,12 +1092,12 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
 // 128-byte swizzle; W^T a K-major operand without swizzle, bf16 high + low, built by the
 // workers from C B^T) and D2 = H C^T (H the walk's K-major image; C a K-major operand with
 // the 128-byte swizzle, K-steps 32 bytes apart inside the swizzle atom). Warp-specialised
-// like the walk, with two stages: warp 9's lane 0 copies item k by TMA and bulk copies into
-// stage k % 2 once the MMAs of item k - 2 have read it; warps 0-7 zero the rows past L,
+// like the walk, with two stages: warp 17's lane 0 copies item k by TMA and bulk copies into
+// stage k % 2 once the MMAs of item k - 2 have read it; warps 0-15 zero the rows past L,
 // build W^T and exp(cs), and write the previous item's outputs (warp w: head rows 32 (w % 4)
-// .. + 31, one per thread, and steps 32 (w / 4) .. + 31; a warp stores 32 consecutive head
-// channels of a step); warp 8's lane 0 issues 8 + N / 16 MMAs per item.
-constexpr int kTcScanWorkers = 256;
+// .. + 31, one per thread, and steps 16 (w / 4) .. + 15; a warp stores 32 consecutive head
+// channels of a step); warp 16's lane 0 issues 8 + N / 16 MMAs per item.
+constexpr int kTcScanWorkers = 512;
 constexpr int kTcScanThreads = kTcScanWorkers + 64;
 template <int N>
 struct SsdTcScan {
@@ -1161,7 +1161,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == 9) {  // ---------------- copier ----------------
+  if (warp == 17) {  // ---------------- copier ----------------
     if (lane == 0) {
       for (int k = 0;; ++k) {
         const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
@@ -1185,7 +1185,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         bulk_load(st + L::kCs, p.ws_cs + it * Q, Q * 4, &loaded[s]);
       }
     }
-  } else if (warp == 8) {  // ---------------- MMA issuer ----------------
+  } else if (warp == 16) {  // ---------------- MMA issuer ----------------
     if (lane == 0) {
       for (int k = 0;; ++k) {
         const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
@@ -1213,7 +1213,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       }
     }
   } else {  // ---------------- workers ----------------
-    const int q = warp & 3, th = warp >> 2;  // TMEM lane quarter, half of the steps
+    const int q = warp & 3, th = warp >> 2;  // TMEM lane quarter, quarter of the steps
     const int prow = 32 * q + lane;          // head row of this thread in the epilogue (TMEM lane)
     // item k's outputs (y rows of its chunk; the MMA results in TMEM buffer k % 2)
     auto epilogue = [&](int k) {
@@ -1223,19 +1223,19 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       const int bsel = k & 1;
       if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort)) return false;
       tc_fence_after();
-      uint32_t v1[32], v2[32];
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)bsel + 32u * (uint32_t)th;
-      tmem_ld32_nowait(ta, v1);
-      tmem_ld32_nowait(ta + 64u, v2);
+      uint32_t v1[16], v2[16];
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)bsel + 16u * (uint32_t)th;
+      tmem_ld16_nowait(ta, v1);
+      tmem_ld16_nowait(ta + 64u, v2);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&tempty[bsel]);
-      const float* e = ecs + bsel * Q + 32 * th;
+      const float* e = ecs + bsel * Q + 16 * th;
       const int64_t ystride = p.H * P;
-      TY* yb = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + 32 * th) * p.H + m.h) * P + prow;
-      const int tn = rv - 32 * th;  // steps of this half inside the sequence
+      TY* yb = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + 16 * th) * p.H + m.h) * P + prow;
+      const int tn = rv - 16 * th;  // steps of this quarter inside the sequence
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 16; ++c) {
         if (c < tn) *yb = from_f32<TY>(fmaf(e[c], __uint_as_float(v2[c]), __uint_as_float(v1[c])));
         yb += ystride;
       }
@@ -1277,12 +1277,18 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
           if (i8 <= t8) {  // blocks above the diagonal stay zero
             const float4 cb0 = *reinterpret_cast<const float4*>(CBs + t * kSsdCBPitch + 8 * i8);
             const float4 cb1 = *reinterpret_cast<const float4*>(CBs + t * kSsdCBPitch + 8 * i8 + 4);
+            const float4 ci0 = *reinterpret_cast<const float4*>(css + 8 * i8);
+            const float4 ci1 = *reinterpret_cast<const float4*>(css + 8 * i8 + 4);
+            const float4 di0 = *reinterpret_cast<const float4*>(dts + 8 * i8);
+            const float4 di1 = *reinterpret_cast<const float4*>(dts + 8 * i8 + 4);
             const float cbv[8] = {cb0.x, cb0.y, cb0.z, cb0.w, cb1.x, cb1.y, cb1.z, cb1.w};
+            const float civ[8] = {ci0.x, ci0.y, ci0.z, ci0.w, ci1.x, ci1.y, ci1.z, ci1.w};
+            const float div[8] = {di0.x, di0.y, di0.z, di0.w, di1.x, di1.y, di1.z, di1.w};
             float w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int i = 8 * i8 + e;
-              w[e] = t >= i ? cbv[e] * __expf(ct - css[i]) * dts[i] : 0.f;
+              w[e] = t >= i ? cbv[e] * __expf(ct - civ[e]) * div[e] : 0.f;
               if (t == i) w[e] += Dh;
             }
             uint32_t hi[4], lo[4];
