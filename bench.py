@@ -447,9 +447,9 @@ def ssd_bench(args, ssm, torch, inputs, dev, peaks):
                          "hbm": {"achieved_gbs": gbs, "peak_gbs": hpk, "frac": gbs / hpk,
                                  "algorithmic_bytes": w.compulsory_bytes()}},
             "calls": args.ssd_steps, "workspace_bytes": nbytes, "launches_per_call": 3,
-            "kernel": "step sizes + C B^T per chunk (mma.sync); state walk on tcgen05 (TMEM accumulators, TMA "
-                      "operands; CTA per batch, head, 32 state columns); persistent read-out on mma.sync m16n8k16 "
-                      "with TMA operands (2 CTAs/SM); bf16 operands, fp32 accumulate"}
+            "kernel": "step sizes + C B^T per chunk (mma.sync); state walk and persistent read-out on tcgen05 "
+                      "(TMEM accumulators, TMA operands, warp-specialised copier / MMA / worker warps); bf16 "
+                      "operands (hi/lo pairs for products of inputs), fp32 accumulate"}
 
 
 def decode_bench(args, ssm, torch, inputs, dev, hbm_peak):
