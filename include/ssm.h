@@ -369,8 +369,8 @@ SSM_API ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_
  *   y[b,t,h,:] = S C[b,t,g,:] + D[h] x[b,t,h,:]
  * computed in chunks of 64 steps: inside a chunk as the masked quadratic form
  * tril(C B^T o decay) (dt X) plus the carried state read out, across chunks by carrying
- * S on chip; the four contractions per chunk run on the tensor cores (bf16 operands,
- * fp32 accumulation, fp32 state).
+ * S (fp32); the contractions per chunk run on the tensor cores (bf16 operands, products
+ * of inputs as bf16 high + low pairs, fp32 accumulation).
  *
  * Descriptors are 3-D views (the last two dimensions of each tensor flattened):
  *   groups       number of B/C groups G (divides H)

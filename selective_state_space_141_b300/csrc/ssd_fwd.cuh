@@ -12,11 +12,12 @@
 // (W and w B reach the tensor cores as bf16 high + low pairs, ~16 significant bits: a
 // single bf16 rounding of these products of inputs would cost 2^-9 of |y| per term, and
 // w B feeds the carried state every chunk, where that rounding accumulates)
-// The four contractions (C B^T, W X, C S^T, X^T (w B)) run on the tensor cores
-// (mma.sync m16n8k16, bf16 operands, fp32 accumulation); the state stays on chip in fp32
-// (with a bf16 copy as the operand of C S^T) for the whole sequence: one CTA of 8 warps
-// per (batch, head) walks the chunks in order, prefetching the next chunk's inputs into
-// registers while the current one is computed.
+// Two schedules. Without a workspace, ssd_fwd_kernel: one CTA of 8 warps per (batch, head)
+// walks the chunks in order with the fp32 state on chip (the four contractions C B^T, W X,
+// C S^T, X^T (w B) on mma.sync m16n8k16), prefetching the next chunk's inputs into
+// registers while the current one is computed. With a workspace, the chunk-parallel
+// schedule further down: step sizes and C B^T per chunk, the state walk, and the read-out
+// of every chunk at once, on tcgen05 for P = 128.
 #pragma once
 
 #include "common.cuh"
