@@ -343,40 +343,66 @@ def run_ours(args, w, ws, rank, local):
 
 
 def e2e(w, d, args, ssm, torch, stream):
-    """Same metric through the public call with HOST inputs: every step copies the
-    inputs from pinned host memory, runs the scan and copies y + last_state back."""
+    """Same metric through the public call with HOST inputs: every step copies its inputs
+    from pinned host memory, runs the scan and copies y + last_state back to pinned host
+    memory. Steps are pipelined the way a serving loop would run them: two sets of device
+    and host buffers, host-to-device copies, the scan and device-to-host copies on three
+    streams, so that step i's upload, step i-1's scan and step i-2's download overlap
+    (events keep every buffer from being reused before its last reader is done)."""
     names = [k for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias") if d.get(k) is not None]
     host = {k: d[k].cpu().pin_memory() for k in names}
-    dev_in = {k: torch.empty_like(d[k]) for k in names}
-    y_h = torch.empty(d["u"].shape, dtype=d["u"].dtype).pin_memory()
-    last_h = torch.empty(w.batch, w.D, w.N, dtype=torch.float32).pin_memory()
-    y = torch.empty_like(d["u"])
-    last = torch.empty(w.batch, w.D, w.N, dtype=torch.float32, device=d["u"].device)
+    dev_in = [{k: torch.empty_like(d[k]) for k in names} for _ in range(2)]
+    y_h = [torch.empty(d["u"].shape, dtype=d["u"].dtype).pin_memory() for _ in range(2)]
+    last_h = [torch.empty(w.batch, w.D, w.N, dtype=torch.float32).pin_memory() for _ in range(2)]
+    y = [torch.empty_like(d["u"]) for _ in range(2)]
+    last = [torch.empty(w.batch, w.D, w.N, dtype=torch.float32, device=d["u"].device) for _ in range(2)]
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
-    d2h = y_h.numel() * y_h.element_size() + last_h.numel() * 4
+    d2h = y_h[0].numel() * y_h[0].element_size() + last_h[0].numel() * 4
+    s_in, s_out, s_comp = torch.cuda.Stream(), torch.cuda.Stream(), stream
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]
+    in_done, comp_done, out_done = ev(), ev(), ev()
+    used = [False, False]
 
-    def step():
-        for k in names:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        ssm.selective_scan_fwd(dev_in["u"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"],
-                               D=dev_in.get("D"), z=dev_in.get("z"), delta_bias=dev_in.get("delta_bias"), y=y,
-                               last_state=last, stream=stream)
-        y_h.copy_(y, non_blocking=True)
-        last_h.copy_(last, non_blocking=True)
+    def step(i):
+        j = i % 2
+        if used[j]:
+            s_in.wait_event(comp_done[j])  # the scan of step i - 2 has read this input set
+            s_comp.wait_event(out_done[j])  # the download of step i - 2 has read this output set
+        with torch.cuda.stream(s_in):
+            for k in names:
+                dev_in[j][k].copy_(host[k], non_blocking=True)
+            in_done[j].record(s_in)
+        s_comp.wait_event(in_done[j])
+        x = dev_in[j]
+        ssm.selective_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x.get("D"), z=x.get("z"),
+                               delta_bias=x.get("delta_bias"), y=y[j], last_state=last[j], stream=s_comp)
+        comp_done[j].record(s_comp)
+        s_out.wait_event(comp_done[j])
+        with torch.cuda.stream(s_out):
+            y_h[j].copy_(y[j], non_blocking=True)
+            last_h[j].copy_(last[j], non_blocking=True)
+            out_done[j].record(s_out)
+        used[j] = True
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     n = max(1, min(args.steps, args.e2e_steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_comp.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(n):
+        step(2 + i)
+    e1.record(s_out)
     torch.cuda.synchronize()
+    jl = (2 + n - 1) % 2  # the last step's buffers: the download must equal the device result
+    if not (torch.equal(y_h[jl], y[jl].cpu()) and torch.equal(last_h[jl], last[jl].cpu())):
+        raise RuntimeError("e2e: downloaded result differs from the device result")
     sec = e0.elapsed_time(e1) / 1e3 / n
     return {"value": w.compulsory_bytes() / sec / 1e9, "unit": "GB/s", "ms_per_step": sec * 1e3,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "pipelining": "2 buffer sets; uploads, scans and downloads on 3 streams"}
 
 
 def backward_bench(args, ssm, torch, w, d, dev, fwd_launch_ms):
