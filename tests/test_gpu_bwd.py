@@ -80,3 +80,32 @@ def test_bwd_empty_sequence():
     g = run(d, torch.float32)
     assert torch.count_nonzero(g["dA"]) == 0 and torch.count_nonzero(g["dD"]) == 0
     assert torch.equal(g["dh0"], d["dlast"])
+
+
+def test_bwd_layer_workload_sampled():
+    """The Mamba-1.4B layer (4 x 4096 x 4096, N = 16) in the bench's launch configuration
+    (bf16 dy and gradients, caller workspace): the per-channel gradients (du, ddelta, dz,
+    dA, dD, dbias) of sampled channels against the oracle run on those channels alone.
+    (dB and dC sum over every channel; the smaller shapes above check them whole.)"""
+    w = inputs.FWD_WORKLOADS["m1p4b"]
+    d = inputs.fwd_inputs(w, DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    dy = torch.randn(d["u"].shape, generator=g, device=DEV).to(d["u"].dtype)
+    wsp = torch.empty(ssm.bwd_workspace_size(w.batch, w.L, w.D, w.N), dtype=torch.uint8, device=DEV)
+    gr = ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, D=d["D"], z=d["z"],
+                                delta_bias=d["delta_bias"], delta_softplus=True, workspace=wsp)
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    rng = np.random.default_rng(94)
+    ds = np.unique(np.concatenate([[0, 15, 16, w.D - 1], rng.choice(w.D, size=8, replace=False)]))
+    idx = torch.as_tensor(ds, device=DEV)
+    pick = lambda t: t.index_select(-1, idx)
+    r = oracle.selective_scan_bwd(pick(d["u"]), pick(d["delta"]), d["A"].index_select(0, idx), d["B"], d["C"],
+                                  pick(dy), D=d["D"].index_select(0, idx), z=pick(d["z"]),
+                                  delta_bias=d["delta_bias"].index_select(0, idx), delta_softplus=True,
+                                  h0=np.zeros((w.batch, len(ds), w.N)))
+    for k in ("du", "ddelta", "dz"):
+        check(pick(gr[k]), r[k], TOL_BF16, True, k)
+    check(gr["dA"].index_select(0, idx), r["dA"], TOL_BF16, False, "dA")
+    for k in ("dD", "dbias"):
+        check(gr[k].index_select(0, idx), r[k], TOL_BF16, False, k)
