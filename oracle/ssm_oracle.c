@@ -45,7 +45,11 @@ double ssm_oracle_silu(double z) {
  * zero-order-hold discretisation; "8.7 State Space Models (Mamba)", section 3), with
  * its limit delta at a = 0. */
 static double zoh_factor(double dt, double a) {
+#if SSM_ORACLE_PLANT == 16
+  return a != 0.0 ? expm1(dt * a) : dt; /* planted: the 1 / a of the hold dropped */
+#else
   return a != 0.0 ? expm1(dt * a) / a : dt;
+#endif
 }
 
 typedef struct {
@@ -249,7 +253,11 @@ int ssm_oracle_conv1d_silu(int64_t batch, int64_t L, int64_t D, const double* x,
             xv = x[(b * L + s) * D + d];
           else
             xv = conv_state ? conv_state[(b * D + d) * 3 + (3 + s)] : 0.0;
+#if SSM_ORACLE_PLANT == 15
+          acc += w[d * 4 + (3 - k)] * xv; /* planted: taps in reverse order */
+#else
           acc += w[d * 4 + k] * xv;
+#endif
         }
         u[(b * L + t) * D + d] = ssm_oracle_silu(acc);
       }
@@ -327,12 +335,25 @@ int ssm_oracle_bwd(int64_t batch, int64_t L, int64_t D, int64_t N,
           const double An = A[d * N + n];
           const double a = exp(dt * An);
           g[n] += dv * C[ixn + n];
+#if SSM_ORACLE_PLANT == 11
+          g[n] *= a; /* planted: g carried to step t-1 before its use at step t */
+#endif
+#if SSM_ORACLE_PLANT == 12
+          dC[ixn + n] += dv * hp[n]; /* planted: dC from h_{t-1} instead of h_t */
+#else
           dC[ixn + n] += dv * ht[n];
+#endif
           dB[ixn + n] += g[n] * dt * x;
           dux += g[n] * dt * B[ixn + n];
+#if SSM_ORACLE_PLANT == 10
+          ddt += g[n] * (B[ixn + n] * x); /* planted: the A a h_{t-1} term of d(dt) dropped */
+#else
           ddt += g[n] * (B[ixn + n] * x + An * a * hp[n]);
+#endif
           dA[d * N + n] += g[n] * a * hp[n] * dt;
+#if SSM_ORACLE_PLANT != 11
           g[n] *= a;
+#endif
         }
         du[ix] = dux;
         const double dr = delta_softplus ? ddt / (1.0 + exp(-rs[t])) : ddt;
@@ -365,7 +386,11 @@ int ssm_oracle_ssd_fwd(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N
   if (!S) return -1;
   for (int64_t b = 0; b < batch; ++b) {
     for (int64_t h = 0; h < H; ++h) {
+#if SSM_ORACLE_PLANT == 13
+      const int64_t g = h % G; /* planted: heads assigned to groups round-robin */
+#else
       const int64_t g = h / (H / G);
+#endif
       for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[(b * H + h) * P * N + i] : 0.0;
       for (int64_t t = 0; t < L; ++t) {
         double r = delta[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
@@ -378,7 +403,11 @@ int ssm_oracle_ssd_fwd(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N
         for (int64_t p = 0; p < P; ++p) {
           double acc = 0.0;
           for (int64_t n = 0; n < N; ++n) {
+#if SSM_ORACLE_PLANT == 14
+            S[p * N + n] = a * (S[p * N + n] + dt * xt[p] * Bt[n]); /* planted: input decayed too */
+#else
             S[p * N + n] = a * S[p * N + n] + dt * xt[p] * Bt[n];
+#endif
             acc += S[p * N + n] * Ct[n];
           }
           yt[p] = acc + (Dskip ? Dskip[h] * xt[p] : 0.0);
