@@ -183,7 +183,7 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
 
 // grid (W = ceil(D / 16), batch), block 32 (one warp: 16 channels x two halves of the
 // states); dynamic shared memory:
-//   hs  [kBwdK + 1][N/2][32] f32  each lane's states h_{t0-1} .. h_{t0+K-1} of the chunk
+//   hs  [kBwdK + 1][N/4][32] f32x2 each lane's state pairs h_{t0-1} .. h_{t0+K-1} of the chunk
 //   bc  [kBwdK][2N]          f32  the chunk's B | C rows
 //   dts [kBwdK][32]          f32  step sizes (both lanes of a channel hold the same)
 //   vs  [kBwdK][32]          f32  read-outs C.h + D u (before the gate)
@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   constexpr int NH = N / 2;   // states per lane
   constexpr int P2 = NH / 2;  // packed pairs per lane
   extern __shared__ __align__(16) float sm[];
-  float* hs = sm;
+  float* hs = sm;  // [kBwdK + 1][P2][32] float2: state pairs of each lane
+  float2* hs2 = reinterpret_cast<float2*>(hs);
   float* bc = hs + (kBwdK + 1) * NH * 32;
   float* dts = bc + kBwdK * 2 * N;
   float* vs = dts + kBwdK * 32;
@@ -235,7 +236,11 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     if (kAccurate) return softplus_precise(r);
     return fmaxf(r, 0.f) + kLn2 * lg2(1.f + ex2(fabsf(r) * -kLog2e));  // SFU form, as the forward
   };
-  auto sigmoid = [&](float x) { return __frcp_rn(1.f + __expf(-x)); };
+  // the bf16 path divides with the fast approximate reciprocal (~2 ulp), well inside its
+  // tolerance; the fp32 path keeps the correctly rounded one
+  auto sigmoid = [&](float x) {
+    return kAccurate ? __frcp_rn(1.f + __expf(-x)) : __fdividef(1.f, 1.f + __expf(-x));
+  };
 
   // ---- forward sweep: the state before every chunk ----
   if (p.nc > 1) stage_chunk<T, TG, N>(stg[0], p, b, 0, d0, false, lane);
@@ -297,8 +302,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
       for (int q = 0; q < P2; ++q) {
         h[q] = vd ? ckp[q] : make_float2(0.f, 0.f);
-        hs[(2 * q) * 32 + lane] = h[q].x;
-        hs[(2 * q + 1) * 32 + lane] = h[q].y;
+        hs2[q * 32 + lane] = h[q];
       }
       for (int k = 0; k < kc; ++k) {
         const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
@@ -313,8 +317,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
         for (int q = 0; q < P2; ++q) {
           h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
           acc = __ffma2_rn(c2[q], h[q], acc);
-          hs[((k + 1) * NH + 2 * q) * 32 + lane] = h[q].x;
-          hs[((k + 1) * NH + 2 * q + 1) * 32 + lane] = h[q].y;
+          hs2[((k + 1) * P2 + q) * 32 + lane] = h[q];
         }
         const float vp = acc.x + acc.y;
         vs[k * 32 + lane] = fmaf(Dk, x, vp + __shfl_xor_sync(0xffffffffu, vp, 1));
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       float vb[NH], vc[NH];
 #pragma unroll
       for (int q = 0; q < P2; ++q) {
-        const float2 hp = make_float2(hs[(k * NH + 2 * q) * 32 + lane], hs[(k * NH + 2 * q + 1) * 32 + lane]);
+        const float2 hp = hs2[(k * P2 + q) * 32 + lane];
         const float2 a = decay2<kAccurate>(dt2, Av[q], A2[q]);
         const float2 B2 = b2[q];
         g[q] = __ffma2_rn(dv2, c2[q], g[q]);                 // g = dL/dh_t
