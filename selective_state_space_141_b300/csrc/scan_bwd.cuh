@@ -172,6 +172,25 @@ __device__ __forceinline__ void stage_chunk(BwdStage<T, TG, N>& sg, const BwdPar
   cp_async_commit();
 }
 
+// The P2 state pairs of this lane's half of a B or C row; 16-byte loads when P2 is even
+// (the row and the half then start 16-byte aligned).
+template <int P2>
+__device__ __forceinline__ void load_pairs(const float* row, float2 (&v)[P2]) {
+  if constexpr (P2 % 2 == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll
+    for (int i = 0; i < P2 / 2; ++i) {
+      const float4 t = r4[i];
+      v[2 * i] = make_float2(t.x, t.y);
+      v[2 * i + 1] = make_float2(t.z, t.w);
+    }
+  } else {
+    const float2* r2 = reinterpret_cast<const float2*>(row);
+#pragma unroll
+    for (int i = 0; i < P2; ++i) v[i] = r2[i];
+  }
+}
+
 // Decay factors of two states: 2^(dt A log2 e) on the SFU, or exp in double on the
 // fp32 I/O path (as the forward kernels).
 template <bool kAccurate>
@@ -260,7 +279,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
       const float dx = dt * to_f32(sg.u[k][ch]);
       const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
+      float2 b2[P2];
+      load_pairs<P2>(bc + k * 2 * N + nb, b2);
 #pragma unroll
       for (int q = 0; q < P2; ++q)
         h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
@@ -310,8 +330,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
         const float dx = dt * x;
         dts[k * 32 + lane] = dt;
         const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-        const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
-        const float2* c2 = reinterpret_cast<const float2*>(bc + k * 2 * N + N + nb);
+        float2 b2[P2], c2[P2];
+        load_pairs<P2>(bc + k * 2 * N + nb, b2);
+        load_pairs<P2>(bc + k * 2 * N + N + nb, c2);
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < P2; ++q) {
@@ -340,8 +361,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       }
       dD_acc = fmaf(dv, x, dD_acc);
       const float2 dv2 = make_float2(dv, dv), dt2 = make_float2(dt, dt), x2 = make_float2(x, x);
-      const float2* b2 = reinterpret_cast<const float2*>(bc + k * 2 * N + nb);
-      const float2* c2 = reinterpret_cast<const float2*>(bc + k * 2 * N + N + nb);
+      float2 b2[P2], c2[P2];
+      load_pairs<P2>(bc + k * 2 * N + nb, b2);
+      load_pairs<P2>(bc + k * 2 * N + N + nb, c2);
       float2 dux2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
       float vb[NH], vc[NH];
 #pragma unroll
