@@ -626,17 +626,21 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_state_walk_kernel(const Ss
 //   workers: form w B of chunk c (bf16 high + low) in stage c % 2 and signal full; then,
 //     for chunk c - 1, load its MMA result from TMEM (one
 //     state row per thread: warp w has TMEM lanes 32 w .. 32 w + 31), write the entering
-//     state (bf16, fragment order) for the read-out, update the fp32 state registers
+//     state (bf16, the read-out's K-major image), update the fp32 state registers
 //     S <- exp(cs_end) S + S_c and release the TMEM buffer;
-//   MMA thread: S_c = X^T (w B) as 8 tcgen05.mma (M = 128 state rows, N = 32 state
-//     columns, K = 16 steps; high and low parts of w B) into TMEM buffer c % 2, then
-//     commit to the buffer's full barrier and to the stage's empty barrier.
+//   MMA thread: X^T [w B high | w B low] as 4 tcgen05.mma (M = 128 state rows, N = 64:
+//     the 32 state columns of the high part beside those of the low part, K = 16 steps)
+//     into TMEM buffer c % 2 (the workers add the two halves: S_c = X^T w B), then commit
+//     to the buffer's full barrier and to the stage's empty barrier. Side by side, one MMA
+//     reads each X tile once, halving the tensor core's time per chunk (three CTAs per SM
+//     share it).
 // So the MMA of chunk c runs while the workers finish chunk c - 1 and start chunk c + 1.
 // X is an MN-major operand with the 128-byte swizzle (a 128-byte row = 64 state rows of
 // one step; 8 steps per 1 KB atom; the descriptor's LBO is the distance between atoms along
 // M and its SBO the distance between atoms along K; measured on B300 against a host
 // product), so TMA moves 128-byte rows. w B is an MN-major operand without swizzle (16-byte
-// rows of 8 bf16 along the state columns, 8 steps per core matrix). Steps past L in a
+// rows of 8 bf16 along the state columns, 8 steps per core matrix; core matrices (n8, t8)
+// at n8 * 128 + t8 * 1024, n8 0-3 the high part and 4-7 the low part). Steps past L in a
 // batch row's last chunk are zeroed (X) or masked (w B) after the copy, so the next row's
 // data never enters. Every wait is bounded; one that runs out raises a CTA-wide abort flag
 // that ends every role's loop.
@@ -647,9 +651,8 @@ template <int N>
 struct SsdTcWalk {
   static constexpr int kX = 0;                            // X: [p half][t][64 p] swizzled, 16 KB
   static constexpr int kB = kX + kSsdQ * kTcP * 2;        // raw B, [t][32 columns], 4 KB
-  static constexpr int kWh = kB + kSsdQ * kSsdNB * 2;     // w B high: 4 x 8 core matrices (n8, t8), 4 KB
-  static constexpr int kWl = kWh + kSsdQ * kSsdNB * 2;    // w B low
-  static constexpr int kDt = kWl + kSsdQ * kSsdNB * 2;    // dt [Q]
+  static constexpr int kW = kB + kSsdQ * kSsdNB * 2;      // [w B high | w B low]: 8 x 8 core matrices (n8, t8), 8 KB
+  static constexpr int kDt = kW + 2 * kSsdQ * kSsdNB * 2; // dt [Q]
   static constexpr int kCs = kDt + kSsdQ * 4;             // cs [Q]
   static constexpr int kStage = (kCs + kSsdQ * 4 + 1023) / 1024 * 1024;  // swizzle atoms 1 KB aligned
   static constexpr int kBar = 2 * kStage;                 // full, empty, tfull, tempty, loaded [2] each
@@ -657,8 +660,8 @@ struct SsdTcWalk {
   static constexpr int kAbort = kSlot + 4;
   static constexpr int kBytes = kAbort + 12 + 1024;       // + room to align the base to 1 KB
   // operand strides (bytes): X atoms (64 p x 8 t, 1 KB) at p-half * 8192 + t8 * 1024; w B core
-  // matrix (n8, t8) at n8 * 128 + t8 * 512
-  static constexpr uint32_t kXlbo = 8192, kXsbo = 1024, kWlbo = 512, kWsbo = 128;
+  // matrix (n8, t8) at n8 * 128 + t8 * 1024
+  static constexpr uint32_t kXlbo = 8192, kXsbo = 1024, kWlbo = 1024, kWsbo = 128;
 };
 
 // Bounded wait on a barrier phase that also gives up once another role has aborted.
@@ -693,7 +696,7 @@ __global__ void __launch_bounds__(kTcThreads)
                              const SsdParams p) {
   using L = SsdTcWalk<N>;
   constexpr int Q = kSsdQ, P = kTcP, NB = kSsdNB;
-  constexpr uint32_t kIdesc = umma_idesc_bf16(P, NB, true, true);
+  constexpr uint32_t kIdesc = umma_idesc_bf16(P, 2 * NB, true, true);  // N: high and low columns
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem_raw = smem_dyn + ((1024u - (umma_saddr(smem_dyn) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L::kBar);
@@ -722,7 +725,7 @@ __global__ void __launch_bounds__(kTcThreads)
     *abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(slot, 64);
+  if (warp == 0) tmem_alloc(slot, 128);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -757,13 +760,12 @@ __global__ void __launch_bounds__(kTcThreads)
         if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort)) break;
         tc_fence_after();
         const unsigned char* st = smem_raw + s * L::kStage;
-        const uint32_t xa = umma_saddr(st + L::kX), wh = umma_saddr(st + L::kWh), wl = umma_saddr(st + L::kWl);
-        const uint32_t d = tmem + 32u * (uint32_t)s;
+        const uint32_t xa = umma_saddr(st + L::kX), wa = umma_saddr(st + L::kW);
+        const uint32_t d = tmem + 64u * (uint32_t)s;
 #pragma unroll
         for (int ks = 0; ks < Q / 16; ++ks) {
           const uint64_t ad = umma_sdesc(xa + ks * 2 * L::kXsbo, L::kXlbo, L::kXsbo, 2);
-          umma_bf16(d, ad, umma_sdesc(wh + ks * 2 * L::kWlbo, L::kWlbo, L::kWsbo), kIdesc, ks > 0);
-          umma_bf16(d, ad, umma_sdesc(wl + ks * 2 * L::kWlbo, L::kWlbo, L::kWsbo), kIdesc, true);
+          umma_bf16(d, ad, umma_sdesc(wa + ks * 2 * L::kWlbo, L::kWlbo, L::kWsbo), kIdesc, ks > 0);
         }
         umma_commit(&tfull[s]);
         umma_commit(&empty[s]);
@@ -790,14 +792,17 @@ __global__ void __launch_bounds__(kTcThreads)
       if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort)) return false;
       tc_fence_after();
       float Sc[NB];
-      {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 32u * (uint32_t)s, v);
+      {  // the high part's 32 columns, then the low part's
+        const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + 64u * (uint32_t)s;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) Sc[j] = v[j];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 32u * (uint32_t)s + 16u, v);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t hv[16], lv[16];
+          tmem_ld16_nowait(ta + 16u * hf, hv);
+          tmem_ld16_nowait(ta + 32u + 16u * hf, lv);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) Sc[16 + j] = v[j];
+          for (int j = 0; j < 16; ++j) Sc[16 * hf + j] = __uint_as_float(hv[j]) + __uint_as_float(lv[j]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty[s]);
@@ -857,8 +862,8 @@ __global__ void __launch_bounds__(kTcThreads)
             split_bf16x2(t < rv ? make_float2(v.x * w, v.y * w) : make_float2(0.f, 0.f), hi[k], lo[k]);
           }
           const int off = n8 * L::kWsbo + (t >> 3) * L::kWlbo + (t & 7) * 16;
-          *reinterpret_cast<uint4*>(st + L::kWh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(st + L::kWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(st + L::kW + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(st + L::kW + off + 4 * L::kWsbo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       fence_smem_to_async();
@@ -878,7 +883,7 @@ __global__ void __launch_bounds__(kTcThreads)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, 128);
   }
 }
 
