@@ -412,10 +412,16 @@ SSM_API const char* ssm_status_string(ssm_status_t status);
 
 /*
  * ssm_device_error -- diagnostic read of the library's device-side error word on the
- * current device. It SYNCHRONISES the given stream, returns the word in *code (0 = no
- * error; otherwise a kernel gave up a bounded wait) and clears it. Returns SSM_OK,
- * SSM_ERR_NULL (code == NULL) or SSM_ERR_CUDA. Kernels never trap: a wait that runs out
- * sets this word and returns.
+ * current device. It SYNCHRONISES the given stream, returns the word in *code and clears
+ * it. Returns SSM_OK, SSM_ERR_NULL (code == NULL) or SSM_ERR_CUDA. Kernels never trap: a
+ * wait that runs out records the first failure here and the kernel returns, leaving the
+ * context usable. Codes: 0 no error; 1 a TMA load never completed; 2 the consumers never
+ * released a staging buffer; 3 a converted B/C tile was never published; 4 a tensor-core
+ * MMA never signalled completion.
+ * The forward pass's bounded waits last about one second by default; the environment
+ * variable SSM_B300_WAIT_LIMIT_CYCLES sets another limit (in SM clock cycles), and
+ * SSM_B300_FAULT_INJECT=skip_loads makes the staging warp issue no copies, so that every
+ * wait for data runs out (used by the failure-detection tests only).
  */
 SSM_API ssm_status_t ssm_device_error(void* stream, int32_t* code);
 

@@ -46,6 +46,11 @@ struct FwdParams {
   const float* seg_h0;
   float* seg_E;
   float* seg_P;
+  // Failure detection (channel kernel): the limit of every bounded wait in cycles (0: the
+  // default of about one second), and a fault-injection switch for tests: when set, the
+  // TMA issuer issues no copy, so every wait for data runs out and reports its code.
+  long long wait_cycles;
+  int fault_skip_loads;
 };
 
 // ------------------------------------------------------------------------------------

@@ -242,6 +242,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   const int64_t t_begin = (int64_t)seg * p.seg_len;
   const int64_t t_end = (t_begin + p.seg_len) < L ? (t_begin + p.seg_len) : L;
   const int nchunks = (int)((t_end - t_begin + TC - 1) / TC);
+  const long long lim = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -254,7 +255,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   __syncthreads();
 
   if (warp == 4) {  // ---------------- TMA issuer ----------------
-    if (lane == 0) {
+    if (lane == 0 && !p.fault_skip_loads) {
       prefetch_tensormap(&tm_u);
       prefetch_tensormap(&tm_dl);
       if (kZ) prefetch_tensormap(&tm_z);
@@ -264,7 +265,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       int issued = 0;
       for (int k = 0; k < nchunks; ++k) {
         const int s = k % S;
-        if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, kErrWaitEmpty)) break;
+        if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, kErrWaitEmpty, lim)) break;
         unsigned char* st = smem + s * Lay::kStage;
         mbar_arrive_expect_tx(&full[s], tx);
         const int32_t t0 = (int32_t)(t_begin + (int64_t)k * TC), col = (int32_t)d0;
@@ -277,7 +278,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       }
       // Never leave with loads in flight into this CTA's shared memory.
       for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
-        if (!mbar_wait(&full[k % S], (k / S) & 1, kErrWaitFull)) break;
+        if (!mbar_wait(&full[k % S], (k / S) & 1, kErrWaitFull, lim)) break;
     }
     return;
   }
@@ -285,7 +286,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   if (warp == 5) {  // ---------------- B, C -> fp32 ----------------
     for (int k = 0; k < nchunks; ++k) {
       const int s = k % S;
-      if (!mbar_wait(&full[s], (k / S) & 1, kErrWaitFull)) return;
+      if (!mbar_wait(&full[s], (k / S) & 1, kErrWaitFull, lim)) return;
       const unsigned char* st = smem + s * Lay::kStage;
       const __nv_bfloat16* Bt = reinterpret_cast<const __nv_bfloat16*>(st + 3 * Lay::kTileIO);
       const __nv_bfloat16* Ct = reinterpret_cast<const __nv_bfloat16*>(st + 3 * Lay::kTileIO + Lay::kTileBC);
@@ -349,8 +350,8 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   for (int k = 0; k < nchunks; ++k) {
     const int s = k % S;
     const uint32_t par = (k / S) & 1;
-    if (!mbar_wait(&ready[s], par, kErrWaitReady)) break;
-    if (!mbar_wait(&full[s], par, kErrWaitFull)) break;
+    if (!mbar_wait(&ready[s], par, kErrWaitReady, lim)) break;
+    if (!mbar_wait(&full[s], par, kErrWaitFull, lim)) break;
     const unsigned char* st = smem + s * Lay::kStage;
     const __nv_bfloat16* su = reinterpret_cast<const __nv_bfloat16*>(st) + j;
     const __nv_bfloat16* sd = reinterpret_cast<const __nv_bfloat16*>(st + Lay::kTileIO) + j;

@@ -84,6 +84,21 @@ FwdVariant forward_variant() {
   return FwdVariant::kAuto;
 }
 
+// ---- failure detection ---------------------------------------------------------------
+// SSM_B300_WAIT_LIMIT_CYCLES: limit of the channel kernel's bounded waits (default about
+// one second). SSM_B300_FAULT_INJECT=skip_loads: the channel kernel's TMA issuer issues
+// nothing, so every wait for data runs out; only the failure-detection tests set it.
+long long wait_limit_cycles() {
+  const char* e = getenv("SSM_B300_WAIT_LIMIT_CYCLES");
+  if (!e) return 0;
+  const long long v = atoll(e);
+  return v > 0 ? v : 0;
+}
+int fault_skip_loads() {
+  const char* e = getenv("SSM_B300_FAULT_INJECT");
+  return (e && strcmp(e, "skip_loads") == 0) ? 1 : 0;
+}
+
 // ---- TMA descriptors -------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -447,6 +462,8 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.seg_len = L;
   p.seg_h0 = nullptr;
   p.seg_E = p.seg_P = nullptr;
+  p.wait_cycles = wait_limit_cycles();
+  p.fault_skip_loads = fault_skip_loads();
 
   cudaError_t e;
   const FwdVariant var = forward_variant();

@@ -56,12 +56,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the barrier's phase with the given parity has completed. Bounded.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int err) {
+// Wait until the barrier's phase with the given parity has completed. Bounded: after
+// `limit` cycles of polling the error code goes to g_ssm_error and the wait returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int err, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitCycles) {
+    if (clock64() - start > limit) {
       atomicCAS(&g_ssm_error, 0, err);
       return false;
     }

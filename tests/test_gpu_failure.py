@@ -1,0 +1,52 @@
+"""Failure detection on the GPU without a fault: a bounded wait that runs out.
+
+The channel kernel's waits on its mbarriers are bounded; a wait that runs out records an
+error code in the library's device error word and the kernel returns (no trap, no hang).
+Here the staging warp is told to issue no copies (SSM_B300_FAULT_INJECT=skip_loads) and
+the wait limit is cut to 2e5 cycles (about 0.1 ms), so every wait for data runs out. The
+test checks that the call returns, that ssm_device_error reports a "data never arrived"
+code, and that a following normal call on the same context is correct.
+"""
+import os
+
+import pytest
+import torch
+
+import oracle
+from parity import TOL_BF16, check
+from selective_state_space_141_b300 import inputs, ssm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _fwd(d):
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], y_dtype=torch.float32, use_workspace=False)
+    return y, last
+
+
+def test_wait_runs_out_and_context_recovers(monkeypatch):
+    d = inputs.random_fwd(2, 200, 256, 16, dtype=torch.bfloat16, device=DEV, seed=71)  # channel-kernel shape
+    assert ssm.device_error() == 0
+    monkeypatch.setenv("SSM_B300_FAULT_INJECT", "skip_loads")
+    monkeypatch.setenv("SSM_B300_WAIT_LIMIT_CYCLES", "200000")
+    _fwd(d)
+    code = ssm.device_error()  # synchronises; the kernel returned on its own
+    assert code in (1, 3), f"expected a 'data never arrived' code (1 or 3), got {code}"
+    monkeypatch.delenv("SSM_B300_FAULT_INJECT")
+    monkeypatch.delenv("SSM_B300_WAIT_LIMIT_CYCLES")
+    y, last = _fwd(d)
+    assert ssm.device_error() == 0
+    yr, sr = oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                       delta_bias=d["delta_bias"])
+    check(y, yr, TOL_BF16, False, "y after recovery")
+    check(last, sr, TOL_BF16, False, "last_state after recovery")
+
+
+def test_short_limit_alone_does_not_fire(monkeypatch):
+    """A short limit is still far above a healthy wait: no error without the fault."""
+    d = inputs.random_fwd(1, 300, 128, 16, dtype=torch.bfloat16, device=DEV, seed=72)
+    monkeypatch.setenv("SSM_B300_WAIT_LIMIT_CYCLES", "2000000")
+    _fwd(d)
+    assert ssm.device_error() == 0

@@ -2,18 +2,23 @@
 
 The no-allocation entry point is for callers that can only pass the buffers they own
 (a fixed memory budget, a plugin interface given just inputs and outputs, a path where
-an allocation must not stall or fail). It must give the same result as the entry point
-that takes a caller-owned workspace. The shape below takes the segmented schedule, so
-the built-in scratch array is really used; two calls in a row with different inputs
-also check that the second call does not depend on what the first left in the array.
+an allocation must not stall or fail). It runs the same kernels as the entry point that
+takes a caller-owned workspace, so the two results must be identical bit for bit; that
+equality also shows the no-allocation call took the segmented schedule (the unsegmented
+kernel associates the recurrence differently and would differ in the last bits). The
+shape below takes the segmented schedule, so the built-in scratch array is really used;
+two calls in a row with different inputs check that the second call does not depend on
+what the first left in the array, and the first is also compared with the oracle on
+sampled channels.
 """
 import ctypes
 
 import pytest
 import torch
 
-from parity import TOL_BF16, check
+from parity import TOL_BF16
 from selective_state_space_141_b300 import inputs, ssm
+from test_gpu_fwd import check_sampled, sample_channels
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -44,5 +49,8 @@ def test_noalloc_matches_workspace_entry_point():
                                                delta_bias=d["delta_bias"], y_dtype=torch.float32)
         torch.cuda.synchronize()
         assert ssm.device_error() == 0
-        check(y, y_ws, TOL_BF16, False, f"y (seed {seed})")
-        check(last, last_ws, TOL_BF16, False, f"last_state (seed {seed})")
+        assert torch.equal(y, y_ws), f"y differs from the workspace entry point (seed {seed})"
+        assert torch.equal(last, last_ws), f"last_state differs from the workspace entry point (seed {seed})"
+        if seed == 301:
+            ref = sample_channels(d, per_row=16, rows=1, seed=seed)
+            check_sampled(y, last, ref, TOL_BF16, False, "noalloc vs oracle")
