@@ -46,12 +46,51 @@ struct FwdParams {
   const float* seg_h0;
   float* seg_E;
   float* seg_P;
+  // Segment scratch kept in the output (channel kernel): when seg_y is set, seg_h0 /
+  // seg_E / seg_P are not used; the start state, end state and decay product of segment
+  // s for channel d live in y itself, in column d of the segment's first rows (see
+  // seg_slot), which the segment's own full pass overwrites with y afterwards.
+  void* seg_y;
+  int seg_y_bf16;
   // Failure detection (channel kernel): the limit of every bounded wait in cycles (0: the
   // default of about one second), and a fault-injection switch for tests: when set, the
   // TMA issuer issues no copy, so every wait for data runs out and reports its code.
   long long wait_cycles;
   int fault_skip_loads;
 };
+
+// Segment scratch inside y: value `kind` (0 start state H, 1 end state E, 2 decay product
+// P) of state n, channel d, batch row b, segment s sits in column d of y at rows
+// s * seg_len + kind * N + n (fp32 y), or as two bf16-sized halves (high, low 16 bits of
+// the fp32 value) at rows s * seg_len + 2 (kind * N + n) + {0, 1} (bf16 y). Every value
+// of a channel stays in that channel's own column and segment, which only the CTA that
+// owns both touches, so no two CTAs of a pass share scratch. Needs seg_len >= 6 N rows.
+struct SegY {
+  void* y;
+  int bf16;
+  int64_t L, D, seg_len;
+  int N;
+};
+__device__ __forceinline__ void seg_slot_store(const SegY& q, int kind, int64_t s, int64_t b, int64_t d, int n,
+                                               float v) {
+  const int64_t r = s * q.seg_len + (int64_t)(kind * q.N + n) * (q.bf16 ? 2 : 1);
+  if (q.bf16) {
+    unsigned short* y = static_cast<unsigned short*>(q.y) + (b * q.L + r) * q.D + d;
+    const uint32_t w = __float_as_uint(v);
+    y[0] = (unsigned short)(w >> 16);
+    y[q.D] = (unsigned short)(w & 0xffffu);
+  } else {
+    static_cast<float*>(q.y)[(b * q.L + r) * q.D + d] = v;
+  }
+}
+__device__ __forceinline__ float seg_slot_load(const SegY& q, int kind, int64_t s, int64_t b, int64_t d, int n) {
+  const int64_t r = s * q.seg_len + (int64_t)(kind * q.N + n) * (q.bf16 ? 2 : 1);
+  if (q.bf16) {
+    const unsigned short* y = static_cast<const unsigned short*>(q.y) + (b * q.L + r) * q.D + d;
+    return __uint_as_float(((uint32_t)y[0] << 16) | (uint32_t)y[q.D]);
+  }
+  return static_cast<const float*>(q.y)[(b * q.L + r) * q.D + d];
+}
 
 // ------------------------------------------------------------------------------------
 // Generic kernel: any D, any L, fp32 or bf16 I/O. Channel-parallel: a group of

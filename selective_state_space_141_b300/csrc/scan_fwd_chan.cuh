@@ -311,13 +311,17 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   const int64_t d = d0 + j;
   const bool vd = d < D;
   const int64_t sidx = (((int64_t)seg * p.batch + b) * D + d) * N;  // [segment][batch][D][N]
+  const SegY sy{p.seg_y, p.seg_y_bf16, L, D, p.seg_len, N};
   float2 A2[N / 2], h[N / 2];
 #pragma unroll
   for (int q = 0; q < N / 2; ++q) {
     A2[q] = vd ? make_float2(p.A[d * N + 2 * q] * kLog2e, p.A[d * N + 2 * q + 1] * kLog2e)
                : make_float2(0.f, 0.f);
-    h[q] = (vd && p.seg_h0) ? make_float2(p.seg_h0[sidx + 2 * q], p.seg_h0[sidx + 2 * q + 1])
-                            : make_float2(0.f, 0.f);
+    if (vd && p.seg_y && !kAgg)  // start state from this segment's rows of y (read before any y store)
+      h[q] = make_float2(seg_slot_load(sy, 0, seg, b, d, 2 * q), seg_slot_load(sy, 0, seg, b, d, 2 * q + 1));
+    else
+      h[q] = (vd && p.seg_h0) ? make_float2(p.seg_h0[sidx + 2 * q], p.seg_h0[sidx + 2 * q + 1])
+                              : make_float2(0.f, 0.f);
   }
   const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
@@ -396,7 +400,15 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
   }
 
   if (kAgg) {
-    if (vd) {
+    if (vd && p.seg_y) {
+#pragma unroll
+      for (int q = 0; q < N / 2; ++q) {
+        seg_slot_store(sy, 1, seg, b, d, 2 * q, h[q].x);
+        seg_slot_store(sy, 1, seg, b, d, 2 * q + 1, h[q].y);
+        seg_slot_store(sy, 2, seg, b, d, 2 * q, ex2(A2[q].x * sdt));
+        seg_slot_store(sy, 2, seg, b, d, 2 * q + 1, ex2(A2[q].y * sdt));
+      }
+    } else if (vd) {
       float4* e4 = reinterpret_cast<float4*>(p.seg_E + sidx);
       float4* p4 = reinterpret_cast<float4*>(p.seg_P + sidx);
 #pragma unroll
@@ -426,6 +438,32 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
 // ("8.7 State Space Models (Mamba)", section 4.1 and "Mamba and State Space Models",
 // "Hardware-Aware Parallel Scan": the recurrence is an associative scan.)
 // Requires nseg <= 32. Layout of E, P, H: [segment][batch * D * N]; h0: [batch * D * N].
+// The same scan with the segment values kept in y (SegY): one warp per (batch, channel,
+// state), index idx = (b * D + d) * N + n.
+__global__ void __launch_bounds__(256) seg_carry_y_kernel(const SegY sy, const float* __restrict__ h0, int nseg,
+                                                          int64_t nbdn) {
+  const int64_t idx = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (idx >= nbdn) return;  // whole warps leave together
+  const int n = (int)(idx % sy.N);
+  const int64_t d = (idx / sy.N) % sy.D, b = idx / ((int64_t)sy.N * sy.D);
+  float a = 1.f, c = (lane == 0 && h0) ? h0[idx] : 0.f;
+  if (lane >= 1 && lane < nseg) {
+    a = seg_slot_load(sy, 2, lane - 1, b, d, n);
+    c = seg_slot_load(sy, 1, lane - 1, b, d, n);
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a_up = __shfl_up_sync(0xffffffffu, a, off);
+    const float c_up = __shfl_up_sync(0xffffffffu, c, off);
+    if (lane >= off) {  // (a_up, c_up) o (a, c)
+      c = fmaf(a, c_up, c);
+      a = a * a_up;
+    }
+  }
+  if (lane < nseg) seg_slot_store(sy, 0, lane, b, d, n, c);
+}
+
 __global__ void __launch_bounds__(256) seg_carry_kernel(const float* __restrict__ E, const float* __restrict__ P,
                                                        const float* __restrict__ h0, float* __restrict__ H, int nseg,
                                                        int64_t nbdn) {

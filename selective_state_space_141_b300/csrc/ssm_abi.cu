@@ -234,7 +234,24 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
   p.seg_h0 = p0.h0;  // one segment: the caller's start state (or zeros)
   p.seg_E = p.seg_P = nullptr;
   int nseg = 1;
-  if (plan.nseg > 1 && ws) {
+  if (plan.nseg > 1 && !ws) {
+    // No workspace: the segment values live in y itself (SegY), each in its channel's
+    // column of its segment's first rows, until the full pass overwrites them.
+    nseg = plan.nseg;
+    p.seg_len = plan.seg_len;
+    p.seg_h0 = nullptr;
+    p.seg_y = p0.y;
+    p.seg_y_bf16 = sizeof(TY) == 2 ? 1 : 0;
+    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
+    if (e != cudaSuccess) return e;
+    const ssm::SegY sy{p0.y, p.seg_y_bf16, p0.L, p0.D, plan.seg_len, N};
+    const int64_t nbdn = p0.batch * p0.D * N;
+    const float* h0 = p0.h0;
+    void* cargs[] = {const_cast<ssm::SegY*>(&sy), &h0, &nseg, const_cast<int64_t*>(&nbdn)};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_y_kernel), dim3((unsigned)((nbdn + 7) / 8)),
+                         dim3(256), cargs, 0, st);
+    if (e != cudaSuccess) return e;
+  } else if (plan.nseg > 1 && ws) {
     // 1) aggregate pass over segments 0 .. nseg-2; 2) carry scan; 3) full pass.
     const int64_t stride = (int64_t)plan.nseg * p0.batch * p0.D * N;
     float* E = static_cast<float*>(ws);
@@ -462,6 +479,8 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.seg_len = L;
   p.seg_h0 = nullptr;
   p.seg_E = p.seg_P = nullptr;
+  p.seg_y = nullptr;
+  p.seg_y_bf16 = 0;
   p.wait_cycles = wait_limit_cycles();
   p.fault_skip_loads = fault_skip_loads();
 
@@ -471,7 +490,10 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     SegPlan plan = plan_segments(batch, L, Dm, N);
     const bool use_ws = plan.nseg > 1 && workspace && workspace_bytes >= plan.bytes &&
                         reinterpret_cast<uintptr_t>(workspace) % 16 == 0;
-    if (!use_ws) plan = SegPlan{1, L, 0};
+    // Without a (large enough) workspace the segments keep their values in y, which needs
+    // 6 N rows per segment (3 N for fp32 y); otherwise one segment.
+    const int64_t rows = (y->dtype == SSM_BF16 ? 6 : 3) * N;
+    if (!use_ws && (plan.nseg <= 1 || plan.seg_len < rows)) plan = SegPlan{1, L, 0};
     bool launched = false;
     e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, plan, use_ws ? workspace : nullptr, st, &launched)
                              : launch_chan_n<float>(N, p, plan, use_ws ? workspace : nullptr, st, &launched);

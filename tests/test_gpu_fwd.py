@@ -263,3 +263,58 @@ def test_workspace_too_small_falls_back():
     torch.cuda.synchronize()
     yr, sr = oracle_fwd(d)
     check(y, yr, TOL_BF16, False, "fallback y")
+
+
+# ---- the time-split schedule through the plain entry point (no workspace) -------------------
+
+def test_long_sequence_plain_call_sampled():
+    """The long sequence through ssm_selective_scan_fwd itself: no workspace, so the
+    segmented schedule keeps its carries in y; sampled channels against the oracle."""
+    d = inputs.fwd_inputs(inputs.LONG, DEV)
+    assert ssm.workspace_size(1, inputs.LONG.L, inputs.LONG.D, 16) > 0, "the shape must segment"
+    ref = sample_channels(d, per_row=32, rows=1, seed=14)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], use_workspace=False)
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    check_sampled(y, last, ref, TOL_BF16, True, "long (plain call)")
+    y_ws, last_ws = gpu_fwd(d)
+    assert torch.equal(y, y_ws) and torch.equal(last, last_ws), "plain call differs from the workspace schedule"
+
+
+def test_long_sequence_plain_call_lti_vs_convolution():
+    d = inputs.fwd_inputs(inputs.LONG, DEV, lti=True)
+    y, _ = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                  delta_bias=d["delta_bias"], y_dtype=torch.float32, use_workspace=False)
+    torch.cuda.synchronize()
+    T = 4096
+    rng = np.random.default_rng(15)
+    A, B0, C0 = to64(d["A"]), to64(d["B"][0, 0]), to64(d["C"][0, 0])
+    bias, Dk = to64(d["delta_bias"]), to64(d["D"])
+    u, z, raw = to64(d["u"][0, :T]), to64(d["z"][0, :T]), to64(d["delta"][0, 0])
+    yg = to64(y[0, :T])
+    for dd in rng.choice(inputs.LONG.D, size=8, replace=False):
+        dt = np.logaddexp(0.0, raw[dd] + bias[dd])
+        K = (C0 * np.exp(np.arange(T)[:, None] * dt * A[dd]) * dt * B0).sum(-1)
+        ref = (np.convolve(u[:, dd], K)[:T] + Dk[dd] * u[:, dd]) * z[:, dd] * expit(z[:, dd])
+        check(yg[:, dd], ref, TOL_BF16, False, f"lti channel {dd} (plain call)")
+
+
+@pytest.mark.parametrize("y_dtype", [torch.bfloat16, torch.float32], ids=["bf16y", "f32y"])
+@pytest.mark.parametrize("shape", [(1, 20000, 256, 16), (2, 9000, 128, 8), (1, 12001, 64, 16)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_plain_call_segments_vs_oracle(shape, y_dtype):
+    """Shapes with few channels and long sequences segment without a workspace; whole
+    tensors against the oracle (ragged last segment and chunk), h0 included."""
+    b, L, D, N = shape
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=torch.bfloat16, seed=L + D))
+    assert ssm.workspace_size(b, L, D, N) > 0, "the shape must segment"
+    h0 = torch.randn(b, D, N, generator=torch.Generator().manual_seed(5)).to(DEV)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], y_dtype=y_dtype, use_workspace=False, h0=h0)
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    yr, sr = oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                       delta_bias=d["delta_bias"], h0=h0)
+    check(y, yr, TOL_BF16, y_dtype == torch.bfloat16, "y")
+    check(last, sr, TOL_BF16, False, "last_state")
