@@ -104,6 +104,16 @@ typedef enum {
  *   stream                    cudaStream_t
  * batch == 0 or L == 0 is a valid no-op; with L == 0 a non-NULL last_state is zeroed.
  * The per-step state never reaches global memory.
+ * Long sequences over few channels (too few channel blocks to fill the GPU) run as
+ * parallel sequence segments: an aggregate pass gives each segment's end state from zero
+ * and its decay product exp(A * sum of dt), a warp scan with the associative operator
+ * (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) gives every segment its start state ("8.7
+ * State Space Models (Mamba)", section 4.1), and the full pass produces y. Without a
+ * workspace those per-segment values live in y itself (each channel's own column of its
+ * segment's first rows, overwritten by the full pass), so nothing is allocated. Segments
+ * reassociate the recurrence (equal up to rounding); SSM_B300_SEGMENTS=0 in the
+ * environment turns them off, for callers who need a prefix plus its continuation to
+ * reproduce one pass bit for bit.
  */
 SSM_API ssm_status_t ssm_selective_scan_fwd(const ssm_tensor_t* u, const ssm_tensor_t* delta,
                                     const ssm_tensor_t* A, const ssm_tensor_t* B,

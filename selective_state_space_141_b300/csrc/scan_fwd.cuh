@@ -101,7 +101,11 @@ __device__ __forceinline__ float seg_slot_load(const SegY& q, int kind, int64_t 
 //   finish : y = sum of partials + D u, gated, stored
 // ------------------------------------------------------------------------------------
 // kZOH: B-bar = (exp(dt A) - 1) / A B (zero-order hold) instead of dt B.
-template <typename T, typename TY, int N, int SPL, int DT, int TC, bool kZOH>
+// kAgg: the aggregate pass of a segmented scan over CTA z's sequence segment (end state
+// from zero and decay product into y's segment rows, see SegY; no outputs).
+// Segments: blockIdx.z covers steps [z * seg_len, (z + 1) * seg_len); with seg_y set the
+// full pass starts each segment from the start state the carry scan left in y.
+template <typename T, typename TY, int N, int SPL, int DT, int TC, bool kZOH, bool kAgg = false>
 __global__ void __launch_bounds__(DT*(N / SPL))
 scan_fwd_generic(const FwdParams p) {
   constexpr int LPC = N / SPL;
@@ -129,16 +133,24 @@ scan_fwd_generic(const FwdParams p) {
   TY* __restrict__ y = static_cast<TY*>(p.y) + b * L * D;
 
   constexpr bool kAccurate = sizeof(T) == 4;  // fp32 I/O: near-correctly-rounded decay
+  const int64_t seg = blockIdx.z;
+  const int64_t seg_len = p.seg_y ? p.seg_len : L;
+  const int64_t t_begin = seg * seg_len;
+  const int64_t t_end = (t_begin + seg_len) < L ? (t_begin + seg_len) : L;
+  const SegY sy{p.seg_y, p.seg_y_bf16, L, D, seg_len, N};
+  double sdt = 0.0;  // kAgg: sum of dt over the segment
   float Av[SPL], A2[SPL], h[SPL];
 #pragma unroll
   for (int k = 0; k < SPL; ++k) {
     Av[k] = vj ? p.A[dj * N + g * SPL + k] : 0.f;
     A2[k] = Av[k] * kLog2e;
-    h[k] = (vj && p.h0) ? p.h0[(b * D + dj) * N + g * SPL + k] : 0.f;
+    if (kAgg) h[k] = 0.f;
+    else if (p.seg_y) h[k] = vj ? seg_slot_load(sy, 0, seg, b, dj, g * SPL + k) : 0.f;
+    else h[k] = (vj && p.h0) ? p.h0[(b * D + dj) * N + g * SPL + k] : 0.f;
   }
 
-  for (int64_t t0 = 0; t0 < L; t0 += TC) {
-    const int tc = (int)((L - t0) < TC ? (L - t0) : TC);
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += TC) {
+    const int tc = (int)((t_end - t0) < TC ? (t_end - t0) : TC);
     for (int i = tid; i < TC * DT; i += NT) {
       const int t = i / DT, jj = i % DT;
       const int64_t d = d0 + jj;
@@ -185,6 +197,7 @@ scan_fwd_generic(const FwdParams p) {
 
     for (int t = 0; t < tc; ++t) {
       const float2 dd = sDD[t][j];
+      if (kAgg) sdt += (double)dd.x;
       float acc = 0.f;
 #pragma unroll
       for (int k = 0; k < SPL; ++k) {
@@ -201,7 +214,7 @@ scan_fwd_generic(const FwdParams p) {
     for (int i = tid; i < TC * DT; i += NT) {
       const int t = i / DT, jj = i % DT;
       const int64_t d = d0 + jj;
-      if (t < tc && d < D) {
+      if (!kAgg && t < tc && d < D) {
         float v = 0.f;
 #pragma unroll
         for (int q = 0; q < LPC; ++q) v += sP[t][jj * LPC + q];
@@ -213,7 +226,18 @@ scan_fwd_generic(const FwdParams p) {
     __syncthreads();
   }
 
-  if (vj && p.last_state) {
+  if (kAgg) {  // end state from zero and decay product exp(A * sum dt) of the segment
+    if (vj) {
+#pragma unroll
+      for (int k = 0; k < SPL; ++k) {
+        seg_slot_store(sy, 1, seg, b, dj, g * SPL + k, h[k]);
+        seg_slot_store(sy, 2, seg, b, dj, g * SPL + k,
+                       kAccurate ? (float)exp((double)Av[k] * sdt) : ex2(A2[k] * (float)sdt));
+      }
+    }
+    return;
+  }
+  if (vj && p.last_state && seg == (int64_t)gridDim.z - 1) {
 #pragma unroll
     for (int k = 0; k < SPL; ++k) p.last_state[(b * D + dj) * N + g * SPL + k] = h[k];
   }

@@ -165,6 +165,33 @@ int num_sms() {
   return n;
 }
 
+// Segment length for nseg segments of a sequence of L steps: a multiple of the chunk tc,
+// at least min_len, and with a last segment of at least `rows` steps (the segments keep
+// their carries in their own first rows of y). Lowers nseg until that holds; returns the
+// number of segments (< 2: do not segment) and the length in *len.
+// SSM_B300_SEGMENTS=0 turns segmentation off: every pass then runs each recurrence in
+// order from its start state, so splitting a sequence into a prefix and its continuation
+// reproduces one pass bit for bit (segments reassociate the recurrence: equal up to
+// rounding).
+bool segments_enabled() {
+  const char* e = getenv("SSM_B300_SEGMENTS");
+  return !(e && strcmp(e, "0") == 0);
+}
+
+int64_t fit_segments(int64_t L, int64_t nseg, int64_t tc, int64_t min_len, int64_t rows, int64_t* len) {
+  if (!segments_enabled()) return 1;
+  for (; nseg >= 2; --nseg) {
+    int64_t l = ((L + nseg - 1) / nseg + tc - 1) / tc * tc;
+    if (l < min_len) l = min_len;
+    const int64_t n = (L + l - 1) / l;
+    if (n >= 2 && L - (n - 1) * l >= rows) {
+      *len = l;
+      return n;
+    }
+  }
+  return 1;
+}
+
 // Sequence segmentation for shapes with too few channel blocks to occupy the GPU: the
 // long sequence is cut into nseg segments of seg_len steps (a multiple of the chunk),
 // each processed by its own CTAs; the workspace holds E, P and H ([nseg][batch][D][N]
@@ -183,9 +210,9 @@ SegPlan plan_segments(int64_t batch, int64_t L, int64_t D, int64_t N) {
   int64_t nseg = sms / ctas;
   if (nseg > 32) nseg = 32;  // one warp scans the segment carries
   if (nseg < 2) return sp;
-  const int64_t len = ((L + nseg - 1) / nseg + kChanTC - 1) / kChanTC * kChanTC;
-  if (len < 8 * kChanTC) return sp;  // too short to pay for the aggregate pass
-  nseg = (L + len - 1) / len;
+  if (((L + nseg - 1) / nseg + kChanTC - 1) / kChanTC * kChanTC < 8 * kChanTC) return sp;  // too short to pay
+  int64_t len = L;
+  nseg = fit_segments(L, nseg, kChanTC, 8 * kChanTC, 6 * N, &len);
   if (nseg < 2) return sp;
   sp.nseg = (int)nseg;
   sp.seg_len = len;
@@ -284,23 +311,69 @@ cudaError_t launch_chan_n(int64_t N, const FwdParams& p, const SegPlan& plan, vo
 }
 
 // ---- generic forward launch ------------------------------------------------------------
-template <typename T, typename TY, int N>
-cudaError_t launch_fwd(const FwdParams& p, cudaStream_t st) {
-  constexpr int SPL = 4, DT = 32, TC = 32;
-  dim3 grid((unsigned)((p.D + DT - 1) / DT), (unsigned)p.batch);
-  dim3 block(DT * (N / SPL));
+constexpr int kGenDT = 32, kGenTC = 32;
+
+// Segments for the generic kernel (32 channels per CTA) when its channel blocks cannot
+// fill the GPU: at most 32 segments (one warp scans the carries), each at least two chunks
+// long and long enough to hold its carries in y (`rows` rows).
+SegPlan plan_generic_segments(int64_t batch, int64_t L, int64_t D, int64_t rows) {
+  SegPlan sp;
+  sp.seg_len = L;
+  const int sms = num_sms();
+  const int64_t ctas = ((D + kGenDT - 1) / kGenDT) * batch;
+  if (sms <= 0 || ctas <= 0 || ctas * 2 > sms) return sp;
+  int64_t nseg = sms / ctas;
+  if (nseg > 32) nseg = 32;
+  const int64_t min_len = ((rows > 2 * kGenTC ? rows : 2 * kGenTC) + kGenTC - 1) / kGenTC * kGenTC;
+  int64_t len = L;
+  nseg = fit_segments(L, nseg, kGenTC, min_len, rows, &len);
+  if (nseg < 2) return sp;
+  sp.nseg = (int)nseg;
+  sp.seg_len = len;
+  return sp;
+}
+
+template <typename T, typename TY, int N, bool kAgg>
+cudaError_t launch_fwd(const FwdParams& p, int nseg, cudaStream_t st) {
+  constexpr int SPL = 4;
+  dim3 grid((unsigned)((p.D + kGenDT - 1) / kGenDT), (unsigned)p.batch, (unsigned)nseg);
+  dim3 block(kGenDT * (N / SPL));
   void* args[] = {const_cast<FwdParams*>(&p)};
-  const void* kern = p.zoh ? reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC, true>)
-                           : reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, DT, TC, false>);
+  const void* kern =
+      p.zoh ? reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, kGenDT, kGenTC, true, kAgg>)
+            : reinterpret_cast<const void*>(&ssm::scan_fwd_generic<T, TY, N, SPL, kGenDT, kGenTC, false, kAgg>);
   return cudaLaunchKernel(kern, grid, block, args, 0, st);
+}
+
+// One pass, or, when the channel blocks are too few, the segmented schedule with its
+// carries in y: aggregate pass over segments 0 .. nseg-2, carry scan, full pass.
+template <typename T, typename TY, int N>
+cudaError_t launch_fwd_seg(const FwdParams& p0, cudaStream_t st) {
+  const SegPlan plan = plan_generic_segments(p0.batch, p0.L, p0.D, (sizeof(TY) == 2 ? 6 : 3) * N);
+  if (plan.nseg <= 1) return launch_fwd<T, TY, N, false>(p0, 1, st);
+  FwdParams p = p0;
+  p.seg_y = p0.y;
+  p.seg_y_bf16 = sizeof(TY) == 2 ? 1 : 0;
+  p.seg_len = plan.seg_len;
+  int nseg = plan.nseg;
+  cudaError_t e = launch_fwd<T, TY, N, true>(p, nseg - 1, st);
+  if (e != cudaSuccess) return e;
+  const ssm::SegY sy{p0.y, p.seg_y_bf16, p0.L, p0.D, plan.seg_len, N};
+  const int64_t nbdn = p0.batch * p0.D * N;
+  const float* h0 = p0.h0;
+  void* cargs[] = {const_cast<ssm::SegY*>(&sy), &h0, &nseg, const_cast<int64_t*>(&nbdn)};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_y_kernel), dim3((unsigned)((nbdn + 7) / 8)),
+                       dim3(256), cargs, 0, st);
+  if (e != cudaSuccess) return e;
+  return launch_fwd<T, TY, N, false>(p, nseg, st);
 }
 
 template <typename T, typename TY>
 cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
   switch (N) {
-    case 4: return launch_fwd<T, TY, 4>(p, st);
-    case 8: return launch_fwd<T, TY, 8>(p, st);
-    default: return launch_fwd<T, TY, 16>(p, st);
+    case 4: return launch_fwd_seg<T, TY, 4>(p, st);
+    case 8: return launch_fwd_seg<T, TY, 8>(p, st);
+    default: return launch_fwd_seg<T, TY, 16>(p, st);
   }
 }
 

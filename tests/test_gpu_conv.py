@@ -65,8 +65,10 @@ def test_conv_fwd_vs_oracle(shape, dtype, with_state):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("split", [1, 2, 3, 37, 64])
-def test_conv_chunked_prefill_is_bit_exact(dtype, split):
-    """prefix, then the rest from the carried conv state and SSM state == one pass."""
+def test_conv_chunked_prefill_is_bit_exact(dtype, split, monkeypatch):
+    """prefix, then the rest from the carried conv state and SSM state == one pass, bit
+    for bit with the sequence segments off (segments reassociate the recurrence)."""
+    monkeypatch.setenv("SSM_B300_SEGMENTS", "0")
     b, L, D, N = 2, 160, 256, 16
     d = conv_inputs(b, L, D, N, dtype, seed=72)
     cs_all = d["conv_state"].clone()

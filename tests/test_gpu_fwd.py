@@ -73,6 +73,22 @@ def test_tiny_fp32_full():
     check(last, sr, TOL_F32, False, "last_state")
 
 
+def test_tiny_fp32_time_split(monkeypatch):
+    """The tiny fp32 workload runs the time-split schedule (4 sequence segments: aggregate
+    pass, shuffle scan of the segment carries, full pass); both it and the single pass
+    (SSM_B300_SEGMENTS=0) match the oracle at 1e-5, and they differ in the last bits,
+    which shows the segments really ran."""
+    d = to_dev(inputs.fwd_inputs(inputs.TINY))
+    yr, sr = oracle_fwd(d)
+    y_seg, last_seg = gpu_fwd(d)
+    monkeypatch.setenv("SSM_B300_SEGMENTS", "0")
+    y_one, last_one = gpu_fwd(d)
+    for y, last, what in ((y_seg, last_seg, "segmented"), (y_one, last_one, "single pass")):
+        check(y, yr, TOL_F32, False, f"y ({what})")
+        check(last, sr, TOL_F32, False, f"last_state ({what})")
+    assert not torch.equal(y_seg, y_one), "expected the segmented schedule to reassociate the recurrence"
+
+
 @pytest.mark.parametrize("key", ["m130m", "m1p4b"])
 def test_layer_workloads_sampled(key):
     w = inputs.FWD_WORKLOADS[key]

@@ -63,13 +63,21 @@ def test_fwd_h0_vs_oracle(shape, dtype):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("split", [1, 37, 64, 199])
-def test_chunked_prefill_is_bit_exact(dtype, split):
-    """prefix, then the rest from the prefix's last_state == one pass (bitwise)."""
+def test_chunked_prefill_is_bit_exact(dtype, split, monkeypatch):
+    """prefix, then the rest from the prefix's last_state == one pass: bitwise with the
+    sequence segments off (SSM_B300_SEGMENTS=0), within tolerance with them."""
     b, L, D, N = 2, 256, 256, 16
     d = inputs.random_fwd(b, L, D, N, dtype, DEV, seed=43)
-    y_all, last_all = fwd(d)
     p = contiguous_slice(d, slice(0, split))
     r = contiguous_slice(d, slice(split, L))
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    y_seg, last_seg = fwd(d)
+    y1, mid = fwd(p)
+    y2, last2 = fwd(r, h0=mid)
+    check(torch.cat([y1, y2], dim=1), y_seg, tol, False, "prefix + rest vs one pass")
+    check(last2, last_seg, tol, False, "last_state")
+    monkeypatch.setenv("SSM_B300_SEGMENTS", "0")
+    y_all, last_all = fwd(d)
     y1, mid = fwd(p)
     y2, last2 = fwd(r, h0=mid)
     assert torch.equal(torch.cat([y1, y2], dim=1), y_all)
