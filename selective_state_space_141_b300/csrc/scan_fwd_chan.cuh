@@ -431,26 +431,42 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
 
 // Carry between sequence segments: for every (batch, channel, state) the segment
 // aggregates (P_s, E_s) are pairs of the recurrence h -> P h + E, combined in time order
-// by (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2). One warp per (batch, channel, state),
-// lane s holding segment s - 1 (lane 0 the start state: (1, h0), h0 = 0 when absent),
-// runs an inclusive Hillis-Steele scan with __shfl_up_sync; lane s then holds the state
-// at the start of segment s.
-// ("8.7 State Space Models (Mamba)", section 4.1 and "Mamba and State Space Models",
-// "Hardware-Aware Parallel Scan": the recurrence is an associative scan.)
-// Requires nseg <= 32. Layout of E, P, H: [segment][batch * D * N]; h0: [batch * D * N].
-// The same scan with the segment values kept in y (SegY): one warp per (batch, channel,
-// state), index idx = (b * D + d) * N + n.
-__global__ void __launch_bounds__(256) seg_carry_y_kernel(const SegY sy, const float* __restrict__ h0, int nseg,
-                                                          int64_t nbdn) {
-  const int64_t idx = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (idx >= nbdn) return;  // whole warps leave together
-  const int n = (int)(idx % sy.N);
-  const int64_t d = (idx / sy.N) % sy.D, b = idx / ((int64_t)sy.N * sy.D);
-  float a = 1.f, c = (lane == 0 && h0) ? h0[idx] : 0.f;
-  if (lane >= 1 && lane < nseg) {
-    a = seg_slot_load(sy, 2, lane - 1, b, d, n);
-    c = seg_slot_load(sy, 1, lane - 1, b, d, n);
+// by (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) ("8.7 State Space Models (Mamba)", section
+// 4.1 and "Mamba and State Space Models", "Hardware-Aware Parallel Scan": the recurrence
+// is an associative scan). Element e of an item's scan is (1, h0) for e = 0 (h0 = 0 when
+// absent) and segment e-1's aggregate otherwise; after an inclusive scan element e holds
+// the state at the start of segment e.
+//   * within a warp: a Hillis-Steele scan over 32 elements with __shfl_up_sync;
+//   * across warps (nseg > 32: up to 128 segments over 4 warps): each warp's total goes
+//     to shared memory and every warp composes the totals of the warps before it (the
+//     block carry), then applies that carry to its elements.
+// CTA of 128 threads; `wpi` warps per item (1, 2 or 4: ceil(nseg / 32)), 4 / wpi items
+// per CTA. kInY: the values live in y (SegY), else flat [segment][batch * D * N] arrays.
+template <bool kInY>
+__global__ void __launch_bounds__(128) seg_carry_kernel(const SegY sy, const float* __restrict__ E,
+                                                       const float* __restrict__ P, const float* __restrict__ h0,
+                                                       float* __restrict__ H, int nseg, int wpi, int64_t nbdn) {
+  __shared__ float2 tot[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wi = warp % wpi;  // warp within the item
+  const int64_t idx = (int64_t)blockIdx.x * (4 / wpi) + warp / wpi;
+  const bool valid = idx < nbdn;
+  const int e = wi * 32 + lane;  // scan element
+  int n = 0;
+  int64_t d = 0, b = 0;
+  if (kInY && valid) {
+    n = (int)(idx % sy.N);
+    d = (idx / sy.N) % sy.D;
+    b = idx / ((int64_t)sy.N * sy.D);
+  }
+  float a = 1.f, c = 0.f;
+  if (valid) {
+    if (e == 0) {
+      c = h0 ? h0[idx] : 0.f;
+    } else if (e < nseg) {
+      a = kInY ? seg_slot_load(sy, 2, e - 1, b, d, n) : P[(int64_t)(e - 1) * nbdn + idx];
+      c = kInY ? seg_slot_load(sy, 1, e - 1, b, d, n) : E[(int64_t)(e - 1) * nbdn + idx];
+    }
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -461,30 +477,21 @@ __global__ void __launch_bounds__(256) seg_carry_y_kernel(const SegY sy, const f
       a = a * a_up;
     }
   }
-  if (lane < nseg) seg_slot_store(sy, 0, lane, b, d, n, c);
-}
-
-__global__ void __launch_bounds__(256) seg_carry_kernel(const float* __restrict__ E, const float* __restrict__ P,
-                                                       const float* __restrict__ h0, float* __restrict__ H, int nseg,
-                                                       int64_t nbdn) {
-  const int64_t idx = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (idx >= nbdn) return;  // whole warps leave together
-  float a = 1.f, c = (lane == 0 && h0) ? h0[idx] : 0.f;
-  if (lane >= 1 && lane < nseg) {
-    a = P[(int64_t)(lane - 1) * nbdn + idx];
-    c = E[(int64_t)(lane - 1) * nbdn + idx];
-  }
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float a_up = __shfl_up_sync(0xffffffffu, a, off);
-    const float c_up = __shfl_up_sync(0xffffffffu, c, off);
-    if (lane >= off) {  // (a_up, c_up) o (a, c)
-      c = fmaf(a, c_up, c);
-      a = a * a_up;
+  if (wpi > 1) {  // block carry: compose the totals of this item's earlier warps
+    if (lane == 31) tot[warp] = make_float2(a, c);
+    __syncthreads();
+    float ca = 1.f, cc = 0.f;
+    for (int w = warp - wi; w < warp; ++w) {
+      const float2 t = tot[w];
+      cc = fmaf(t.x, cc, t.y);
+      ca *= t.x;
     }
+    c = fmaf(a, cc, c);
   }
-  if (lane < nseg) H[(int64_t)lane * nbdn + idx] = c;
+  if (valid && e < nseg) {
+    if (kInY) seg_slot_store(sy, 0, e, b, d, n, c);
+    else H[(int64_t)e * nbdn + idx] = c;
+  }
 }
 
 }  // namespace ssm

@@ -208,16 +208,28 @@ SegPlan plan_segments(int64_t batch, int64_t L, int64_t D, int64_t N) {
   const int64_t ctas = ((D + ssm::kChanCTA - 1) / ssm::kChanCTA) * batch;
   if (sms <= 0 || ctas <= 0 || ctas * 2 > sms) return sp;
   int64_t nseg = sms / ctas;
-  if (nseg > 32) nseg = 32;  // one warp scans the segment carries
+  if (nseg > 128) nseg = 128;  // the carry scan covers up to 4 warps x 32 segments
   if (nseg < 2) return sp;
-  if (((L + nseg - 1) / nseg + kChanTC - 1) / kChanTC * kChanTC < 8 * kChanTC) return sp;  // too short to pay
-  int64_t len = L;
+  int64_t len = L;  // segments of at least 8 chunks: shorter ones do not pay for the aggregate pass
   nseg = fit_segments(L, nseg, kChanTC, 8 * kChanTC, 6 * N, &len);
   if (nseg < 2) return sp;
   sp.nseg = (int)nseg;
   sp.seg_len = len;
   sp.bytes = (size_t)3 * nseg * batch * D * N * sizeof(float);
   return sp;
+}
+
+// The carry scan over segments (block carry across warps above 32 segments): values in
+// y (sy.y set) or in the flat workspace arrays E, P -> H.
+cudaError_t launch_carry(const ssm::SegY& sy, const float* E, const float* P, const float* h0, float* H, int nseg,
+                         int64_t nbdn, cudaStream_t st) {
+  int wpi = (nseg + 31) / 32;
+  if (wpi == 3) wpi = 4;
+  const int64_t per_cta = 4 / wpi;
+  void* args[] = {const_cast<ssm::SegY*>(&sy), &E, &P, &h0, &H, &nseg, &wpi, &nbdn};
+  const void* kern = sy.y ? reinterpret_cast<const void*>(&ssm::seg_carry_kernel<true>)
+                          : reinterpret_cast<const void*>(&ssm::seg_carry_kernel<false>);
+  return cudaLaunchKernel(kern, dim3((unsigned)((nbdn + per_cta - 1) / per_cta)), dim3(128), args, 0, st);
 }
 
 // Run-time switches (softplus, gate, conv prologue) to template arguments. The
@@ -272,11 +284,7 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
     if (e != cudaSuccess) return e;
     const ssm::SegY sy{p0.y, p.seg_y_bf16, p0.L, p0.D, plan.seg_len, N};
-    const int64_t nbdn = p0.batch * p0.D * N;
-    const float* h0 = p0.h0;
-    void* cargs[] = {const_cast<ssm::SegY*>(&sy), &h0, &nseg, const_cast<int64_t*>(&nbdn)};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_y_kernel), dim3((unsigned)((nbdn + 7) / 8)),
-                         dim3(256), cargs, 0, st);
+    e = launch_carry(sy, nullptr, nullptr, p0.h0, nullptr, nseg, p0.batch * p0.D * N, st);
     if (e != cudaSuccess) return e;
   } else if (plan.nseg > 1 && ws) {
     // 1) aggregate pass over segments 0 .. nseg-2; 2) carry scan; 3) full pass.
@@ -291,11 +299,7 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     p.seg_P = P;
     cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
     if (e != cudaSuccess) return e;
-    const int64_t nbdn = p0.batch * p0.D * N;
-    const float* h0 = p0.h0;
-    void* cargs[] = {&E, &P, &h0, &H, &nseg, const_cast<int64_t*>(&nbdn)};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_kernel), dim3((unsigned)((nbdn + 7) / 8)),
-                         dim3(256), cargs, 0, st);
+    e = launch_carry(ssm::SegY{}, E, P, p0.h0, H, nseg, p0.batch * p0.D * N, st);
     if (e != cudaSuccess) return e;
     p.seg_h0 = H;
     p.seg_E = p.seg_P = nullptr;
@@ -314,7 +318,7 @@ cudaError_t launch_chan_n(int64_t N, const FwdParams& p, const SegPlan& plan, vo
 constexpr int kGenDT = 32, kGenTC = 32;
 
 // Segments for the generic kernel (32 channels per CTA) when its channel blocks cannot
-// fill the GPU: at most 32 segments (one warp scans the carries), each at least two chunks
+// fill the GPU: at most 128 segments (the carry scan's four warps), each at least two chunks
 // long and long enough to hold its carries in y (`rows` rows).
 SegPlan plan_generic_segments(int64_t batch, int64_t L, int64_t D, int64_t rows) {
   SegPlan sp;
@@ -323,7 +327,7 @@ SegPlan plan_generic_segments(int64_t batch, int64_t L, int64_t D, int64_t rows)
   const int64_t ctas = ((D + kGenDT - 1) / kGenDT) * batch;
   if (sms <= 0 || ctas <= 0 || ctas * 2 > sms) return sp;
   int64_t nseg = sms / ctas;
-  if (nseg > 32) nseg = 32;
+  if (nseg > 128) nseg = 128;
   const int64_t min_len = ((rows > 2 * kGenTC ? rows : 2 * kGenTC) + kGenTC - 1) / kGenTC * kGenTC;
   int64_t len = L;
   nseg = fit_segments(L, nseg, kGenTC, min_len, rows, &len);
@@ -359,11 +363,7 @@ cudaError_t launch_fwd_seg(const FwdParams& p0, cudaStream_t st) {
   cudaError_t e = launch_fwd<T, TY, N, true>(p, nseg - 1, st);
   if (e != cudaSuccess) return e;
   const ssm::SegY sy{p0.y, p.seg_y_bf16, p0.L, p0.D, plan.seg_len, N};
-  const int64_t nbdn = p0.batch * p0.D * N;
-  const float* h0 = p0.h0;
-  void* cargs[] = {const_cast<ssm::SegY*>(&sy), &h0, &nseg, const_cast<int64_t*>(&nbdn)};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(&ssm::seg_carry_y_kernel), dim3((unsigned)((nbdn + 7) / 8)),
-                       dim3(256), cargs, 0, st);
+  e = launch_carry(sy, nullptr, nullptr, p0.h0, nullptr, nseg, p0.batch * p0.D * N, st);
   if (e != cudaSuccess) return e;
   return launch_fwd<T, TY, N, false>(p, nseg, st);
 }

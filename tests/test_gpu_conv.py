@@ -81,13 +81,17 @@ def test_conv_chunked_prefill_is_bit_exact(dtype, split, monkeypatch):
     assert torch.equal(cs, cs_all)
 
 
-def test_conv_segmented_schedule():
+def test_conv_segmented_schedule(monkeypatch):
     """Later segments take their first three conv inputs from x before their start."""
     b, L, D, N = 1, 16384, 256, 16
     assert ssm.workspace_size(b, L, D, N) > 0
     d = conv_inputs(b, L, D, N, torch.bfloat16, seed=73)
     y, last = gpu(d, d["conv_state"].clone(), y_dtype=torch.float32)
+    y_y, last_y = gpu(d, d["conv_state"].clone(), y_dtype=torch.float32, use_workspace=False)  # carries in y
+    assert torch.equal(y, y_y) and torch.equal(last, last_y)
+    monkeypatch.setenv("SSM_B300_SEGMENTS", "0")
     y_u, last_u = gpu(d, d["conv_state"].clone(), y_dtype=torch.float32, use_workspace=False)
+    monkeypatch.delenv("SSM_B300_SEGMENTS")
     check(y, y_u, TOL_BF16, False, "segmented vs unsegmented y")
     check(last, last_u, TOL_BF16, False, "segmented vs unsegmented last_state")
     ds = np.sort(np.random.default_rng(74).choice(D, size=10, replace=False))

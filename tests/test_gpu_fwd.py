@@ -317,7 +317,7 @@ def test_long_sequence_plain_call_lti_vs_convolution():
 
 
 @pytest.mark.parametrize("y_dtype", [torch.bfloat16, torch.float32], ids=["bf16y", "f32y"])
-@pytest.mark.parametrize("shape", [(1, 20000, 256, 16), (2, 9000, 128, 8), (1, 12001, 64, 16)],
+@pytest.mark.parametrize("shape", [(1, 20000, 256, 16), (2, 9000, 128, 8), (1, 12001, 64, 16), (1, 40000, 64, 16)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_plain_call_segments_vs_oracle(shape, y_dtype):
     """Shapes with few channels and long sequences segment without a workspace; whole
@@ -334,3 +334,21 @@ def test_plain_call_segments_vs_oracle(shape, y_dtype):
                                        delta_bias=d["delta_bias"], h0=h0)
     check(y, yr, TOL_BF16, y_dtype == torch.bfloat16, "y")
     check(last, sr, TOL_BF16, False, "last_state")
+
+
+@pytest.mark.parametrize("shape", [(1, 4096, 32, 16), (1, 2000, 64, 8), (2, 1500, 40, 4)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_fp32_segments_vs_oracle(shape, monkeypatch):
+    """fp32 I/O (generic kernel) split into 2 .. 64 sequence segments: the carry scan's
+    warps and their block carry, against the oracle at 1e-5, h0 included."""
+    b, L, D, N = shape
+    d = to_dev(inputs.random_fwd(b, L, D, N, dtype=torch.float32, seed=L + 3 * D))
+    h0 = torch.randn(b, D, N, generator=torch.Generator().manual_seed(6)).to(DEV)
+    yr, sr = oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                       delta_bias=d["delta_bias"], h0=h0)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     delta_bias=d["delta_bias"], h0=h0, use_workspace=False)
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    check(y, yr, TOL_F32, False, "y")
+    check(last, sr, TOL_F32, False, "last_state")
