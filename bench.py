@@ -336,10 +336,107 @@ def run_ours(args, w, ws, rank, local):
         result["backward"] = backward_bench(args, ssm, torch, w, d, dev, launch_ms)
     if not args.no_ssd:
         result["ssd"] = ssd_bench(args, ssm, torch, inputs, dev, peaks)
+    samples = {}
+    if not args.no_configs:
+        result["configs"], samples = configs_bench(args, ssm, torch, inputs, dev, alu_peak, hbm_peak)
+        if "decode" in result:
+            dec = result["decode"]
+            result["configs"]["decode"] = {"workload": dec["workload"], "us_per_step": dec["us_per_step"],
+                                           "GB/s": dec["GB/s"], "elem_per_s": dec["elem_per_s"],
+                                           "roofline": {"bound": "hbm", "frac": dec["hbm_frac"]}}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
+        if samples:
+            # the oracle on the configs' sampled channels: GPU output error from the same run
+            for key, e in sampled_oracle_errors(samples).items():
+                result["configs"][key]["oracle_check"] = e
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def configs_bench(args, ssm, torch, inputs, dev, alu_peak, hbm_peak):
+    """Every forward workload besides the headline one, each through the plain
+    ssm_selective_scan_fwd call (no workspace), and the decode workload: median of CUDA
+    event times per call, throughput and both roofline terms. Returns (objects, samples):
+    samples keep sampled channels' inputs and GPU outputs on the host for the oracle check
+    that the CPU-baseline leg runs."""
+    import numpy as np
+
+    out, samples = {}, {}
+    rng = np.random.default_rng(2024)
+    stream = torch.cuda.current_stream()
+    for key, reps in (("tiny", 50), ("m130m", 20), ("long", 8)):
+        w = inputs.FWD_WORKLOADS[key]
+        d = inputs.fwd_inputs(w, dev)
+        y = torch.empty_like(d["u"])
+        last = torch.empty(w.batch, w.D, w.N, dtype=torch.float32, device=dev)
+
+        def call():
+            ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                   delta_bias=d["delta_bias"], delta_softplus=w.delta_softplus, y=y,
+                                   last_state=last, stream=stream, use_workspace=False)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        if ssm.device_error() != 0:
+            raise RuntimeError(f"device error word set during the {key} timing")
+        ms = statistics.median(ts)
+        t_alu = w.element_steps / alu_peak * 1e3
+        t_hbm = w.compulsory_bytes() / (hbm_peak * 1e9) * 1e3
+        out[key] = {"workload": w.name, "call": "ssm_selective_scan_fwd (no workspace)", "ms": ms,
+                    "GB/s": w.compulsory_bytes() / (ms / 1e3) / 1e9, "elem_per_s": w.elems / (ms / 1e3),
+                    "roofline": {"t_alu_ms": t_alu, "t_hbm_ms": t_hbm, "bound": "alu" if t_alu >= t_hbm else "hbm",
+                                 "frac": max(t_alu, t_hbm) / ms},
+                    "io": "fp32" if w.dtype == torch.float32 else "bf16", "reps": reps,
+                    "segmented": ssm.workspace_size(w.batch, w.L, w.D, w.N) > 0 if w.dtype != torch.float32 else None}
+        # One more call (untimed) with fp32 output, so the oracle check measures the
+        # computation rather than the bf16 output's own rounding.
+        if w.dtype != torch.float32:
+            y = torch.empty(y.shape, dtype=torch.float32, device=dev)
+            call()
+            torch.cuda.synchronize()
+        b0 = int(rng.integers(w.batch))
+        ds = np.sort(rng.choice(w.D, size=min(w.D, 16 if key == "long" else 64), replace=False))
+        idx = torch.as_tensor(ds, device=dev)
+        pick = lambda t: None if t is None else t[b0:b0 + 1].index_select(2, idx).cpu()
+        chan = lambda t: None if t is None else t.index_select(0, idx).cpu()
+        samples[key] = dict(u=pick(d["u"]), delta=pick(d["delta"]), z=pick(d["z"]), B=d["B"][b0:b0 + 1].cpu(),
+                            C=d["C"][b0:b0 + 1].cpu(), A=chan(d["A"]), D=chan(d["D"]), delta_bias=chan(d["delta_bias"]),
+                            delta_softplus=w.delta_softplus, y=pick(y), last=last[b0:b0 + 1].index_select(1, idx).cpu())
+        del d, y, last
+        torch.cuda.empty_cache()
+    return out, samples
+
+
+def sampled_oracle_errors(samples):
+    """Max |GPU - oracle| / rms(oracle) over each config's sampled channels (the oracle fed
+    the same inputs), with the oracle's time for the sample."""
+    import numpy as np
+
+    import oracle
+
+    res = {}
+    for key, sm in samples.items():
+        arr = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in sm.items()}
+        t0 = time.perf_counter()
+        yr, sr = oracle.selective_scan_fwd(arr["u"], arr["delta"], arr["A"], arr["B"], arr["C"], D=arr["D"],
+                                           z=arr["z"], delta_bias=arr["delta_bias"],
+                                           delta_softplus=arr["delta_softplus"], nthreads=os.cpu_count() or 1)
+        t = time.perf_counter() - t0
+        rms = lambda a: float(np.sqrt(np.mean(a * a)))
+        res[key] = {"y_err_rel_rms": float(np.max(np.abs(arr["y"] - yr)) / rms(yr)),
+                    "state_err_rel_rms": float(np.max(np.abs(arr["last"] - sr)) / rms(sr)),
+                    "channels": int(arr["u"].shape[2]), "oracle_s": t}
+    return res
 
 
 def e2e(w, d, args, ssm, torch, stream):
@@ -540,6 +637,7 @@ def main():
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=5)
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--ssd-steps", type=int, default=10)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
