@@ -380,7 +380,7 @@ cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
 // ---- decode launch -------------------------------------------------------------------
 template <typename T, typename TY, int N>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
-  const int64_t threads = p.batch * p.D * (N / 4);
+  const int64_t threads = p.batch * p.D * (N / (N >= 8 ? 8 : 4));  // 8 states per thread (4 for N = 4)
   dim3 grid((unsigned)((threads + 255) / 256)), block(256);
   void* args[] = {const_cast<DecodeParams*>(&p)};
   const bool ext = p.delta_bias || p.delta_softplus || p.zoh || p.conv_w;

@@ -8,7 +8,9 @@
 //  one iteration of the loop body.)
 //
 // The step streams the whole state once (read + write, 16-byte vectors); it is bound
-// by memory bandwidth, not arithmetic.
+// by memory bandwidth, not arithmetic. Each thread keeps two 16-byte state vectors (8
+// states) in flight: twice the bytes in flight per SM of one vector per thread, with
+// every warp still reading one contiguous 1 KB run.
 #pragma once
 
 #include "common.cuh"
@@ -37,14 +39,15 @@ struct DecodeParams {
   int64_t batch, D;
 };
 
-// One thread per (b, d, group of 4 states); the N/4 lanes of a channel are adjacent
+// One thread per (b, d, group of 8 states; 4 for N = 4); the lanes of a channel are adjacent
 // in the warp and combine their partial C.h with xor-shuffles.
 // kExt: the step-size map, the zero-order hold and the conv prologue are compiled in;
 // the plain step (all of them off) keeps the lean kernel (fewer registers, more resident
 // threads for this latency-bound update).
 template <typename T, typename TY, int N, bool kExt>
 __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p) {
-  constexpr int LPC = N / 4;
+  constexpr int SPT = N >= 8 ? 8 : 4;  // states per thread: two 16-byte vectors where N allows
+  constexpr int LPC = N / SPT;
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t bd = gt / LPC;
   const int g = (int)(gt % LPC);
@@ -53,12 +56,11 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
   const int64_t b = v ? bd / p.D : 0, d = v ? bd % p.D : 0;
 
   float acc = 0.f, x = 0.f;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (v) {
     const T* xp = static_cast<const T*>(p.x);
     const T* dp = static_cast<const T*>(p.delta);
-    const T* Bp = static_cast<const T*>(p.B) + b * N + g * 4;
-    const T* Cp = static_cast<const T*>(p.C) + b * N + g * 4;
+    const T* Bp = static_cast<const T*>(p.B) + b * N + g * SPT;
+    const T* Cp = static_cast<const T*>(p.C) + b * N + g * SPT;
     x = to_f32(xp[bd]);
     if (kExt && p.conv_w) {  // the block's causal conv + SiLU over (cs0, cs1, cs2, x)
       const T* cs = static_cast<const T*>(p.conv_state) + bd * 3;
@@ -74,19 +76,24 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecodeParams p)
     if (kExt && p.delta_bias) dt += p.delta_bias[d];
     if (kExt && p.delta_softplus) dt = softplus_precise(dt);
     const float dx = dt * x;
-    float4* sp = reinterpret_cast<float4*>(p.state + bd * N + g * 4);
-    s = *sp;
-    const float4 a4 = *reinterpret_cast<const float4*>(p.A + d * N + g * 4);
-    float sv[4] = {s.x, s.y, s.z, s.w};
-    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+    float4* sp = reinterpret_cast<float4*>(p.state + bd * N + g * SPT);
+    const float4* ap = reinterpret_cast<const float4*>(p.A + d * N + g * SPT);
+    float sv[SPT], av[SPT];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int q = 0; q < SPT / 4; ++q) {
+      const float4 s4 = sp[q], a4 = ap[q];
+      sv[4 * q] = s4.x; sv[4 * q + 1] = s4.y; sv[4 * q + 2] = s4.z; sv[4 * q + 3] = s4.w;
+      av[4 * q] = a4.x; av[4 * q + 1] = a4.y; av[4 * q + 2] = a4.z; av[4 * q + 3] = a4.w;
+    }
+#pragma unroll
+    for (int k = 0; k < SPT; ++k) {
       const float a = decay<sizeof(T) == 4>(dt, av[k], av[k] * kLog2e);
       const float bx = (kExt && p.zoh) ? zoh_factor<sizeof(T) == 4>(dt, av[k]) * x : dx;  // B-bar u = bx B
       sv[k] = fmaf(a, sv[k], bx * to_f32(Bp[k]));
       acc = fmaf(to_f32(Cp[k]), sv[k], acc);
     }
-    *sp = make_float4(sv[0], sv[1], sv[2], sv[3]);
+#pragma unroll
+    for (int q = 0; q < SPT / 4; ++q) sp[q] = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
   }
 #pragma unroll
   for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);

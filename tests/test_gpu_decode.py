@@ -35,9 +35,9 @@ def test_decode_workload_sampled():
     d = inputs.decode_inputs(w, DEV)
     state = d["state"]
     rng = np.random.default_rng(31)
-    rows = sorted(rng.choice(w.batch, size=2, replace=False).tolist())
-    picks = {b: np.sort(rng.choice(w.D, size=16, replace=False)) for b in rows}
-    ref_state = {b: np.zeros((1, 16, w.N)) for b in rows}
+    rows = sorted(rng.choice(w.batch, size=4, replace=False).tolist())
+    picks = {b: np.sort(rng.choice(w.D, size=64, replace=False)) for b in rows}  # 256 channels
+    ref_state = {b: np.zeros((1, 64, w.N)) for b in rows}
     ys = []
     for t in range(w.steps):
         y = ssm.state_update(state, d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t], D=d["D"], z=d["z"][t])
@@ -55,6 +55,29 @@ def test_decode_workload_sampled():
             yr, st = oracle.state_update(st, x[t][None], dl[t][None], A, Bm[t][None], Cm[t][None], D=Dk, z=z[t][None])
             check(ys[t][b], yr[0], TOL_BF16, True, f"y b={b} t={t}")
         check(state[b].index_select(0, ds), st[0], TOL_BF16, False, f"state b={b}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_decode_unaligned_B_C(dtype):
+    """B and C at an element offset that is not 16-byte aligned take the scalar loads."""
+    N = 16
+    w = inputs.DecodeWorkload("t", 3, 96, N, 1, dtype, 23)
+    d = inputs.decode_inputs(w, DEV)
+    Bbuf = torch.empty(3 * N + 1, dtype=dtype, device=DEV)
+    Cbuf = torch.empty(3 * N + 1, dtype=dtype, device=DEV)
+    B = Bbuf[1:].view(3, N)
+    C = Cbuf[1:].view(3, N)
+    B.copy_(d["B"][0])
+    C.copy_(d["C"][0])
+    assert B.data_ptr() % 16 != 0
+    state = torch.randn(3, 96, N, generator=torch.Generator().manual_seed(24)).to(DEV)
+    st_ref = to64(state)
+    yr, st_ref = oracle.state_update(st_ref, d["x"][0], d["delta"][0], d["A"], B, C, D=d["D"], z=d["z"][0])
+    y = ssm.state_update(state, d["x"][0], d["delta"][0], d["A"], B, C, D=d["D"], z=d["z"][0])
+    torch.cuda.synchronize()
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    check(y, yr, tol, dtype == torch.bfloat16, "y")
+    check(state, st_ref, tol, False, "state")
 
 
 def test_decode_delta_zero_keeps_state_bitwise():
