@@ -276,7 +276,9 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         if (!kAgg) tma_load_3d(st + 3 * Lay::kTileIO + Lay::kTileBC, &tm_C, 0, t0, b, &full[s]);
         issued = k + 1;
       }
-      // Never leave with loads in flight into this CTA's shared memory.
+      // Wait (bounded) for the loads still in flight before leaving. The wait limit is far
+      // longer than any copy takes (about a second against microseconds), so a load can
+      // outlive the CTA only if the copy engine stopped completing copies altogether.
       for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
         if (!mbar_wait(&full[k % S], (k / S) & 1, kErrWaitFull, lim)) break;
     }

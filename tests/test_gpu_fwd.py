@@ -93,7 +93,7 @@ def test_tiny_fp32_time_split(monkeypatch):
 def test_layer_workloads_sampled(key):
     w = inputs.FWD_WORKLOADS[key]
     d = inputs.fwd_inputs(w, DEV)
-    ref = sample_channels(d, per_row=24, rows=3, seed=11)
+    ref = sample_channels(d, per_row=64, rows=4, seed=11)  # 256 channels over the whole sequence
     y, last = gpu_fwd(d)
     check_sampled(y, last, ref, TOL_BF16, True, key)
     y32, last32 = gpu_fwd(d, y_dtype=torch.float32)
@@ -104,7 +104,7 @@ def test_layer_workloads_sampled(key):
 
 def test_long_sequence_sampled():
     d = inputs.fwd_inputs(inputs.LONG, DEV)
-    ref = sample_channels(d, per_row=6, rows=1, seed=12)
+    ref = sample_channels(d, per_row=256, rows=1, seed=12)  # 256 channels over all 131072 steps
     y, last = gpu_fwd(d)
     check_sampled(y, last, ref, TOL_BF16, True, "long")
 
