@@ -9,6 +9,8 @@ namespace ssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Steps between the state checkpoints of the backward pass's recomputation.
+constexpr int kCkSteps = 16;
 
 // ---- element conversions --------------------------------------------------------
 template <typename T> __device__ __forceinline__ float to_f32(T v);

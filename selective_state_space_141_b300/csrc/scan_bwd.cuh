@@ -15,15 +15,17 @@
 //
 // Layout: two lanes per channel, each holding half of its N states in registers (a warp
 // covers 16 channels; one warp per CTA, several CTAs per SM), so that twice as many warps
-// hide the latency of the per-step dependency chains. A forward sweep stores the state before every
-// chunk of kBwdK steps (checkpoints); the reverse sweep recomputes a chunk's states into
-// shared memory, then walks it backwards. Each chunk's inputs are staged into shared
-// memory with asynchronous copies (cp.async), double-buffered: the next chunk streams
-// in while the current one is computed, and B, C are read as shared-memory broadcasts.
-// dB and dC are sums over channels: each warp
-// reduces its 16 channels with a transpose-reduce butterfly (shuffles) and writes one
-// partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over warps, and
-// dA, dD, dbias over batch rows, in a fixed order (deterministic, no atomics).
+// hide the latency of the per-step dependency chains. The state before every chunk of
+// kBwdK steps (a checkpoint) comes from the channel kernel's forward sweep (ck_ready), or
+// from a forward sweep here when that kernel does not apply. Per chunk, in reverse order:
+// the raw inputs, staged into shared memory by asynchronous copies (cp.async), become
+// per-(step, channel) scalars in a prologue (each computed once), the buffer is refilled
+// with the previous chunk at once, the chunk's states are recomputed into shared memory
+// from its checkpoint, and the chunk is walked backwards; the read-out C.h + D u that the
+// gate's gradient needs is recomputed in that walk. dB and dC are sums over channels:
+// each warp reduces its 16 channels with one transpose-reduce (shuffles) per step and
+// writes one partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over
+// warps, and dA, dD, dbias over batch rows, in a fixed order (deterministic, no atomics).
 #pragma once
 
 #include "common.cuh"
@@ -56,27 +58,31 @@ struct BwdParams {
   int64_t batch, L, D;
   int nc, W;          // chunks of kBwdK steps; warps along D
   bool async_ok;      // every staged row starts 16-byte aligned: stage with cp.async
+  int ck_ready;       // 1: ck already holds the checkpoints (no forward sweep here)
 };
 
-constexpr int kBwdK = 16;
+constexpr int kBwdK = kCkSteps;
 constexpr int kBwdCh = 16;  // channels per warp (two lanes per channel)
 
-// Sum over the warp's 16 channels (lanes of equal parity: lane = 2 * channel + half) of
-// each of v[0..NH-1]; lane l ends with the sum of v[(l >> (5 - log2 NH)) & (NH - 1)] of
-// its half. Each round halves the values a lane holds: the lanes with the round's bit set
-// keep the upper half and send the lower, the others the reverse; bit 0 (the half) is
-// never summed.
-template <int NH>
-__device__ __forceinline__ float pair_transpose_reduce(float (&v)[NH], int lane) {
-  constexpr int kLog = NH == 8 ? 3 : NH == 4 ? 2 : 1;
-  int m = NH;
+// Sums over the warp's 16 channels (lane = 2 * channel + half) of the 2 NH values v[]
+// of every lane (its half's dB contributions, then its dC contributions): a transpose-
+// reduce. Each round halves what a lane holds: the lanes with the round's bit set keep
+// the upper half and send the lower, the others the reverse. After the rounds over lane
+// bits 4..1 (2 NH = 16) lane l holds the sum for value index (l >> 1) & 15 of its half,
+// i.e. kind (l >> 4) & 1 (0 = dB, 1 = dC) and state half * NH + ((l >> 1) & 7).
+// N = 8 / 4 (2 NH = 8 / 4 values) stop after 3 / 2 rounds; lane bits 2 / 3..1 left over
+// still separate channels, so those lanes finish with plain xor-shuffle sums.
+template <int NV>
+__device__ __forceinline__ float bwd_transpose_reduce(float (&v)[NV], int lane) {
+  constexpr int kLog = NV == 16 ? 4 : NV == 8 ? 3 : 2;
+  int m = NV;
 #pragma unroll
   for (int r = 0; r < kLog; ++r) {
     const int o = 16 >> r;
     const bool upper = (lane & o) != 0;
     const int half = m / 2;
 #pragma unroll
-    for (int i = 0; i < NH / 2; ++i) {
+    for (int i = 0; i < NV / 2; ++i) {
       if (i < half) {
         const float send = upper ? v[i] : v[i + half];
         const float keep = upper ? v[i + half] : v[i];
@@ -90,7 +96,6 @@ __device__ __forceinline__ float pair_transpose_reduce(float (&v)[NH], int lane)
   for (int o = 16 >> kLog; o >= 2; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
 }
-
 // ---- chunk staging: global -> shared memory, asynchronous (cp.async) ----
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
@@ -204,25 +209,28 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
 // states); dynamic shared memory:
 //   hs  [kBwdK + 1][N/4][32] f32x2 each lane's state pairs h_{t0-1} .. h_{t0+K-1} of the chunk
 //   bc  [kBwdK][2N]          f32  the chunk's B | C rows
-//   dts [kBwdK][32]          f32  step sizes (both lanes of a channel hold the same)
-//   vs  [kBwdK][32]          f32  read-outs C.h + D u (before the gate)
-//   stage[2]                      raw inputs of the current and the next chunk
+//   sc  [kBwdK][16]          f32x4 per (step, channel): dt, dt u, dv, u
+//   sx  [kBwdK][16]          f32x2 per (step, channel): d(dt)/d(delta), dy silu'(z)
+//   red [16][32]             f32  (N = 16) one step's dB | dC values per channel, for the channel sums
+//   stage                         raw inputs of one chunk (refilled as soon as they are read)
 template <typename T, typename TG, int N>
 constexpr int bwd_smem_bytes() {
-  return ((kBwdK + 1) * (N / 2) * 32 + kBwdK * 2 * N + 2 * kBwdK * 32) * 4 + 2 * (int)sizeof(BwdStage<T, TG, N>);
+  return ((kBwdK + 1) * (N / 2) * 32 + kBwdK * 2 * N + kBwdK * kBwdCh * 6 + (N == 16 ? kBwdCh * 32 : 0)) * 4 +
+         (int)sizeof(BwdStage<T, TG, N>);
 }
 
 template <typename T, typename TG, int N>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   constexpr int NH = N / 2;   // states per lane
   constexpr int P2 = NH / 2;  // packed pairs per lane
+  constexpr int kItems = kBwdK * kBwdCh / 32;  // (step, channel) items per lane in a chunk
   extern __shared__ __align__(16) float sm[];
-  float* hs = sm;  // [kBwdK + 1][P2][32] float2: state pairs of each lane
-  float2* hs2 = reinterpret_cast<float2*>(hs);
-  float* bc = hs + (kBwdK + 1) * NH * 32;
-  float* dts = bc + kBwdK * 2 * N;
-  float* vs = dts + kBwdK * 32;
-  BwdStage<T, TG, N>* stg = reinterpret_cast<BwdStage<T, TG, N>*>(vs + kBwdK * 32);
+  float2* hs2 = reinterpret_cast<float2*>(sm);  // [kBwdK + 1][P2][32]
+  float* bc = sm + (kBwdK + 1) * NH * 32;
+  float4* sc = reinterpret_cast<float4*>(bc + kBwdK * 2 * N);  // [kBwdK][16]
+  float2* sx = reinterpret_cast<float2*>(sc + kBwdK * kBwdCh);  // [kBwdK][16]
+  float* red = reinterpret_cast<float*>(sx + kBwdK * kBwdCh);  // [16][32] when N = 16
+  BwdStage<T, TG, N>& sg = *reinterpret_cast<BwdStage<T, TG, N>*>(red + (N == 16 ? kBwdCh * 32 : 0));
   const int lane = threadIdx.x, ch = lane >> 1, half = lane & 1, nb = half * NH;
   const int w = blockIdx.x;
   const int64_t b = blockIdx.y;
@@ -230,9 +238,11 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   const int64_t d0 = (int64_t)w * kBwdCh, d = d0 + ch;
   const bool vd = d < D;
   constexpr bool kAccurate = sizeof(T) == 4;
-  const float bias = (vd && p.delta_bias) ? p.delta_bias[d] : 0.f;
+  // the prologue's items all belong to channel lane & 15
+  const int pch = lane & 15;
+  const float pbias = (d0 + pch < D && p.delta_bias) ? p.delta_bias[d0 + pch] : 0.f;
 
-  float2 Av[P2], A2[P2], h[P2];
+  float2 Av[P2], A2[P2], h[P2];  // A, A log2(e) (Av: the fp32 path's exact decay and sums)
 #pragma unroll
   for (int q = 0; q < P2; ++q) {
     Av[q] = vd ? make_float2(p.A[d * N + nb + 2 * q], p.A[d * N + nb + 2 * q + 1]) : make_float2(0.f, 0.f);
@@ -240,52 +250,75 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     h[q] = (vd && p.h0) ? make_float2(p.h0[(b * D + d) * N + nb + 2 * q], p.h0[(b * D + d) * N + nb + 2 * q + 1])
                         : make_float2(0.f, 0.f);
   }
-  auto convert_bc = [&](const BwdStage<T, TG, N>& sg, bool with_c) {
-    for (int i = lane; i < kBwdK * N; i += 32) {
-      const int k = i / N, n = i % N;
-      bc[k * 2 * N + n] = to_f32(sg.B[i]);
-      if (with_c) bc[k * 2 * N + N + n] = to_f32(sg.C[i]);
-    }
-    __syncwarp();
-  };
-  auto step_dt = [&](const BwdStage<T, TG, N>& sg, int k, float* r_out) {
-    const float r = to_f32(sg.dl[k][ch]) + bias;
-    if (r_out) *r_out = r;
-    if (!p.delta_softplus) return r;
-    if (kAccurate) return softplus_precise(r);
-    return fmaxf(r, 0.f) + kLn2 * lg2(1.f + ex2(fabsf(r) * -kLog2e));  // SFU form, as the forward
-  };
   // the bf16 path divides with the fast approximate reciprocal (~2 ulp), well inside its
   // tolerance; the fp32 path keeps the correctly rounded one
   auto sigmoid = [&](float x) {
     return kAccurate ? __frcp_rn(1.f + __expf(-x)) : __fdividef(1.f, 1.f + __expf(-x));
   };
+  // Chunk prologue: B | C rows to f32, and the per-(step, channel) scalars computed once
+  // (not once per lane of the channel and per sweep). full = false: the forward sweep's
+  // dt and dt u only (dy and z are not staged there).
+  auto prologue = [&](bool full) {
+    for (int i = lane; i < kBwdK * N; i += 32) {
+      const int k = i / N, n = i % N;
+      bc[k * 2 * N + n] = to_f32(sg.B[i]);
+      if (full) bc[k * 2 * N + N + n] = to_f32(sg.C[i]);
+    }
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      const int k = 2 * j + (lane >> 4);
+      const float r = to_f32(sg.dl[k][pch]) + pbias;
+      float dt = r, sr = 1.f;
+      if (p.delta_softplus) {
+        dt = kAccurate ? softplus_precise(r) : fmaxf(r, 0.f) + kLn2 * lg2(1.f + ex2(fabsf(r) * -kLog2e));
+        if (full) sr = sigmoid(r);
+      }
+      const float x = to_f32(sg.u[k][pch]);
+      float dv = 0.f, dyz = 0.f;
+      if (full) {
+        const float dyv = to_f32(sg.dy[k][pch]);
+        dv = dyv;
+        if (p.z) {
+          const float zz = to_f32(sg.z[k][pch]);
+          const float s = sigmoid(zz);
+          dv = dyv * zz * s;                          // dy silu(z)
+          dyz = dyv * (s * (1.f + zz * (1.f - s)));   // dy silu'(z)
+        }
+      }
+      sc[k * kBwdCh + pch] = make_float4(dt, dt * x, dv, x);
+      sx[k * kBwdCh + pch] = make_float2(sr, dyz);
+    }
+    __syncwarp();
+  };
+  // One step of the recurrence for this lane's pairs from the scalars of step k.
+  auto fwd_step = [&](int k) {
+    const float4 s = sc[k * kBwdCh + ch];
+    const float2 dt2 = make_float2(s.x, s.x), du2 = make_float2(s.y, s.y);
+    float2 b2[P2];
+    load_pairs<P2>(bc + k * 2 * N + nb, b2);
+#pragma unroll
+    for (int q = 0; q < P2; ++q) h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(du2, b2[q]));
+  };
 
-  // ---- forward sweep: the state before every chunk ----
-  if (p.nc > 1) stage_chunk<T, TG, N>(stg[0], p, b, 0, d0, false, lane);
-  for (int c = 0; c < p.nc; ++c) {
-    if (vd) {
-      float2* ckp = reinterpret_cast<float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
-#pragma unroll
-      for (int q = 0; q < P2; ++q) ckp[q] = h[q];
+  // ---- forward sweep, only when the checkpoints were not supplied ----
+  if (!p.ck_ready) {
+    if (p.nc > 1) {
+      stage_chunk<T, TG, N>(sg, p, b, 0, d0, false, lane);
     }
-    if (c == p.nc - 1) break;  // the state after the last chunk is not needed
-    cp_async_wait_all();
-    __syncwarp();
-    const BwdStage<T, TG, N>& sg = stg[c & 1];
-    convert_bc(sg, false);
-    if (c + 1 < p.nc - 1) stage_chunk<T, TG, N>(stg[(c + 1) & 1], p, b, c + 1, d0, false, lane);
-    for (int k = 0; k < kBwdK; ++k) {  // chunks before the last are full
-      const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
-      const float dx = dt * to_f32(sg.u[k][ch]);
-      const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-      float2 b2[P2];
-      load_pairs<P2>(bc + k * 2 * N + nb, b2);
+    for (int c = 0; c < p.nc; ++c) {
+      if (vd) {
+        float2* ckp = reinterpret_cast<float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
 #pragma unroll
-      for (int q = 0; q < P2; ++q)
-        h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
+        for (int q = 0; q < P2; ++q) ckp[q] = h[q];
+      }
+      if (c == p.nc - 1) break;  // the state after the last chunk is not needed
+      cp_async_wait_all();
+      __syncwarp();
+      prologue(false);
+      if (c + 1 < p.nc - 1) stage_chunk<T, TG, N>(sg, p, b, c + 1, d0, false, lane);
+      for (int k = 0; k < kBwdK; ++k) fwd_step(k);  // chunks before the last are full
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   // ---- reverse sweep ----
@@ -298,25 +331,39 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   }
   float dD_acc = 0.f, dbias_acc = 0.f;
   const float Dk = (vd && p.Dskip) ? p.Dskip[d] : 0.f;
-  constexpr int kLog = NH == 8 ? 3 : NH == 4 ? 2 : 1;
-  const int n_red = nb + ((lane >> (5 - kLog)) & (NH - 1));
-  const bool writer = (lane & (((1 << (5 - kLog)) - 1) & ~1)) == 0;
+  constexpr int NV = 2 * NH;
+  constexpr int kLog = NV == 16 ? 4 : NV == 8 ? 3 : 2;
+  const int vidx = (lane >> (5 - kLog)) & (NV - 1);
+  // kind * N + state of the channel sum this lane ends with (the shared-memory sums of
+  // N = 16 leave sum j in lane j)
+  const int n_red = N == 16 ? lane : (vidx / NH) * N + nb + (vidx % NH);
+  const bool writer = (lane & ((1 << (5 - kLog)) - 2)) == 0;
   const bool lead = half == 0 && vd;  // writes the channel's per-step outputs
   TG* du = static_cast<TG*>(p.du) + b * L * D + d;
   TG* ddl = static_cast<TG*>(p.ddelta) + b * L * D + d;
   TG* dzp = p.dz ? static_cast<TG*>(p.dz) + b * L * D + d : nullptr;
-  float* part = p.part + ((b * L) * p.W + w) * 2 * N;  // + t * W * 2N
+  const int64_t pstride = (int64_t)p.W * 2 * N;
+  float* part = p.part + ((b * L) * p.W + w) * 2 * N + n_red;  // + t * W * 2N
+  // Channel sums through shared memory (N = 16): lane (ch, half) stores its 16 values (dB,
+  // then dC, of its 8 states) into row ch of red[16][32]; lane j then adds column j over
+  // the 16 rows, the sum for kind j >> 4 and state j & 15 (so n_red = j). Float4 group g of
+  // row ch sits at g ^ f(ch), f(ch) = (ch & 1) | (ch & 2) << 1: the 16-byte stores (8 lanes
+  // per phase) and the column reads each touch 32 distinct banks.
+  const int fch = (ch & 1) | ((ch & 2) << 1);
+  float4* red_w = reinterpret_cast<float4*>(red + ch * 32);
+  int rd_off[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) rd_off[c] = ((((lane >> 2) ^ ((c & 1) | ((c & 2) << 1))) << 2) | (lane & 3));
 
-  stage_chunk<T, TG, N>(stg[(p.nc - 1) & 1], p, b, p.nc - 1, d0, true, lane);
+  stage_chunk<T, TG, N>(sg, p, b, p.nc - 1, d0, true, lane);
   for (int c = p.nc - 1; c >= 0; --c) {
     const int64_t t0 = (int64_t)c * kBwdK;
     const int kc = (int)((L - t0) < kBwdK ? (L - t0) : kBwdK);
     cp_async_wait_all();
     __syncwarp();
-    const BwdStage<T, TG, N>& sg = stg[c & 1];
-    convert_bc(sg, true);
-    if (c > 0) stage_chunk<T, TG, N>(stg[(c - 1) & 1], p, b, c - 1, d0, true, lane);
-    // recompute the chunk's states and read-outs
+    prologue(true);
+    if (c > 0) stage_chunk<T, TG, N>(sg, p, b, c - 1, d0, true, lane);
+    // recompute the chunk's states from its checkpoint
     {
       const float2* ckp = reinterpret_cast<const float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
 #pragma unroll
@@ -325,84 +372,80 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
         hs2[q * 32 + lane] = h[q];
       }
       for (int k = 0; k < kc; ++k) {
-        const float dt = vd ? step_dt(sg, k, nullptr) : 0.f;
-        const float x = to_f32(sg.u[k][ch]);
-        const float dx = dt * x;
-        dts[k * 32 + lane] = dt;
-        const float2 dt2 = make_float2(dt, dt), dx2 = make_float2(dx, dx);
-        float2 b2[P2], c2[P2];
-        load_pairs<P2>(bc + k * 2 * N + nb, b2);
-        load_pairs<P2>(bc + k * 2 * N + N + nb, c2);
-        float2 acc = make_float2(0.f, 0.f);
+        fwd_step(k);
 #pragma unroll
-        for (int q = 0; q < P2; ++q) {
-          h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(dx2, b2[q]));
-          acc = __ffma2_rn(c2[q], h[q], acc);
-          hs2[((k + 1) * P2 + q) * 32 + lane] = h[q];
-        }
-        const float vp = acc.x + acc.y;
-        vs[k * 32 + lane] = fmaf(Dk, x, vp + __shfl_xor_sync(0xffffffffu, vp, 1));
+        for (int q = 0; q < P2; ++q) hs2[((k + 1) * P2 + q) * 32 + lane] = h[q];
       }
     }
     // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
+#pragma unroll 2
+    const int64_t tl = t0 + kc - 1;
+    TG* pdu = du + tl * D;
+    TG* pddl = ddl + tl * D;
+    TG* pdz = dzp ? dzp + tl * D : nullptr;
+    float* ppart = part + tl * pstride;
     for (int k = kc - 1; k >= 0; --k) {
-      const int64_t t = t0 + k;
-      const float dt = dts[k * 32 + lane];
-      float r = 0.f;
-      if (vd) step_dt(sg, k, &r);
-      const float x = to_f32(sg.u[k][ch]), dyv = to_f32(sg.dy[k][ch]);
-      const float v = vs[k * 32 + lane];
-      float dv = dyv;
-      if (dzp) {
-        const float zz = to_f32(sg.z[k][ch]);
-        const float sgm = sigmoid(zz);
-        if (lead) dzp[t * D] = from_f32<TG>(dyv * v * (sgm * (1.f + zz * (1.f - sgm))));
-        dv = dyv * zz * sgm;
-      }
-      dD_acc = fmaf(dv, x, dD_acc);
-      const float2 dv2 = make_float2(dv, dv), dt2 = make_float2(dt, dt), x2 = make_float2(x, x);
+      const float4 s = sc[k * kBwdCh + ch];  // dt, dt u, dv, u
+      const float2 sxv = sx[k * kBwdCh + ch];
+      const float2 dt2 = make_float2(s.x, s.x), du2 = make_float2(s.y, s.y), dv2 = make_float2(s.z, s.z);
       float2 b2[P2], c2[P2];
       load_pairs<P2>(bc + k * 2 * N + nb, b2);
       load_pairs<P2>(bc + k * 2 * N + N + nb, c2);
-      float2 dux2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
-      float vb[NH], vc[NH];
+      float2 vacc = make_float2(0.f, 0.f), sgB = make_float2(0.f, 0.f), sAg = make_float2(0.f, 0.f);
+      float vr[NV];
 #pragma unroll
       for (int q = 0; q < P2; ++q) {
-        const float2 hp = hs2[(k * P2 + q) * 32 + lane];
+        const float2 hp = hs2[(k * P2 + q) * 32 + lane];      // h_{t-1}
         const float2 a = decay2<kAccurate>(dt2, Av[q], A2[q]);
-        const float2 B2 = b2[q];
-        g[q] = __ffma2_rn(dv2, c2[q], g[q]);                 // g = dL/dh_t
-        const float2 cv = __fmul2_rn(dv2, h[q]);             // dC_t contribution: dv h_t
-        const float2 gdt = __fmul2_rn(g[q], dt2);
-        const float2 bv = __fmul2_rn(gdt, x2);               // dB_t contribution: g dt u
-        dux2 = __ffma2_rn(gdt, B2, dux2);
-        const float2 ah = __fmul2_rn(a, hp);
-        ddt2 = __ffma2_rn(g[q], __ffma2_rn(B2, x2, __fmul2_rn(Av[q], ah)), ddt2);
-        dA_acc[q] = __ffma2_rn(__fmul2_rn(g[q], ah), dt2, dA_acc[q]);
-        g[q] = __fmul2_rn(g[q], a);                          // dL/dh_{t-1} (through the recurrence)
-        h[q] = hp;                                           // h_t of step t-1
-        vb[2 * q] = bv.x;
-        vb[2 * q + 1] = bv.y;
-        vc[2 * q] = cv.x;
-        vc[2 * q + 1] = cv.y;
+        g[q] = __ffma2_rn(dv2, c2[q], g[q]);                  // g = dL/dh_t
+        const float2 cv = __fmul2_rn(dv2, h[q]);              // dC_t: dv h_t
+        vacc = __ffma2_rn(c2[q], h[q], vacc);                 // C_t . h_t
+        const float2 bv = __fmul2_rn(g[q], du2);              // dB_t: g dt u
+        sgB = __ffma2_rn(g[q], b2[q], sgB);                   // sum g B_t
+        const float2 gah = __fmul2_rn(g[q], __fmul2_rn(a, hp));
+        dA_acc[q] = __ffma2_rn(gah, dt2, dA_acc[q]);          // dA: g a h_{t-1} dt
+        sAg = __ffma2_rn(kAccurate ? Av[q] : A2[q], gah, sAg); // sum A g a h_{t-1} (A log2 e on bf16)
+        g[q] = __fmul2_rn(g[q], a);                           // dL/dh_{t-1} through the recurrence
+        h[q] = hp;
+        vr[2 * q] = bv.x;
+        vr[2 * q + 1] = bv.y;
+        vr[NH + 2 * q] = cv.x;
+        vr[NH + 2 * q + 1] = cv.y;
       }
-      float dux = dux2.x + dux2.y, ddt = ddt2.x + ddt2.y;
-      dux += __shfl_xor_sync(0xffffffffu, dux, 1);          // the channel's other half
-      ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
-      dux = fmaf(dv, Dk, dux);
-      const float dr = p.delta_softplus ? ddt * sigmoid(r) : ddt;
+      float v = vacc.x + vacc.y, gb = sgB.x + sgB.y, ag = sAg.x + sAg.y;
+      v += __shfl_xor_sync(0xffffffffu, v, 1);  // the channel's other half
+      gb += __shfl_xor_sync(0xffffffffu, gb, 1);
+      ag += __shfl_xor_sync(0xffffffffu, ag, 1);
+      v = fmaf(Dk, s.w, v);                                         // read-out before the gate
+      const float dux = fmaf(s.z, Dk, s.x * gb);                    // du = dv D + dt sum g B
+      const float ddt = fmaf(s.w, gb, (kAccurate ? 1.f : kLn2) * ag);  // d(dt)
+      const float dr = ddt * sxv.x;
+      dD_acc = fmaf(s.z, s.w, dD_acc);
       dbias_acc += dr;
       if (lead) {
-        du[t * D] = from_f32<TG>(dux);
-        ddl[t * D] = from_f32<TG>(dr);
+        *pdu = from_f32<TG>(dux);
+        *pddl = from_f32<TG>(dr);
+        if (pdz) *pdz = from_f32<TG>(sxv.y * v);  // dz = dy v silu'(z)
       }
-      const float sb = pair_transpose_reduce<NH>(vb, lane);
-      const float sc = pair_transpose_reduce<NH>(vc, lane);
-      if (writer) {
-        float* pp = part + t * p.W * 2 * N;
-        pp[n_red] = sb;
-        pp[N + n_red] = sc;
+      pdu -= D;
+      pddl -= D;
+      if (pdz) pdz -= D;
+      float sr;
+      if constexpr (N == 16) {
+        red_w[(2 * half) ^ fch] = make_float4(vr[0], vr[1], vr[2], vr[3]);
+        red_w[(2 * half + 1) ^ fch] = make_float4(vr[4], vr[5], vr[6], vr[7]);
+        red_w[(4 + 2 * half) ^ fch] = make_float4(vr[8], vr[9], vr[10], vr[11]);
+        red_w[(5 + 2 * half) ^ fch] = make_float4(vr[12], vr[13], vr[14], vr[15]);
+        __syncwarp();
+        sr = red[rd_off[0]];
+#pragma unroll
+        for (int c = 1; c < kBwdCh; ++c) sr += red[c * 32 + rd_off[c & 3]];
+        __syncwarp();  // every lane has read before the next step's stores
+      } else {
+        sr = bwd_transpose_reduce<NV>(vr, lane);
       }
+      if (writer) *ppart = sr;
+      ppart -= pstride;
     }
     __syncwarp();
   }
@@ -426,7 +469,6 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     }
   }
 }
-
 // Fixed-order sums of the partials: dB, dC (batch, L, N) over the W warps along D;
 // dA (D, N), dD (D), dbias (D) over the batch rows. One thread per output element.
 template <typename TG>

@@ -365,11 +365,25 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     const float* bc = reinterpret_cast<const float*>(st + 3 * Lay::kTileIO + 2 * Lay::kTileBC);
     const int64_t tk = t_begin + (int64_t)k * TC;
     const int tc = (int)((t_end - tk) < TC ? (t_end - tk) : TC);
+    // Aggregate pass: the state before step tk + t0, when that step starts a checkpoint chunk.
+    auto checkpoint = [&](int t0) {
+      if (kAgg && p.ck && vd && t0 % kCkSteps == 0) {
+        float4* c4 = reinterpret_cast<float4*>(p.ck + (((int64_t)b * p.ck_nc + (tk + t0) / kCkSteps) * D + d) * N);
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) c4[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
+      }
+    };
     if (kAgg) {
       if (tc == TC) {
-        for (int t0 = 0; t0 < TC; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, false, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+        for (int t0 = 0; t0 < TC; t0 += kChanSub) {
+          checkpoint(t0);
+          chan_subchunk_agg<N, kSoftplus, false, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+        }
       } else {
-        for (int t0 = 0; t0 < tc; t0 += kChanSub) chan_subchunk_agg<N, kSoftplus, true, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+        for (int t0 = 0; t0 < tc; t0 += kChanSub) {
+          checkpoint(t0);
+          chan_subchunk_agg<N, kSoftplus, true, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -410,7 +424,7 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
         seg_slot_store(sy, 2, seg, b, d, 2 * q, ex2(A2[q].x * sdt));
         seg_slot_store(sy, 2, seg, b, d, 2 * q + 1, ex2(A2[q].y * sdt));
       }
-    } else if (vd) {
+    } else if (vd && p.seg_E) {
       float4* e4 = reinterpret_cast<float4*>(p.seg_E + sidx);
       float4* p4 = reinterpret_cast<float4*>(p.seg_P + sidx);
 #pragma unroll

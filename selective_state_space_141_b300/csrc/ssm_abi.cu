@@ -314,6 +314,33 @@ cudaError_t launch_chan_n(int64_t N, const FwdParams& p, const SegPlan& plan, vo
   return launch_chan<TY, 16>(p, plan, ws, st, launched);
 }
 
+// Checkpoints for the backward pass: the channel kernel's aggregate pass over one
+// segment (the recurrence without read-out) writes the state before every kCkSteps-step
+// chunk to ck[b][c][D][N]. *launched = false when a tensor map cannot be built.
+template <int N>
+cudaError_t launch_chan_ckpt(const FwdParams& p0, float* ck, int64_t nc, cudaStream_t st, bool* launched) {
+  *launched = false;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t L = (uint64_t)p0.L, Bt = (uint64_t)p0.batch, D = (uint64_t)p0.D;
+  CUtensorMap maps[6];  // u, delta, z, B, C, y
+  if (!encode_3d(&maps[0], p0.u, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[1], p0.delta, bf, 2, D, L, Bt, ssm::kChanCTA, kChanTC) ||
+      !encode_3d(&maps[3], p0.B, bf, 2, N, L, Bt, N, kChanTC))
+    return cudaSuccess;
+  maps[2] = maps[0];  // z, C and y: the aggregate pass reads and writes none of them
+  maps[4] = maps[3];
+  maps[5] = maps[0];
+  *launched = true;
+  FwdParams p = p0;
+  p.seg_len = p0.L;
+  p.seg_h0 = p0.h0;
+  p.seg_E = p.seg_P = nullptr;
+  p.seg_y = nullptr;
+  p.ck = ck;
+  p.ck_nc = nc;
+  return launch_chan_sw<__nv_bfloat16, N, true>(p, maps, 1, st, p0.delta_softplus != 0, false);
+}
+
 // ---- generic forward launch ------------------------------------------------------------
 constexpr int kGenDT = 32, kGenTC = 32;
 
@@ -556,6 +583,8 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.seg_y_bf16 = 0;
   p.wait_cycles = wait_limit_cycles();
   p.fault_skip_loads = fault_skip_loads();
+  p.ck = nullptr;
+  p.ck_nc = 0;
 
   cudaError_t e;
   const FwdVariant var = forward_variant();
@@ -942,6 +971,29 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   }
 
   cudaError_t e;
+  p.ck_ready = 0;
+  if (io == SSM_BF16 && (N == 8 || N == 16) && forward_variant() != FwdVariant::kGeneric) {
+    // The checkpoints from the channel kernel (as the forward pass's fast path)
+    FwdParams fp{};
+    fp.u = u->data;
+    fp.delta = delta->data;
+    fp.A = p.A;
+    fp.B = B->data;
+    fp.C = C->data;
+    fp.delta_bias = p.delta_bias;
+    fp.delta_softplus = delta_softplus;
+    fp.h0 = p.h0;
+    fp.batch = batch;
+    fp.L = L;
+    fp.D = Dm;
+    fp.wait_cycles = wait_limit_cycles();
+    if (chan_eligible(fp, N)) {
+      bool launched = false;
+      e = N == 8 ? launch_chan_ckpt<8>(fp, p.ck, p.nc, st, &launched) : launch_chan_ckpt<16>(fp, p.ck, p.nc, st, &launched);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+      p.ck_ready = launched ? 1 : 0;
+    }
+  }
   if (io == SSM_F32)
     e = launch_bwd_n<float, float>(N, p, st);
   else if (gt == SSM_BF16)
