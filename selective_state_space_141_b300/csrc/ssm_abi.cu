@@ -20,6 +20,7 @@
 #include "scan_fwd_chan.cuh"
 #include "ssd_fwd.cuh"
 #include "state_update.cuh"
+#include "state_update_stream.cuh"
 
 namespace {
 
@@ -176,6 +177,13 @@ int num_sms() {
 bool segments_enabled() {
   const char* e = getenv("SSM_B300_SEGMENTS");
   return !(e && strcmp(e, "0") == 0);
+}
+
+// SSM_B300_DECODE=plain: the decode step always uses the one-launch-per-thread kernel
+// (tests compare it with the streamed one).
+bool decode_streamed() {
+  const char* e = getenv("SSM_B300_DECODE");
+  return !(e && strcmp(e, "plain") == 0);
 }
 
 int64_t fit_segments(int64_t L, int64_t nseg, int64_t tc, int64_t min_len, int64_t rows, int64_t* len) {
@@ -405,8 +413,43 @@ cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
 }
 
 // ---- decode launch -------------------------------------------------------------------
+// The streamed decode kernel: the plain step with bf16 inputs and N = 16 when D splits
+// into whole tiles and every streamed tensor starts 16-byte aligned.
+template <typename TY>
+cudaError_t launch_dec_stream(const DecodeParams& p, cudaStream_t st, bool* launched) {
+  *launched = false;
+  if (p.delta_bias || p.delta_softplus || p.zoh || p.conv_w || p.D % ssm::kDecTile != 0) return cudaSuccess;
+  for (const void* q : {static_cast<const void*>(p.state), p.x, p.delta, static_cast<const void*>(p.A), p.B, p.C, p.z})
+    if (!aligned16(q)) return cudaSuccess;
+  auto kern = &ssm::state_update_stream<TY>;
+  constexpr int smem = ssm::dec_stream_smem_bytes();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr != cudaSuccess) return attr;
+  constexpr int threads = ssm::kDecConsumers + 32;
+  static int per_sm = -1;
+  if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+                     per_sm < 1))
+    per_sm = 1;
+  int64_t ntiles = p.batch * p.D / ssm::kDecTile;
+  int64_t grid = (int64_t)(num_sms() > 0 ? num_sms() : 1) * per_sm;
+  if (grid > ntiles) grid = ntiles;
+  *launched = true;
+  long long wc = wait_limit_cycles();
+  int skip = fault_skip_loads();
+  void* args[] = {const_cast<DecodeParams*>(&p), &ntiles, &wc, &skip};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)grid), dim3(threads), args, smem, st);
+}
+
 template <typename T, typename TY, int N>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
+  if constexpr (N == 16 && sizeof(T) == 2) {
+    if (decode_streamed()) {
+      bool launched = false;
+      const cudaError_t e = launch_dec_stream<TY>(p, st, &launched);
+      if (e != cudaSuccess || launched) return e;
+    }
+  }
   const int64_t threads = p.batch * p.D * (N / (N >= 8 ? 8 : 4));  // 8 states per thread (4 for N = 4)
   dim3 grid((unsigned)((threads + 255) / 256)), block(256);
   void* args[] = {const_cast<DecodeParams*>(&p)};

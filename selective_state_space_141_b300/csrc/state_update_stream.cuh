@@ -1,0 +1,156 @@
+// state_update_stream.cuh -- the plain decode step (bf16 inputs, N = 16) as a streamed,
+// persistent kernel.
+//
+// Same step and the same arithmetic as state_update_kernel<bf16, TY, 16, false> ("8.7
+// State Space Models (Mamba)", section 5: O(1) work per generated token on a fixed d*n
+// state; "Mamba and State Space Models", "Selective scan pseudo-code", one iteration of
+// the loop body): for each channel (b, d)
+//   state[n] = exp(delta A[d,n]) state[n] + delta B[b,n] x,   y = (C[b] . state + D x) silu(z)
+//
+// The step reads and writes the whole fp32 state once, so its time is the time to move
+// those bytes. Here the bytes in flight per SM do not depend on the thread count: one
+// producer thread per CTA streams tiles of kDecTile consecutive channels (their state and
+// A rows, x, delta, z and the batch row's B and C) into a ring of kDecStages shared-memory
+// stages with 1-D bulk copies, completion counted on an mbarrier per stage; the consumer
+// threads update a tile from shared memory, write the state back with 16-byte stores and
+// release the stage. CTAs are persistent (a fixed grid walks all tiles), so there is no
+// tail of short-lived blocks. Every wait is bounded (tma.cuh).
+#pragma once
+
+#include "common.cuh"
+#include "state_update.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+
+// Tile and ring depth measured on the 2.8B-shaped decode step (256 x 5120): 128 channels
+// x 2 stages (17 KB each; several CTAs per SM) 29.9 us per step; 64 x 4: 31.6; 64 x 8:
+// 37.2; 256 x 3: 30.6; 128 x 1 (no overlap): 34.8.
+constexpr int kDecTile = 128;                 // channels per tile (D % kDecTile == 0)
+constexpr int kDecStages = 2;                 // tiles in flight per CTA
+constexpr int kDecConsumers = 2 * kDecTile;   // two threads per channel, 8 states each
+
+struct alignas(16) DecStage {
+  float state[kDecTile * 16];
+  float A[kDecTile * 16];
+  __nv_bfloat16 x[kDecTile];
+  __nv_bfloat16 dl[kDecTile];
+  __nv_bfloat16 z[kDecTile];
+  __nv_bfloat16 B[16];
+  __nv_bfloat16 C[16];
+};
+static_assert(sizeof(DecStage) % 16 == 0, "stage members start 16-byte aligned");
+
+constexpr int dec_stream_smem_bytes() { return kDecStages * (int)sizeof(DecStage) + 2 * kDecStages * 8; }
+
+// Eight bf16 values (one 16-byte vector) to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// grid: persistent (a multiple of the SM count, at most one CTA per tile); block:
+// kDecConsumers consumer threads + one producer warp.
+// wait_cycles: the limit of every wait (0: the default); skip_loads (failure-detection
+// tests only): the producer issues no copies, so every consumer wait runs out.
+template <typename TY>
+__global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const DecodeParams p, int64_t ntiles,
+                                                                          long long wait_cycles, int skip_loads) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  DecStage* stg = reinterpret_cast<DecStage*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDecStages * sizeof(DecStage));
+  uint64_t* empty = full + kDecStages;
+  const int tid = threadIdx.x;
+  const long long lim = wait_cycles > 0 ? wait_cycles : kWaitCycles;
+  constexpr int N = 16;
+  if (tid == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecConsumers / 32);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const int64_t D = p.D;
+  if (tid >= kDecConsumers) {  // ---------------- producer ----------------
+    if (tid == kDecConsumers && !skip_loads) {
+      const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+      const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.delta);
+      const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(p.z);
+      const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
+      const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(p.C);
+      const uint32_t tx = 2 * kDecTile * N * 4 + (z ? 3 : 2) * kDecTile * 2 + 2 * N * 2;
+      int i = 0;
+      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        const int s = i % kDecStages;
+        if (i >= kDecStages && !mbar_wait(&empty[s], ((i / kDecStages) - 1) & 1, kErrWaitEmpty, lim)) break;
+        DecStage& sg = stg[s];
+        const int64_t c0 = tile * kDecTile, b = c0 / D, d0 = c0 - b * D;
+        mbar_arrive_expect_tx(&full[s], tx);
+        bulk_load(sg.state, p.state + c0 * N, kDecTile * N * 4, &full[s]);
+        bulk_load(sg.A, p.A + d0 * N, kDecTile * N * 4, &full[s]);
+        bulk_load(sg.x, x + c0, kDecTile * 2, &full[s]);
+        bulk_load(sg.dl, dl + c0, kDecTile * 2, &full[s]);
+        if (z) bulk_load(sg.z, z + c0, kDecTile * 2, &full[s]);
+        bulk_load(sg.B, B + b * N, N * 2, &full[s]);
+        bulk_load(sg.C, C + b * N, N * 2, &full[s]);
+      }
+      // Wait (bounded) for the copies still in flight before leaving.
+      const int issued = i;
+      for (int k = (issued > kDecStages ? issued - kDecStages : 0); k < issued; ++k)
+        if (!mbar_wait(&full[k % kDecStages], (k / kDecStages) & 1, kErrWaitFull, lim)) break;
+    }
+    return;
+  }
+
+  // ---------------- consumers: thread = (channel j of the tile, state half g) ----------------
+  const int j = tid >> 1, g = tid & 1, lane = tid & 31;
+  int i = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+    const int s = i % kDecStages;
+    if (!mbar_wait(&full[s], (i / kDecStages) & 1, kErrWaitFull, lim)) break;
+    const DecStage& sg = stg[s];
+    const int64_t c0 = tile * kDecTile, bd = c0 + j, d = (c0 - (c0 / D) * D) + j;
+    const float x = __bfloat162float(sg.x[j]);
+    const float dt = __bfloat162float(sg.dl[j]);
+    const float zz = p.z ? __bfloat162float(sg.z[j]) : 0.f;
+    const float dx = dt * x;
+    const float4* sp = reinterpret_cast<const float4*>(sg.state + j * N + g * 8);
+    const float4* ap = reinterpret_cast<const float4*>(sg.A + j * N + g * 8);
+    float sv[8], av[8], Bv[8], Cv[8];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float4 s4 = sp[q], a4 = ap[q];
+      sv[4 * q] = s4.x; sv[4 * q + 1] = s4.y; sv[4 * q + 2] = s4.z; sv[4 * q + 3] = s4.w;
+      av[4 * q] = a4.x; av[4 * q + 1] = a4.y; av[4 * q + 2] = a4.z; av[4 * q + 3] = a4.w;
+    }
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(sg.B)[g], Bv);
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(sg.C)[g], Cv);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage is read: release it to the producer
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a = decay<false>(dt, av[k], av[k] * kLog2e);
+      sv[k] = fmaf(a, sv[k], dx * Bv[k]);
+      acc = fmaf(Cv[k], sv[k], acc);
+    }
+    float4* out = reinterpret_cast<float4*>(p.state + bd * N + g * 8);
+    out[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    out[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (g == 0) {
+      float o = acc;
+      if (p.Dskip) o = fmaf(p.Dskip[d], x, o);
+      if (p.z) o *= silu_precise(zz);
+      static_cast<TY*>(p.y)[bd] = from_f32<TY>(o);
+    }
+  }
+}
+
+}  // namespace ssm

@@ -135,3 +135,36 @@ def test_prefix_state_then_decode():
                              z=d["z"][:, t].contiguous())
         check(y, y_all[:, t], TOL_F32, False, f"y t={t}")
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("gate", [True, False], ids=["z-D", "bare"])
+@pytest.mark.parametrize("y_dtype", [torch.bfloat16, torch.float32], ids=["y-bf16", "y-f32"])
+def test_decode_streamed_kernel(gate, y_dtype, monkeypatch):
+    """The streamed decode kernel (bf16, N = 16, D a multiple of its 128-channel tile)
+    against the oracle over several steps, and bit for bit against the one-thread-per-8-
+    states kernel (SSM_B300_DECODE=plain) on the same inputs."""
+    b, Dm, N = 5, 256, 16
+    w = inputs.DecodeWorkload("t", b, Dm, N, 4, torch.bfloat16, 41)
+    d = inputs.decode_inputs(w, DEV)
+    g = torch.Generator(device="cpu").manual_seed(42)
+    s0 = torch.randn(b, Dm, N, generator=g).to(DEV)
+    kw = lambda t: dict(D=d["D"] if gate else None, z=d["z"][t] if gate else None, y_dtype=y_dtype)
+    runs = {}
+    for mode in ("stream", "plain"):
+        if mode == "plain":
+            monkeypatch.setenv("SSM_B300_DECODE", "plain")
+        state = s0.clone()
+        ys = [ssm.state_update(state, d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t], **kw(t))
+              for t in range(w.steps)]
+        torch.cuda.synchronize()
+        runs[mode] = (ys, state)
+    monkeypatch.delenv("SSM_B300_DECODE")
+    for t in range(w.steps):
+        assert torch.equal(runs["stream"][0][t], runs["plain"][0][t]), t
+    assert torch.equal(runs["stream"][1], runs["plain"][1])
+    st_ref = to64(s0)
+    for t in range(w.steps):
+        args = (d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t])
+        yr, st_ref = oracle.state_update(st_ref, *args, D=d["D"] if gate else None, z=d["z"][t] if gate else None)
+        check(runs["stream"][0][t], yr, TOL_BF16, y_dtype == torch.bfloat16, f"y step {t}")
+    check(runs["stream"][1], st_ref, TOL_BF16, False, "state")

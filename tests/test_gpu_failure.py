@@ -1,11 +1,12 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-The channel kernel's waits on its mbarriers are bounded; a wait that runs out records an
-error code in the library's device error word and the kernel returns (no trap, no hang).
-Here the staging warp is told to issue no copies (SSM_B300_FAULT_INJECT=skip_loads) and
-the wait limit is cut to 2e5 cycles (about 0.1 ms), so every wait for data runs out. The
-test checks that the call returns, that ssm_device_error reports a "data never arrived"
-code, and that a following normal call on the same context is correct.
+The channel kernel's and the streamed decode kernel's waits on their mbarriers are
+bounded; a wait that runs out records an error code in the library's device error word and
+the kernel returns (no trap, no hang). Here the staging thread is told to issue no copies
+(SSM_B300_FAULT_INJECT=skip_loads) and the wait limit is cut to 2e5 cycles (about 0.1
+ms), so every wait for data runs out. The tests check that the call returns, that
+ssm_device_error reports a "data never arrived" code, and that a following normal call
+on the same context is correct.
 """
 import os
 
@@ -50,3 +51,28 @@ def test_short_limit_alone_does_not_fire(monkeypatch):
     monkeypatch.setenv("SSM_B300_WAIT_LIMIT_CYCLES", "2000000")
     _fwd(d)
     assert ssm.device_error() == 0
+
+
+def test_decode_wait_runs_out_and_context_recovers(monkeypatch):
+    """The streamed decode kernel's waits: with no copies issued every consumer wait runs
+    out, the step returns with a 'data never arrived' code, and a following normal step
+    on the same context matches the oracle."""
+    w = inputs.DecodeWorkload("t", 4, 256, 16, 1, torch.bfloat16, 73)  # streamed-kernel shape
+    d = inputs.decode_inputs(w, DEV)
+    g = torch.Generator(device="cpu").manual_seed(74)
+    s0 = torch.randn(4, 256, 16, generator=g).to(DEV)
+    args = (d["x"][0], d["delta"][0], d["A"], d["B"][0], d["C"][0])
+    assert ssm.device_error() == 0
+    monkeypatch.setenv("SSM_B300_FAULT_INJECT", "skip_loads")
+    monkeypatch.setenv("SSM_B300_WAIT_LIMIT_CYCLES", "200000")
+    state = s0.clone()
+    ssm.state_update(state, *args, D=d["D"], z=d["z"][0])
+    assert ssm.device_error() == 1
+    monkeypatch.delenv("SSM_B300_FAULT_INJECT")
+    monkeypatch.delenv("SSM_B300_WAIT_LIMIT_CYCLES")
+    state = s0.clone()
+    y = ssm.state_update(state, *args, D=d["D"], z=d["z"][0])
+    assert ssm.device_error() == 0
+    yr, sr = oracle.state_update(s0, *args, D=d["D"], z=d["z"][0])
+    check(y, yr, TOL_BF16, True, "y after recovery")
+    check(state, sr, TOL_BF16, False, "state after recovery")
