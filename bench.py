@@ -504,33 +504,66 @@ def e2e(w, d, args, ssm, torch, stream):
 
 def backward_bench(args, ssm, torch, w, d, dev, fwd_launch_ms):
     """The backward pass (all gradients) on the same workload, bf16 dy, CUDA events around
-    each call (two launches: the sweep kernel and the fixed-order reduction)."""
+    each call. Standalone (`ms`): three launches, the checkpoint pass (the channel kernel's
+    recurrence without read-out), the reverse kernel and the fixed-order reduction. In a
+    training step (`training_step`): the forward pass writes the checkpoints itself
+    (ssm_selective_scan_fwd_train) and the backward pass is the last two launches."""
     g = torch.Generator(device=dev).manual_seed(5)
     dy = torch.randn(d["u"].shape, generator=g, device=dev).to(d["u"].dtype)
     nbytes = ssm.bwd_workspace_size(w.batch, w.L, w.D, w.N)
     wsp = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty(d["u"].shape, dtype=d["u"].dtype, device=dev)
+    last = torch.empty((w.batch, w.D, w.N), dtype=torch.float32, device=dev)
+    written = [False]
 
-    def call():
+    def bwd(ready=False):
         return ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, D=d["D"], z=d["z"],
-                                      delta_bias=d["delta_bias"], delta_softplus=True, workspace=wsp)
+                                      delta_bias=d["delta_bias"], delta_softplus=True, workspace=wsp,
+                                      checkpoints_ready=ready)
 
-    for _ in range(2):
-        call()
-    torch.cuda.synchronize()
-    ms = []
-    for _ in range(args.bwd_steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        call()
-        e1.record()
+    def fwd_train():
+        written[0] = ssm.selective_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], wsp, D=d["D"], z=d["z"],
+                                                  delta_bias=d["delta_bias"], delta_softplus=True, y=y,
+                                                  last_state=last)[2]
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
         torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        ms = []
+        for _ in range(args.bwd_steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    m = timed(bwd)
+    # training step: the forward pass with checkpoints, then the backward pass that uses them
+    mf = timed(fwd_train)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    mfb, mb = [], []
+    for _ in range(args.bwd_steps):
+        ev[0].record()
+        fwd_train()
+        ev[1].record()
+        bwd(ready=written[0])
+        ev[2].record()
+        torch.cuda.synchronize()
+        mfb.append(ev[0].elapsed_time(ev[2]))
+        mb.append(ev[1].elapsed_time(ev[2]))
     if ssm.device_error() != 0:
         raise RuntimeError("device error word set during the backward pass")
-    m = statistics.median(ms)
+    mb_med = statistics.median(mb)
     return {"workload": w.name, "ms": m, "ratio_to_forward": m / fwd_launch_ms, "elem_per_s": w.elems / (m / 1e3),
-            "calls": args.bwd_steps, "workspace_bytes": nbytes, "launches_per_call": 2,
-            "gradients": "du, ddelta, dA, dB, dC, dD, dz, dbias (bf16 dy; fp32 accumulation)"}
+            "calls": args.bwd_steps, "workspace_bytes": nbytes, "launches_per_call": 3,
+            "gradients": "du, ddelta, dA, dB, dC, dD, dz, dbias (bf16 dy; fp32 accumulation)",
+            "training_step": {"forward_with_checkpoints_ms": mf, "backward_ms": mb_med,
+                              "backward_ratio_to_forward": mb_med / fwd_launch_ms,
+                              "forward_plus_backward_ms": statistics.median(mfb),
+                              "checkpoints_written": bool(written[0]), "backward_launches": 2}}
 
 
 def ssd_bench(args, ssm, torch, inputs, dev, peaks):

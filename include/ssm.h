@@ -13,7 +13,9 @@
  *   ssm_conv_selective_scan_fwd, ssm_conv_state_update
  *                            the same two with the block's causal width-4 depthwise
  *                            conv + SiLU (the step before the SSM) fused in front
- *   ssm_selective_scan_bwd   the backward pass of the forward pass (all gradients)
+ *   ssm_selective_scan_bwd   the backward pass of the forward pass (all gradients);
+ *                            ssm_selective_scan_fwd_train + ssm_selective_scan_bwd_ex:
+ *                            the forward pass writing the backward's state checkpoints
  *   ssm_ssd_fwd              the Mamba-2 SSD forward pass (scalar decay per head,
  *                            chunked, tensor cores)
  *
@@ -366,6 +368,58 @@ SSM_API ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_ten
                                             ssm_tensor_t* dB, ssm_tensor_t* dC, ssm_tensor_t* dD,
                                             ssm_tensor_t* dz, ssm_tensor_t* dbias, ssm_tensor_t* dh0,
                                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ssm_selective_scan_fwd_train -- the forward pass of a training step: y and last_state
+ * exactly as ssm_selective_scan_fwd_ex (flags 0) with h0, plus, into the checkpoint region
+ * of a backward workspace, the state before every 16-step chunk that the backward pass
+ * recomputes its states from ("Mamba and State Space Models", "Hardware-Aware Parallel
+ * Scan": the states are not stored, they are recomputed in the backward pass; storing one
+ * state per chunk bounds that recomputation to one chunk).
+ *
+ *   u ... h0, y, last_state   as ssm_selective_scan_fwd_ex
+ *   bwd_workspace             at least ssm_selective_scan_bwd_workspace_size bytes for this
+ *                             shape, 256-byte aligned, overlapping no tensor; pass the same
+ *                             buffer to ssm_selective_scan_bwd_ex for this step
+ *   checkpoints_written       out: 1 when the checkpoints were written (bf16 inputs, N = 8
+ *                             or 16, the channel kernel's alignment: 16-byte aligned rows,
+ *                             D % 8 == 0), else 0 (y is computed all the same; the backward
+ *                             pass then makes its own checkpoints: call it without
+ *                             SSM_BWD_CHECKPOINTS)
+ * Errors as ssm_selective_scan_fwd_ex; SSM_ERR_NULL (checkpoints_written or, for a
+ * non-empty problem, bwd_workspace NULL), SSM_ERR_LAYOUT (misaligned or overlapping
+ * workspace), SSM_ERR_SHAPE (workspace too short).
+ */
+SSM_API ssm_status_t ssm_selective_scan_fwd_train(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                                  const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                                  const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                                  const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                                  int delta_softplus, const ssm_tensor_t* h0,
+                                                  ssm_tensor_t* y, ssm_tensor_t* last_state,
+                                                  void* bwd_workspace, size_t bwd_workspace_bytes,
+                                                  int32_t* checkpoints_written, void* stream);
+
+#define SSM_BWD_CHECKPOINTS 1u /* the workspace holds ssm_selective_scan_fwd_train's checkpoints */
+
+/*
+ * ssm_selective_scan_bwd_ex -- ssm_selective_scan_bwd with flags. flags & SSM_BWD_CHECKPOINTS:
+ * the workspace's checkpoint region already holds the checkpoints of this step's forward
+ * pass (ssm_selective_scan_fwd_train reported checkpoints_written = 1 for the same inputs,
+ * h0 and workspace, and nothing wrote the workspace since), so the checkpoint pass is
+ * skipped. Results are identical to ssm_selective_scan_bwd. Other flag bits:
+ * SSM_ERR_UNSUPPORTED. ssm_selective_scan_bwd(...) is ssm_selective_scan_bwd_ex(..., 0, ...).
+ */
+SSM_API ssm_status_t ssm_selective_scan_bwd_ex(const ssm_tensor_t* u, const ssm_tensor_t* delta,
+                                               const ssm_tensor_t* A, const ssm_tensor_t* B,
+                                               const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                               const ssm_tensor_t* z, const ssm_tensor_t* delta_bias,
+                                               int delta_softplus, const ssm_tensor_t* h0,
+                                               const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
+                                               ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA,
+                                               ssm_tensor_t* dB, ssm_tensor_t* dC, ssm_tensor_t* dD,
+                                               ssm_tensor_t* dz, ssm_tensor_t* dbias, ssm_tensor_t* dh0,
+                                               uint32_t flags, void* workspace, size_t workspace_bytes,
+                                               void* stream);
 
 /* Bytes of workspace ssm_selective_scan_bwd needs for this shape (0 for an empty problem):
  * the state before every 16-step chunk, per-warp partial sums of dB and dC, and per-row

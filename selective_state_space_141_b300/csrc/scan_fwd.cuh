@@ -57,7 +57,8 @@ struct FwdParams {
   // TMA issuer issues no copy, so every wait for data runs out and reports its code.
   long long wait_cycles;
   int fault_skip_loads;
-  // State checkpoints (channel kernel's aggregate pass, one segment): when set, the state before every
+  // State checkpoints (channel kernel: the aggregate pass over one segment, or the full
+  // pass of a training forward): when set, the state before every
   // kCkSteps-step chunk c of the sequence is written to ck[b][c][D][N] (f32), c < ck_nc.
   // The backward pass recomputes each chunk's states from these.
   float* ck;

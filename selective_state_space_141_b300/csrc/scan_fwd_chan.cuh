@@ -216,11 +216,13 @@ __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const
   }
 }
 
-// kAgg = false: the full pass (y, and last_state from the last segment).
-// kAgg = true:  the aggregate pass of a segmented scan (seg_E, seg_P; no y).
+// kAgg = false: the full pass (y, and last_state from the last segment); with kCk it also
+//               writes the state checkpoints (p.ck) for the backward pass.
+// kAgg = true:  the aggregate pass of a segmented scan (seg_E, seg_P; no y), or of one
+//               segment writing the checkpoints only.
 // blockIdx = (channel block of 128, batch row, sequence segment).
 // kConv: the u tensor holds the conv input x; u is its causal conv + SiLU (ConvLane).
-template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg, bool kConv>
+template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg, bool kConv, bool kCk = false>
 __global__ void __launch_bounds__(kChanThreads, 1)
 scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -365,9 +367,10 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     const float* bc = reinterpret_cast<const float*>(st + 3 * Lay::kTileIO + 2 * Lay::kTileBC);
     const int64_t tk = t_begin + (int64_t)k * TC;
     const int tc = (int)((t_end - tk) < TC ? (t_end - tk) : TC);
-    // Aggregate pass: the state before step tk + t0, when that step starts a checkpoint chunk.
+    // Checkpoints (the aggregate pass, or the full pass with kCk): the state before step
+    // tk + t0, when that step starts a checkpoint chunk.
     auto checkpoint = [&](int t0) {
-      if (kAgg && p.ck && vd && t0 % kCkSteps == 0) {
+      if ((kAgg || kCk) && p.ck && vd && t0 % kCkSteps == 0) {
         float4* c4 = reinterpret_cast<float4*>(p.ck + (((int64_t)b * p.ck_nc + (tk + t0) / kCkSteps) * D + d) * N);
 #pragma unroll
         for (int q = 0; q < N / 4; ++q) c4[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
@@ -397,11 +400,15 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       __syncwarp();
     }
     if (tc == TC) {
-      for (int t0 = 0; t0 < TC; t0 += kChanSub)
+      for (int t0 = 0; t0 < TC; t0 += kChanSub) {
+        checkpoint(t0);
         chan_subchunk<TY, N, kSoftplus, kGate, false, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
+      }
     } else {
-      for (int t0 = 0; t0 < tc; t0 += kChanSub)
+      for (int t0 = 0; t0 < tc; t0 += kChanSub) {
+        checkpoint(t0);
         chan_subchunk<TY, N, kSoftplus, kGate, true, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
+      }
     }
     // Release the input stage, then send this chunk's y tile (rows past L and columns
     // past D are clipped by the TMA store; segments start on chunk boundaries).

@@ -144,9 +144,9 @@ bool chan_eligible(const FwdParams& p, int64_t N) {
          aligned16(p.last_state) && encode_fn() != nullptr;
 }
 
-template <typename TY, int N, bool kSP, bool kZ, bool kAgg, bool kConv>
+template <typename TY, int N, bool kSP, bool kZ, bool kAgg, bool kConv, bool kCk = false>
 cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st) {
-  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg, kConv>;
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg, kConv, kCk>;
   constexpr int smem = ssm::chan_smem_bytes<TY, N, kChanTC, kChanStages>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -245,6 +245,14 @@ cudaError_t launch_carry(const ssm::SegY& sy, const float* E, const float* P, co
 template <typename TY, int N, bool kAgg, bool kConv>
 cudaError_t launch_chan_sz(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st, bool sp, bool z) {
   if (kAgg) z = false;
+  if constexpr (!kAgg && !kConv) {
+    if (p.ck) {  // the full pass of a training forward: y and the backward's checkpoints
+      if (sp && z) return launch_chan_k<TY, N, true, true, false, false, true>(p, maps, nseg, st);
+      if (sp) return launch_chan_k<TY, N, true, false, false, false, true>(p, maps, nseg, st);
+      if (z) return launch_chan_k<TY, N, false, true, false, false, true>(p, maps, nseg, st);
+      return launch_chan_k<TY, N, false, false, false, false, true>(p, maps, nseg, st);
+    }
+  }
   if (sp && z) return launch_chan_k<TY, N, true, !kAgg, kAgg, kConv>(p, maps, nseg, st);
   if (sp) return launch_chan_k<TY, N, true, false, kAgg, kConv>(p, maps, nseg, st);
   if (z) return launch_chan_k<TY, N, false, !kAgg, kAgg, kConv>(p, maps, nseg, st);
@@ -289,7 +297,9 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     p.seg_h0 = nullptr;
     p.seg_y = p0.y;
     p.seg_y_bf16 = sizeof(TY) == 2 ? 1 : 0;
-    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
+    FwdParams pa = p;
+    pa.ck = nullptr;  // the aggregate pass starts every segment from zero: no checkpoints
+    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(pa, maps, nseg - 1, st, sp, false);
     if (e != cudaSuccess) return e;
     const ssm::SegY sy{p0.y, p.seg_y_bf16, p0.L, p0.D, plan.seg_len, N};
     e = launch_carry(sy, nullptr, nullptr, p0.h0, nullptr, nseg, p0.batch * p0.D * N, st);
@@ -305,7 +315,9 @@ cudaError_t launch_chan(const FwdParams& p0, const SegPlan& plan, void* ws, cuda
     p.seg_h0 = nullptr;  // the aggregate pass runs every segment from zero; h0 enters in the carry scan
     p.seg_E = E;
     p.seg_P = P;
-    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(p, maps, nseg - 1, st, sp, false);
+    FwdParams pa = p;
+    pa.ck = nullptr;
+    cudaError_t e = launch_chan_sw<__nv_bfloat16, N, true>(pa, maps, nseg - 1, st, sp, false);
     if (e != cudaSuccess) return e;
     e = launch_carry(ssm::SegY{}, E, P, p0.h0, H, nseg, p0.batch * p0.D * N, st);
     if (e != cudaSuccess) return e;
@@ -524,11 +536,19 @@ ssm_status_t finish_fwd(cudaError_t e, const FwdParams& p, ssm_dtype_t io, ssm_t
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// The backward pass's checkpoint region, for a training forward (written only by the
+// channel kernel: *written = 1 when it ran).
+struct CkArgs {
+  float* ck;
+  int64_t nc;
+  int32_t* written;
+};
+
 ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A, const ssm_tensor_t* B,
                       const ssm_tensor_t* C, const ssm_tensor_t* D, const ssm_tensor_t* z,
                       const ssm_tensor_t* delta_bias, int delta_softplus, const ssm_tensor_t* h0, uint32_t flags,
                       ssm_tensor_t* y, ssm_tensor_t* last_state, void* workspace, size_t workspace_bytes,
-                      void* stream, const ConvArgs* conv = nullptr) {
+                      void* stream, const ConvArgs* conv = nullptr, const CkArgs* ck = nullptr) {
   if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
   if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
   const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
@@ -626,8 +646,8 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
   p.seg_y_bf16 = 0;
   p.wait_cycles = wait_limit_cycles();
   p.fault_skip_loads = fault_skip_loads();
-  p.ck = nullptr;
-  p.ck_nc = 0;
+  p.ck = ck ? ck->ck : nullptr;
+  p.ck_nc = ck ? ck->nc : 0;
 
   cudaError_t e;
   const FwdVariant var = forward_variant();
@@ -642,6 +662,7 @@ ssm_status_t fwd_impl(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ss
     bool launched = false;
     e = y->dtype == SSM_BF16 ? launch_chan_n<__nv_bfloat16>(N, p, plan, use_ws ? workspace : nullptr, st, &launched)
                              : launch_chan_n<float>(N, p, plan, use_ws ? workspace : nullptr, st, &launched);
+    if (ck && launched && e == cudaSuccess) *ck->written = 1;
     if (launched || e != cudaSuccess) return finish_fwd(e, p, io, cst, st);
   }
   if (io == SSM_F32)
@@ -896,13 +917,15 @@ ssm_status_t ssm_selective_scan_bwd_workspace_size(int64_t batch, int64_t L, int
   return SSM_OK;
 }
 
-ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
-                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
-                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
-                                    const ssm_tensor_t* h0, const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
-                                    ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA, ssm_tensor_t* dB,
-                                    ssm_tensor_t* dC, ssm_tensor_t* dD, ssm_tensor_t* dz, ssm_tensor_t* dbias,
-                                    ssm_tensor_t* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+ssm_status_t ssm_selective_scan_bwd_ex(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                       const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                       const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                       const ssm_tensor_t* h0, const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
+                                       ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA, ssm_tensor_t* dB,
+                                       ssm_tensor_t* dC, ssm_tensor_t* dD, ssm_tensor_t* dz, ssm_tensor_t* dbias,
+                                       ssm_tensor_t* dh0, uint32_t flags, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (flags & ~SSM_BWD_CHECKPOINTS) return SSM_ERR_UNSUPPORTED;
   if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return SSM_ERR_NULL;
   if ((D != nullptr) != (dD != nullptr) || (z != nullptr) != (dz != nullptr) ||
       (delta_bias != nullptr) != (dbias != nullptr))
@@ -1014,8 +1037,8 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   }
 
   cudaError_t e;
-  p.ck_ready = 0;
-  if (io == SSM_BF16 && (N == 8 || N == 16) && forward_variant() != FwdVariant::kGeneric) {
+  p.ck_ready = (flags & SSM_BWD_CHECKPOINTS) ? 1 : 0;  // written by ssm_selective_scan_fwd_train
+  if (!p.ck_ready && io == SSM_BF16 && (N == 8 || N == 16) && forward_variant() != FwdVariant::kGeneric) {
     // The checkpoints from the channel kernel (as the forward pass's fast path)
     FwdParams fp{};
     fp.u = u->data;
@@ -1050,6 +1073,50 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* d
   e = gt == SSM_BF16 ? launch_bwd_reduce<__nv_bfloat16>(p, N, dB->data, dC->data, dAp, dDp, dbp, st)
                      : launch_bwd_reduce<float>(p, N, dB->data, dC->data, dAp, dDp, dbp, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status_t ssm_selective_scan_bwd(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                    const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                    const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                    const ssm_tensor_t* h0, const ssm_tensor_t* dy, const ssm_tensor_t* dlast,
+                                    ssm_tensor_t* du, ssm_tensor_t* ddelta, ssm_tensor_t* dA, ssm_tensor_t* dB,
+                                    ssm_tensor_t* dC, ssm_tensor_t* dD, ssm_tensor_t* dz, ssm_tensor_t* dbias,
+                                    ssm_tensor_t* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+  return ssm_selective_scan_bwd_ex(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dy, dlast, du, ddelta, dA,
+                                   dB, dC, dD, dz, dbias, dh0, 0u, workspace, workspace_bytes, stream);
+}
+
+ssm_status_t ssm_selective_scan_fwd_train(const ssm_tensor_t* u, const ssm_tensor_t* delta, const ssm_tensor_t* A,
+                                          const ssm_tensor_t* B, const ssm_tensor_t* C, const ssm_tensor_t* D,
+                                          const ssm_tensor_t* z, const ssm_tensor_t* delta_bias, int delta_softplus,
+                                          const ssm_tensor_t* h0, ssm_tensor_t* y, ssm_tensor_t* last_state,
+                                          void* bwd_workspace, size_t bwd_workspace_bytes,
+                                          int32_t* checkpoints_written, void* stream) {
+  if (!checkpoints_written || !u || !A) return SSM_ERR_NULL;
+  *checkpoints_written = 0;
+  if (u->ndim != 3 || A->ndim != 2) return SSM_ERR_SHAPE;
+  const int64_t batch = u->shape[0], L = u->shape[1], Dm = u->shape[2], N = A->shape[1];
+  if (batch < 0 || L < 0 || Dm < 0 || N < 0) return SSM_ERR_SHAPE;
+  const bool empty = batch == 0 || L == 0 || Dm == 0 || !n_supported(N);
+  CkArgs ck{nullptr, 0, checkpoints_written};
+  if (!empty) {
+    const BwdPlan pl = plan_bwd(batch, L, Dm, N);
+    if (!bwd_workspace) return SSM_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(bwd_workspace) % 256 != 0) return SSM_ERR_LAYOUT;
+    if (bwd_workspace_bytes < pl.bytes) return SSM_ERR_SHAPE;
+    ssm_tensor_t w{};
+    w.data = bwd_workspace;
+    w.dtype = SSM_F32;
+    w.ndim = 1;
+    w.shape[0] = (int64_t)(bwd_workspace_bytes / 4);
+    for (const ssm_tensor_t* t : {u, delta, A, B, C, D, z, delta_bias, h0, static_cast<const ssm_tensor_t*>(y),
+                                  static_cast<const ssm_tensor_t*>(last_state)})
+      if (t && overlaps(&w, t)) return SSM_ERR_LAYOUT;
+    ck.ck = reinterpret_cast<float*>(static_cast<unsigned char*>(bwd_workspace) + pl.off_ck);
+    ck.nc = pl.nc;
+  }
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, 0u, y, last_state, nullptr, 0, stream,
+                  nullptr, empty ? nullptr : &ck);
 }
 
 }  // extern "C"

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libssm_b300.so")
 
 SSM_F32, SSM_BF16 = 0, 1
 SSM_FWD_ZOH = 1  # flag of the extended entry points (include/ssm.h)
+SSM_BWD_CHECKPOINTS = 1  # the backward workspace holds the training forward's checkpoints
 _BAD_DTYPE = 99  # forwarded for any other torch dtype so the library reports SSM_ERR_DTYPE
 _DTYPES = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
 
@@ -72,6 +73,12 @@ def load_library(path: str | None = None):
     lib.ssm_selective_scan_bwd.restype = ctypes.c_int
     lib.ssm_selective_scan_bwd.argtypes = [_P] * 8 + [ctypes.c_int] + [_P] * 12 + [ctypes.c_void_p, ctypes.c_size_t,
                                                                                 ctypes.c_void_p]
+    lib.ssm_selective_scan_bwd_ex.restype = ctypes.c_int
+    lib.ssm_selective_scan_bwd_ex.argtypes = [_P] * 8 + [ctypes.c_int] + [_P] * 12 + [ctypes.c_uint32, ctypes.c_void_p,
+                                                                                   ctypes.c_size_t, ctypes.c_void_p]
+    lib.ssm_selective_scan_fwd_train.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_train.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P, _P, ctypes.c_void_p, ctypes.c_size_t,
+                                                             ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]
     lib.ssm_selective_scan_bwd_workspace_size.restype = ctypes.c_int
     lib.ssm_selective_scan_bwd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_ssd_fwd.restype = ctypes.c_int
@@ -191,13 +198,37 @@ def bwd_workspace_size(batch, L, D, N) -> int:
     return int(n.value)
 
 
+def selective_scan_fwd_train(u, delta, A, B, C, workspace, D=None, z=None, delta_bias=None, delta_softplus=True,
+                             h0=None, y=None, last_state=None, y_dtype=None, stream=None):
+    """Forward pass of a training step (``ssm_selective_scan_fwd_train``): y and last_state
+    as ``selective_scan_fwd`` and, into ``workspace`` (a uint8 tensor of
+    ``bwd_workspace_size(...)`` bytes, handed on to ``selective_scan_bwd``), the state
+    checkpoints of the backward pass. Returns (y, last_state, checkpoints_written)."""
+    lib = load_library()
+    if y is None:
+        y = torch.empty(u.shape, dtype=y_dtype or u.dtype, device=u.device)
+    if last_state is None:
+        last_state = torch.empty((u.shape[0], u.shape[2], A.shape[-1]), dtype=torch.float32, device=u.device)
+    ds = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    written = ctypes.c_int32(0)
+    ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_ptr else 0
+    st = lib.ssm_selective_scan_fwd_train(*[_ref(x) for x in ds], int(bool(delta_softplus)), _ref(describe(h0)),
+                                          _ref(describe(y)), _ref(describe(last_state)), ctypes.c_void_p(ws_ptr),
+                                          ctypes.c_size_t(ws_bytes), ctypes.byref(written), _stream(stream))
+    if st != 0:
+        raise SsmError(st, "ssm_selective_scan_fwd_train")
+    return y, last_state, bool(written.value)
+
+
 def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True, h0=None,
-                       dlast=None, want_dh0=False, workspace=None, stream=None):
-    """Backward pass (``ssm_selective_scan_bwd``): gradients of sum(dy * y) +
+                       dlast=None, want_dh0=False, workspace=None, stream=None, checkpoints_ready=False):
+    """Backward pass (``ssm_selective_scan_bwd_ex``): gradients of sum(dy * y) +
     sum(dlast * last_state). dy's dtype (the I/O dtype or fp32) is the dtype of du,
     ddelta, dz, dB, dC; dA, dD, dbias, dh0 are fp32. Returns a dict with du, ddelta, dA,
     dB, dC and, for the optional inputs given, dD, dz, dbias (dh0 when h0 is given or
-    ``want_dh0``)."""
+    ``want_dh0``). ``checkpoints_ready``: ``workspace`` holds the checkpoints that
+    ``selective_scan_fwd_train`` wrote for these inputs (it returned True)."""
     lib = load_library()
     batch, L, Dm = u.shape
     N = A.shape[-1]
@@ -218,10 +249,17 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, d
     ins = [describe(t) for t in (u, delta, A, B, C, D, z, delta_bias)]
     rest = [describe(t) for t in (h0, dy, dlast, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"],
                                   g["dbias"], g["dh0"])]
-    st = lib.ssm_selective_scan_bwd(*[_ref(d) for d in ins], int(bool(delta_softplus)), *[_ref(d) for d in rest],
-                                    ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes), _stream(stream))
+    if checkpoints_ready:
+        st = lib.ssm_selective_scan_bwd_ex(*[_ref(d) for d in ins], int(bool(delta_softplus)), *[_ref(d) for d in rest],
+                                           ctypes.c_uint32(SSM_BWD_CHECKPOINTS), ctypes.c_void_p(ws_ptr),
+                                           ctypes.c_size_t(ws_bytes), _stream(stream))
+        name = "ssm_selective_scan_bwd_ex"
+    else:
+        st = lib.ssm_selective_scan_bwd(*[_ref(d) for d in ins], int(bool(delta_softplus)), *[_ref(d) for d in rest],
+                                        ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes), _stream(stream))
+        name = "ssm_selective_scan_bwd"
     if st != 0:
-        raise SsmError(st, "ssm_selective_scan_bwd")
+        raise SsmError(st, name)
     return {k: v for k, v in g.items() if v is not None}
 
 

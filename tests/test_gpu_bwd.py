@@ -109,3 +109,27 @@ def test_bwd_layer_workload_sampled():
     check(gr["dA"].index_select(0, idx), r["dA"], TOL_BF16, False, "dA")
     for k in ("dD", "dbias"):
         check(gr[k].index_select(0, idx), r[k], TOL_BF16, False, k)
+
+
+@pytest.mark.parametrize("shape", [(2, 333, 200, 16), (3, 45, 64, 8), (2, 77, 100, 16), (1, 40, 48, 4)])
+def test_fwd_train_checkpoints_feed_bwd(shape):
+    """ssm_selective_scan_fwd_train: y and last_state bit for bit those of the forward pass
+    with the same h0; it writes the checkpoints exactly where the channel kernel runs (bf16,
+    N = 8 or 16, D % 8 == 0), and the backward pass given them (SSM_BWD_CHECKPOINTS) returns
+    the same gradients, bit for bit, as the backward pass that makes its own."""
+    b, L, Dm, N = shape
+    d = case(b, L, Dm, N, torch.bfloat16, seed=97 + L)
+    ws = torch.empty(ssm.bwd_workspace_size(b, L, Dm, N), dtype=torch.uint8, device=DEV)
+    kw = dict(D=d["D"], z=d["z"], delta_bias=d["delta_bias"], delta_softplus=True, h0=d["h0"])
+    y, last, written = ssm.selective_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], ws, **kw)
+    y0, last0 = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], use_workspace=False, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0) and torch.equal(last, last0)
+    assert written == (N in (8, 16) and Dm % 8 == 0)
+    g_own = run(d, torch.float32)
+    g_ck = ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["dy"].to(torch.float32), D=d["D"],
+                                  z=d["z"], delta_bias=d["delta_bias"], delta_softplus=True, h0=d["h0"],
+                                  dlast=d["dlast"], want_dh0=True, workspace=ws, checkpoints_ready=written)
+    torch.cuda.synchronize()
+    for k in g_own:
+        assert torch.equal(g_own[k], g_ck[k]), k
