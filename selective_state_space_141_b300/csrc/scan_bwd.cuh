@@ -378,24 +378,28 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       }
     }
     // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
-#pragma unroll 2
     const int64_t tl = t0 + kc - 1;
     TG* pdu = du + tl * D;
     TG* pddl = ddl + tl * D;
-    TG* pdz = dzp ? dzp + tl * D : nullptr;
+    TG* pdz = (dzp ? dzp : du) + tl * D;  // advanced always, written only with dz
     float* ppart = part + tl * pstride;
+    const float4* scp = sc + (kc - 1) * kBwdCh + ch;
+    const float2* sxp = sx + (kc - 1) * kBwdCh + ch;
+    const float* bcp = bc + (kc - 1) * 2 * N + nb;
+    const float2* hsp = hs2 + (kc - 1) * P2 * 32 + lane;
+#pragma unroll 2
     for (int k = kc - 1; k >= 0; --k) {
-      const float4 s = sc[k * kBwdCh + ch];  // dt, dt u, dv, u
-      const float2 sxv = sx[k * kBwdCh + ch];
+      const float4 s = *scp;  // dt, dt u, dv, u
+      const float2 sxv = *sxp;
       const float2 dt2 = make_float2(s.x, s.x), du2 = make_float2(s.y, s.y), dv2 = make_float2(s.z, s.z);
       float2 b2[P2], c2[P2];
-      load_pairs<P2>(bc + k * 2 * N + nb, b2);
-      load_pairs<P2>(bc + k * 2 * N + N + nb, c2);
+      load_pairs<P2>(bcp, b2);
+      load_pairs<P2>(bcp + N, c2);
       float2 vacc = make_float2(0.f, 0.f), sgB = make_float2(0.f, 0.f), sAg = make_float2(0.f, 0.f);
       float vr[NV];
 #pragma unroll
       for (int q = 0; q < P2; ++q) {
-        const float2 hp = hs2[(k * P2 + q) * 32 + lane];      // h_{t-1}
+        const float2 hp = hsp[q * 32];                        // h_{t-1}
         const float2 a = decay2<kAccurate>(dt2, Av[q], A2[q]);
         g[q] = __ffma2_rn(dv2, c2[q], g[q]);                  // g = dL/dh_t
         const float2 cv = __fmul2_rn(dv2, h[q]);              // dC_t: dv h_t
@@ -425,11 +429,15 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       if (lead) {
         *pdu = from_f32<TG>(dux);
         *pddl = from_f32<TG>(dr);
-        if (pdz) *pdz = from_f32<TG>(sxv.y * v);  // dz = dy v silu'(z)
+        if (dzp) *pdz = from_f32<TG>(sxv.y * v);  // dz = dy v silu'(z)
       }
       pdu -= D;
       pddl -= D;
-      if (pdz) pdz -= D;
+      pdz -= D;
+      scp -= kBwdCh;
+      sxp -= kBwdCh;
+      bcp -= 2 * N;
+      hsp -= P2 * 32;
       float sr;
       if constexpr (N == 16) {
         red_w[(2 * half) ^ fch] = make_float4(vr[0], vr[1], vr[2], vr[3]);
