@@ -430,17 +430,23 @@ cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
 template <typename TY>
 cudaError_t launch_dec_stream(const DecodeParams& p, cudaStream_t st, bool* launched) {
   *launched = false;
-  if (p.delta_bias || p.delta_softplus || p.zoh || p.conv_w || p.D % ssm::kDecTile != 0) return cudaSuccess;
-  for (const void* q : {static_cast<const void*>(p.state), p.x, p.delta, static_cast<const void*>(p.A), p.B, p.C, p.z})
+  if (p.zoh || p.conv_w || p.D % ssm::kDecTile != 0) return cudaSuccess;
+  for (const void* q : {static_cast<const void*>(p.state), p.x, p.delta, static_cast<const void*>(p.A), p.B, p.C, p.z,
+                        static_cast<const void*>(p.delta_bias)})
     if (!aligned16(q)) return cudaSuccess;
-  auto kern = &ssm::state_update_stream<TY>;
+  const bool map = p.delta_bias || p.delta_softplus;
+  auto kern = map ? &ssm::state_update_stream<TY, true> : &ssm::state_update_stream<TY, false>;
   constexpr int smem = ssm::dec_stream_smem_bytes();
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (attr != cudaSuccess) return attr;
+  static const cudaError_t attr0 = cudaFuncSetAttribute(
+      reinterpret_cast<const void*>(&ssm::state_update_stream<TY, false>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static const cudaError_t attr1 = cudaFuncSetAttribute(
+      reinterpret_cast<const void*>(&ssm::state_update_stream<TY, true>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr0 != cudaSuccess) return attr0;
+  if (attr1 != cudaSuccess) return attr1;
   constexpr int threads = ssm::kDecConsumers + 32;
-  static int per_sm = -1;
-  if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+  static int per_sm = -1;  // the same for both instantiations (same smem, threads, near registers)
+  if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, &ssm::state_update_stream<TY, true>, threads,
+                                                                   smem) != cudaSuccess ||
                      per_sm < 1))
     per_sm = 1;
   int64_t ntiles = p.batch * p.D / ssm::kDecTile;

@@ -1,11 +1,12 @@
-// state_update_stream.cuh -- the plain decode step (bf16 inputs, N = 16) as a streamed,
-// persistent kernel.
+// state_update_stream.cuh -- the decode step (bf16 inputs, N = 16; plain, or with the
+// forward pass's step-size map) as a streamed, persistent kernel.
 //
-// Same step and the same arithmetic as state_update_kernel<bf16, TY, 16, false> ("8.7
+// Same step and the same arithmetic as state_update_kernel<bf16, TY, 16, kExt> ("8.7
 // State Space Models (Mamba)", section 5: O(1) work per generated token on a fixed d*n
 // state; "Mamba and State Space Models", "Selective scan pseudo-code", one iteration of
-// the loop body): for each channel (b, d)
-//   state[n] = exp(delta A[d,n]) state[n] + delta B[b,n] x,   y = (C[b] . state + D x) silu(z)
+// the loop body): for each channel (b, d), with dt = delta (kMap: softplus(delta + bias[d])
+// or delta + bias[d] as the forward pass maps it)
+//   state[n] = exp(dt A[d,n]) state[n] + dt B[b,n] x,   y = (C[b] . state + D x) silu(z)
 //
 // The step reads and writes the whole fp32 state once, so its time is the time to move
 // those bytes. Here the bytes in flight per SM do not depend on the thread count: one
@@ -38,6 +39,7 @@ struct alignas(16) DecStage {
   __nv_bfloat16 z[kDecTile];
   __nv_bfloat16 B[16];
   __nv_bfloat16 C[16];
+  float bias[kDecTile];  // kMap with delta_bias only
 };
 static_assert(sizeof(DecStage) % 16 == 0, "stage members start 16-byte aligned");
 
@@ -57,7 +59,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 // kDecConsumers consumer threads + one producer warp.
 // wait_cycles: the limit of every wait (0: the default); skip_loads (failure-detection
 // tests only): the producer issues no copies, so every consumer wait runs out.
-template <typename TY>
+// kMap: the step-size map (delta_bias, delta_softplus) is compiled in.
+template <typename TY, bool kMap>
 __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const DecodeParams p, int64_t ntiles,
                                                                           long long wait_cycles, int skip_loads) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -84,7 +87,8 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
       const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(p.z);
       const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
       const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(p.C);
-      const uint32_t tx = 2 * kDecTile * N * 4 + (z ? 3 : 2) * kDecTile * 2 + 2 * N * 2;
+      const bool bias = kMap && p.delta_bias;
+      const uint32_t tx = 2 * kDecTile * N * 4 + (z ? 3 : 2) * kDecTile * 2 + 2 * N * 2 + (bias ? kDecTile * 4 : 0);
       int i = 0;
       for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
         const int s = i % kDecStages;
@@ -99,6 +103,7 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
         if (z) bulk_load(sg.z, z + c0, kDecTile * 2, &full[s]);
         bulk_load(sg.B, B + b * N, N * 2, &full[s]);
         bulk_load(sg.C, C + b * N, N * 2, &full[s]);
+        if (bias) bulk_load(sg.bias, p.delta_bias + d0, kDecTile * 4, &full[s]);
       }
       // Wait (bounded) for the copies still in flight before leaving.
       const int issued = i;
@@ -117,7 +122,9 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     const DecStage& sg = stg[s];
     const int64_t c0 = tile * kDecTile, bd = c0 + j, d = (c0 - (c0 / D) * D) + j;
     const float x = __bfloat162float(sg.x[j]);
-    const float dt = __bfloat162float(sg.dl[j]);
+    float dt = __bfloat162float(sg.dl[j]);
+    if (kMap && p.delta_bias) dt += sg.bias[j];
+    if (kMap && p.delta_softplus) dt = softplus_precise(dt);
     const float zz = p.z ? __bfloat162float(sg.z[j]) : 0.f;
     const float dx = dt * x;
     const float4* sp = reinterpret_cast<const float4*>(sg.state + j * N + g * 8);
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     float acc = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float a = decay<false>(dt, av[k], av[k] * kLog2e);
+      const float a = decay<false>(dt, av[k], av[k] * kLog2e);  // as state_update_kernel (bf16)
       sv[k] = fmaf(a, sv[k], dx * Bv[k]);
       acc = fmaf(Cv[k], sv[k], acc);
     }

@@ -137,9 +137,10 @@ def test_prefix_state_then_decode():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("step_map", [False, True], ids=["dt", "softplus-bias"])
 @pytest.mark.parametrize("gate", [True, False], ids=["z-D", "bare"])
 @pytest.mark.parametrize("y_dtype", [torch.bfloat16, torch.float32], ids=["y-bf16", "y-f32"])
-def test_decode_streamed_kernel(gate, y_dtype, monkeypatch):
+def test_decode_streamed_kernel(gate, y_dtype, step_map, monkeypatch):
     """The streamed decode kernel (bf16, N = 16, D a multiple of its 128-channel tile)
     against the oracle over several steps, and bit for bit against the one-thread-per-8-
     states kernel (SSM_B300_DECODE=plain) on the same inputs."""
@@ -148,7 +149,9 @@ def test_decode_streamed_kernel(gate, y_dtype, monkeypatch):
     d = inputs.decode_inputs(w, DEV)
     g = torch.Generator(device="cpu").manual_seed(42)
     s0 = torch.randn(b, Dm, N, generator=g).to(DEV)
-    kw = lambda t: dict(D=d["D"] if gate else None, z=d["z"][t] if gate else None, y_dtype=y_dtype)
+    bias = (torch.rand(Dm, generator=g) * 2 - 3).to(DEV) if step_map else None  # softplus(delta + bias)
+    mp = dict(delta_bias=bias, delta_softplus=True) if step_map else {}
+    kw = lambda t: dict(D=d["D"] if gate else None, z=d["z"][t] if gate else None, y_dtype=y_dtype, **mp)
     runs = {}
     for mode in ("stream", "plain"):
         if mode == "plain":
@@ -165,6 +168,7 @@ def test_decode_streamed_kernel(gate, y_dtype, monkeypatch):
     st_ref = to64(s0)
     for t in range(w.steps):
         args = (d["x"][t], d["delta"][t], d["A"], d["B"][t], d["C"][t])
-        yr, st_ref = oracle.state_update(st_ref, *args, D=d["D"] if gate else None, z=d["z"][t] if gate else None)
+        yr, st_ref = oracle.state_update(st_ref, *args, D=d["D"] if gate else None, z=d["z"][t] if gate else None,
+                                         **mp)
         check(runs["stream"][0][t], yr, TOL_BF16, y_dtype == torch.bfloat16, f"y step {t}")
     check(runs["stream"][1], st_ref, TOL_BF16, False, "state")
