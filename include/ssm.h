@@ -247,8 +247,8 @@ SSM_API ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_tensor_t* u, const
  *   stream                cudaStream_t
  * batch == 0 is a valid no-op. Only state may alias itself; y must not overlap any input.
  * With bf16 inputs, N = 16, D a multiple of 128 and 16-byte aligned state, x, delta, z,
- * A, B and C (and delta_bias, with ssm_state_update_ex; not ZOH, not the conv prologue)
- * the step runs as a persistent kernel that streams tiles of 128 channels through shared
+ * A, B and C (and delta_bias with ssm_state_update_ex, the conv operands with
+ * ssm_conv_state_update; not ZOH) the step runs as a persistent kernel that streams tiles of 128 channels through shared
  * memory; otherwise one thread updates 8 states (4 for N = 4). The two give identical
  * results (SSM_B300_DECODE=plain selects the second always).
  */

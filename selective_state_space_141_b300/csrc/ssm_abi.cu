@@ -430,27 +430,32 @@ cudaError_t launch_fwd_n(int64_t N, const FwdParams& p, cudaStream_t st) {
 template <typename TY>
 cudaError_t launch_dec_stream(const DecodeParams& p, cudaStream_t st, bool* launched) {
   *launched = false;
-  if (p.zoh || p.conv_w || p.D % ssm::kDecTile != 0) return cudaSuccess;
+  if (p.zoh || p.D % ssm::kDecTile != 0) return cudaSuccess;
   for (const void* q : {static_cast<const void*>(p.state), p.x, p.delta, static_cast<const void*>(p.A), p.B, p.C, p.z,
-                        static_cast<const void*>(p.delta_bias)})
+                        static_cast<const void*>(p.delta_bias), static_cast<const void*>(p.conv_w),
+                        static_cast<const void*>(p.conv_b), static_cast<const void*>(p.conv_state)})
     if (!aligned16(q)) return cudaSuccess;
-  const bool map = p.delta_bias || p.delta_softplus;
-  auto kern = map ? &ssm::state_update_stream<TY, true> : &ssm::state_update_stream<TY, false>;
+  const bool map = p.delta_bias || p.delta_softplus, conv = p.conv_w != nullptr;
+  auto kern = conv ? (map ? &ssm::state_update_stream<TY, true, true> : &ssm::state_update_stream<TY, false, true>)
+                   : (map ? &ssm::state_update_stream<TY, true, false> : &ssm::state_update_stream<TY, false, false>);
   constexpr int smem = ssm::dec_stream_smem_bytes();
-  static const cudaError_t attr0 = cudaFuncSetAttribute(
-      reinterpret_cast<const void*>(&ssm::state_update_stream<TY, false>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  static const cudaError_t attr1 = cudaFuncSetAttribute(
-      reinterpret_cast<const void*>(&ssm::state_update_stream<TY, true>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (attr0 != cudaSuccess) return attr0;
-  if (attr1 != cudaSuccess) return attr1;
   constexpr int threads = ssm::kDecConsumers + 32;
-  static int per_sm = -1;  // the same for both instantiations (same smem, threads, near registers)
-  if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, &ssm::state_update_stream<TY, true>, threads,
-                                                                   smem) != cudaSuccess ||
-                     per_sm < 1))
-    per_sm = 1;
+  static const auto set_up = [](const void* k, int* per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k, threads, smem);
+    if (*per_sm < 1) *per_sm = 1;
+    return e;
+  };
+  static int per_sm[4] = {0, 0, 0, 0};
+  static const cudaError_t attr[4] = {
+      set_up(reinterpret_cast<const void*>(&ssm::state_update_stream<TY, false, false>), &per_sm[0]),
+      set_up(reinterpret_cast<const void*>(&ssm::state_update_stream<TY, true, false>), &per_sm[1]),
+      set_up(reinterpret_cast<const void*>(&ssm::state_update_stream<TY, false, true>), &per_sm[2]),
+      set_up(reinterpret_cast<const void*>(&ssm::state_update_stream<TY, true, true>), &per_sm[3])};
+  const int vi = (map ? 1 : 0) + (conv ? 2 : 0);
+  if (attr[vi] != cudaSuccess) return attr[vi];
   int64_t ntiles = p.batch * p.D / ssm::kDecTile;
-  int64_t grid = (int64_t)(num_sms() > 0 ? num_sms() : 1) * per_sm;
+  int64_t grid = (int64_t)(num_sms() > 0 ? num_sms() : 1) * per_sm[vi];
   if (grid > ntiles) grid = ntiles;
   *launched = true;
   long long wc = wait_limit_cycles();

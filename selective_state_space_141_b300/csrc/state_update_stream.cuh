@@ -5,7 +5,9 @@
 // State Space Models (Mamba)", section 5: O(1) work per generated token on a fixed d*n
 // state; "Mamba and State Space Models", "Selective scan pseudo-code", one iteration of
 // the loop body): for each channel (b, d), with dt = delta (kMap: softplus(delta + bias[d])
-// or delta + bias[d] as the forward pass maps it)
+// or delta + bias[d] as the forward pass maps it) and x the token input (kConv: the
+// block's causal conv + SiLU of it, silu(conv_b + w0 cs0 + w1 cs1 + w2 cs2 + w3 x) over the
+// carried conv state, which is then shifted to (cs1, cs2, x))
 //   state[n] = exp(dt A[d,n]) state[n] + dt B[b,n] x,   y = (C[b] . state + D x) silu(z)
 //
 // The step reads and writes the whole fp32 state once, so its time is the time to move
@@ -40,6 +42,9 @@ struct alignas(16) DecStage {
   __nv_bfloat16 B[16];
   __nv_bfloat16 C[16];
   float bias[kDecTile];  // kMap with delta_bias only
+  float cw[kDecTile * 4];                // kConv: conv weights, 4 per channel
+  float cb[kDecTile];                    // kConv with conv_b
+  __nv_bfloat16 cs[kDecTile * 3 + 8];    // kConv: conv state, 3 per channel (+ pad to 16 B)
 };
 static_assert(sizeof(DecStage) % 16 == 0, "stage members start 16-byte aligned");
 
@@ -59,8 +64,9 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 // kDecConsumers consumer threads + one producer warp.
 // wait_cycles: the limit of every wait (0: the default); skip_loads (failure-detection
 // tests only): the producer issues no copies, so every consumer wait runs out.
-// kMap: the step-size map (delta_bias, delta_softplus) is compiled in.
-template <typename TY, bool kMap>
+// kMap: the step-size map (delta_bias, delta_softplus) is compiled in; kConv: the conv
+// prologue (conv_w, conv_b, conv_state).
+template <typename TY, bool kMap, bool kConv>
 __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const DecodeParams p, int64_t ntiles,
                                                                           long long wait_cycles, int skip_loads) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -87,8 +93,9 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
       const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(p.z);
       const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
       const __nv_bfloat16* C = static_cast<const __nv_bfloat16*>(p.C);
-      const bool bias = kMap && p.delta_bias;
-      const uint32_t tx = 2 * kDecTile * N * 4 + (z ? 3 : 2) * kDecTile * 2 + 2 * N * 2 + (bias ? kDecTile * 4 : 0);
+      const bool bias = kMap && p.delta_bias, cbias = kConv && p.conv_b;
+      const uint32_t tx = 2 * kDecTile * N * 4 + (z ? 3 : 2) * kDecTile * 2 + 2 * N * 2 + (bias ? kDecTile * 4 : 0) +
+                          (kConv ? kDecTile * 4 * 4 + kDecTile * 3 * 2 : 0) + (cbias ? kDecTile * 4 : 0);
       int i = 0;
       for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
         const int s = i % kDecStages;
@@ -104,6 +111,11 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
         bulk_load(sg.B, B + b * N, N * 2, &full[s]);
         bulk_load(sg.C, C + b * N, N * 2, &full[s]);
         if (bias) bulk_load(sg.bias, p.delta_bias + d0, kDecTile * 4, &full[s]);
+        if (kConv) {
+          bulk_load(sg.cw, p.conv_w + d0 * 4, kDecTile * 4 * 4, &full[s]);
+          bulk_load(sg.cs, static_cast<const __nv_bfloat16*>(p.conv_state) + c0 * 3, kDecTile * 3 * 2, &full[s]);
+          if (cbias) bulk_load(sg.cb, p.conv_b + d0, kDecTile * 4, &full[s]);
+        }
       }
       // Wait (bounded) for the copies still in flight before leaving.
       const int issued = i;
@@ -121,7 +133,21 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     if (!mbar_wait(&full[s], (i / kDecStages) & 1, kErrWaitFull, lim)) break;
     const DecStage& sg = stg[s];
     const int64_t c0 = tile * kDecTile, bd = c0 + j, d = (c0 - (c0 / D) * D) + j;
-    const float x = __bfloat162float(sg.x[j]);
+    const __nv_bfloat16 xraw = sg.x[j];
+    float x = __bfloat162float(xraw);
+    __nv_bfloat16 cs1, cs2;
+    if (kConv) {  // the block's causal conv + SiLU over (cs0, cs1, cs2, x), as state_update_kernel
+      const float* w = sg.cw + j * 4;
+      const __nv_bfloat16 cs0 = sg.cs[j * 3];
+      cs1 = sg.cs[j * 3 + 1];
+      cs2 = sg.cs[j * 3 + 2];
+      float c = p.conv_b ? sg.cb[j] : 0.f;
+      c = fmaf(w[0], __bfloat162float(cs0), c);
+      c = fmaf(w[1], __bfloat162float(cs1), c);
+      c = fmaf(w[2], __bfloat162float(cs2), c);
+      c = fmaf(w[3], x, c);
+      x = silu_precise(c);
+    }
     float dt = __bfloat162float(sg.dl[j]);
     if (kMap && p.delta_bias) dt += sg.bias[j];
     if (kMap && p.delta_softplus) dt = softplus_precise(dt);
@@ -151,6 +177,12 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     out[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
     out[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (kConv && g == 0) {  // shift the conv state: (cs1, cs2, the raw input)
+      __nv_bfloat16* cso = static_cast<__nv_bfloat16*>(p.conv_state) + bd * 3;
+      cso[0] = cs1;
+      cso[1] = cs2;
+      cso[2] = xraw;
+    }
     if (g == 0) {
       float o = acc;
       if (p.Dskip) o = fmaf(p.Dskip[d], x, o);

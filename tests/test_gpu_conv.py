@@ -152,3 +152,47 @@ def test_conv_decode_continues_forward():
         check(y, y_all[:, t], TOL_BF16, False, f"y t={t}")
     torch.cuda.synchronize()
     check(st, last_all, TOL_BF16, False, "state")
+
+
+@pytest.mark.parametrize("with_conv_bias", [True, False], ids=["conv-bias", "no-conv-bias"])
+def test_conv_decode_streamed_kernel(with_conv_bias, monkeypatch):
+    """bf16, N = 16, D a multiple of 128: the conv decode step runs on the streamed kernel
+    (conv state, weights and bias streamed with each tile, conv state shifted in place);
+    three steps against the oracle, and bit for bit against the per-thread kernel
+    (SSM_B300_DECODE=plain) on the same inputs."""
+    b, D, N, T = 3, 384, 16, 3
+    g = torch.Generator(device="cpu").manual_seed(77)
+    cs0 = torch.randn(b, D, 3, generator=g).to(torch.bfloat16).to(DEV)
+    s0 = torch.randn(b, D, N, generator=g).to(DEV)
+    xs = torch.randn(T, b, D, generator=g).to(torch.bfloat16).to(DEV)
+    w = (torch.randn(D, 4, generator=g) * 0.5).to(DEV)
+    cb = (torch.randn(D, generator=g) * 0.1).to(DEV) if with_conv_bias else None
+    raws = (torch.randn(T, b, D, generator=g) * 0.5 - 2.0).to(torch.bfloat16).to(DEV)
+    bias = (torch.rand(D, generator=g) * 0.05).to(DEV)
+    A = -(torch.rand(D, N, generator=g) * 4 + 0.1).to(DEV)
+    Bs = torch.randn(T, b, N, generator=g).to(torch.bfloat16).to(DEV)
+    Cs = torch.randn(T, b, N, generator=g).to(torch.bfloat16).to(DEV)
+    Dk = torch.randn(D, generator=g).to(DEV)
+    zs = torch.randn(T, b, D, generator=g).to(torch.bfloat16).to(DEV)
+    runs = {}
+    for mode in ("stream", "plain"):
+        if mode == "plain":
+            monkeypatch.setenv("SSM_B300_DECODE", "plain")
+        st, c = s0.clone(), cs0.clone()
+        ys = [ssm.conv_state_update(c, st, xs[t], w, raws[t], A, Bs[t], Cs[t], conv_bias=cb, D=Dk, z=zs[t],
+                                    delta_bias=bias, delta_softplus=True, y_dtype=torch.float32) for t in range(T)]
+        torch.cuda.synchronize()
+        runs[mode] = (ys, st, c)
+    monkeypatch.delenv("SSM_B300_DECODE")
+    for t in range(T):
+        assert torch.equal(runs["stream"][0][t], runs["plain"][0][t]), t
+    assert torch.equal(runs["stream"][1], runs["plain"][1]) and torch.equal(runs["stream"][2], runs["plain"][2])
+    st_ref, cs_ref = to64(s0), to64(cs0)
+    for t in range(T):
+        u = oracle.conv1d_silu(to64(xs[t])[:, None, :], w, cb, cs_ref)[:, 0, :]
+        yr, st_ref = oracle.state_update(st_ref, u, raws[t], A, Bs[t], Cs[t], D=Dk, z=zs[t], delta_bias=bias,
+                                         delta_softplus=True)
+        cs_ref = oracle.next_conv_state(to64(xs[t])[:, None, :], cs_ref)
+        check(runs["stream"][0][t], yr, TOL_BF16, False, f"y step {t}")
+    check(runs["stream"][1], st_ref, TOL_BF16, False, "state")
+    assert np.array_equal(to64(runs["stream"][2]), cs_ref), "conv state"
