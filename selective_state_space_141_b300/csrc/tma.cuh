@@ -56,12 +56,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread is suspended (it takes no issue slots)
+// until the phase completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the barrier's phase with the given parity has completed. Bounded: after
-// `limit` cycles of polling the error code goes to g_ssm_error and the wait returns false.
+// `limit` cycles the error code goes to g_ssm_error and the wait returns false. Between
+// checks of the clock the thread waits suspended (up to 20 us a try), not polling: a
+// staging warp that polls competes for issue slots and register-file writes with the
+// compute warp on its SM sub-partition.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int err, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_suspend(bar, parity, 20000u)) {
     if (clock64() - start > limit) {
       atomicCAS(&g_ssm_error, 0, err);
       return false;
