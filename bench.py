@@ -50,20 +50,32 @@ def load_peaks():
 
 def profiled_traffic():
     """DRAM bytes per forward launch from the committed Nsight Compute summary, or None
-    when the kernel source has changed since those counters were taken."""
-    import hashlib
+    when the kernel's sources have changed since those counters were taken."""
     import re
     prof = os.path.join(ROOT, "profiles", "scan_fwd_chan_m1p4b.md")
-    src = os.path.join(ROOT, "selective_state_space_141_b300", "csrc", "scan_fwd_chan.cuh")
-    if not (os.path.exists(prof) and os.path.exists(src)):
+    csrc = os.path.join(ROOT, "selective_state_space_141_b300", "csrc")
+    srcs = [os.path.join(csrc, f) for f in KERNEL_SOURCES]
+    if not (os.path.exists(prof) and all(os.path.exists(f) for f in srcs)):
         return None
     text = open(prof).read()
     t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     if not (t and h):
         return None
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return int(t.group(1)) if cur == h.group(1) else None
+    return int(t.group(1)) if kernel_source_hash(srcs) == h.group(1) else None
+
+
+# The sources the forward kernel is compiled from (its own file and the headers it uses).
+KERNEL_SOURCES = ("scan_fwd_chan.cuh", "scan_fwd.cuh", "tma.cuh", "common.cuh")
+
+
+def kernel_source_hash(paths):
+    """First 16 hex digits of the sha256 of the files' bytes, concatenated in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in paths:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def alu_peak_elem_steps(sm_mhz, sms=SM_COUNT):

@@ -665,10 +665,12 @@ struct SsdTcWalk {
 };
 
 // Bounded wait on a barrier phase that also gives up once another role has aborted.
+// Suspended between checks (up to 2 us a try), so that waiting warps leave the issue
+// slots to the warps with work.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_suspend(bar, parity, 2000u)) {
     if (*abort) return false;
     if (clock64() - start > kWaitCycles) {
       atomicCAS(&g_ssm_error, 0, (int)kErrWaitMma);
