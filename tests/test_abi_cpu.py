@@ -338,3 +338,47 @@ def test_ssd_validation(lib):
     assert n.value == r256(items * 64 * 64 * 2) + 2 * r256(items * 64 * 4) + r256(cbs * 64 * 72 * 4)
     assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 0, 64, 64, ctypes.byref(n)) == 2
     assert lib.ssm_ssd_fwd_workspace_size(2, 100, 4, 2, 64, 64, None) == 1
+
+
+def call_fwd_train(lib, a, ws_addr, ws_bytes, with_flag=True):
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    written = ctypes.c_int32(7)
+    st = lib.ssm_selective_scan_fwd_train(r("u"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("bias"), 1,
+                                          None, r("y"), r("last"), ctypes.c_void_p(ws_addr), ctypes.c_size_t(ws_bytes),
+                                          ctypes.byref(written) if with_flag else None, None)
+    return st, written.value
+
+
+def test_fwd_train_validation(lib):
+    """ssm_selective_scan_fwd_train: the checkpoints_written out-pointer and the backward
+    workspace are checked before anything runs; the flag reads 0 on every error."""
+    a = fwd_args()
+    ws = T((1 << 16,), ssm.SSM_F32)
+    n = ctypes.c_size_t(0)
+    assert lib.ssm_selective_scan_bwd_workspace_size(2, 5, 8, 16, ctypes.byref(n)) == 0
+    wa = (ws.data + 255) // 256 * 256
+    assert call_fwd_train(lib, a, wa, n.value, with_flag=False)[0] == 1   # no out-pointer
+    assert call_fwd_train(lib, a, 0, n.value) == (1, 0)                    # no workspace
+    assert call_fwd_train(lib, a, wa + 16, n.value) == (4, 0)              # not 256-byte aligned
+    assert call_fwd_train(lib, a, wa, 16) == (2, 0)                        # too small
+    assert call_fwd_train(lib, a, a["u"].data, n.value) == (4, 0)          # over an input
+    b = fwd_args()
+    b["y"].dtype = 99                                                      # the forward pass's own checks follow
+    assert call_fwd_train(lib, b, wa, n.value) == (3, 0)
+
+
+def test_bwd_ex_flags(lib):
+    """ssm_selective_scan_bwd_ex: only SSM_BWD_CHECKPOINTS is a known flag."""
+    a = bwd_args()
+    r = lambda k: None if a[k] is None else ctypes.byref(a[k])
+    n = ctypes.c_size_t(0)
+    assert lib.ssm_selective_scan_bwd_workspace_size(2, 5, 8, 16, ctypes.byref(n)) == 0
+    wa = (a["ws"].data + 255) // 256 * 256
+    call = lambda flags: lib.ssm_selective_scan_bwd_ex(
+        r("u"), r("delta"), r("A"), r("B"), r("C"), r("D"), r("z"), r("bias"), 1, None, r("dy"), None, r("du"),
+        r("ddelta"), r("dA"), r("dB"), r("dC"), r("dD"), r("dz"), r("dbias"), None, ctypes.c_uint32(flags),
+        ctypes.c_void_p(wa), ctypes.c_size_t(n.value), None)
+    assert call(2) == 5
+    assert call(ssm.SSM_BWD_CHECKPOINTS | 4) == 5
+    a["dD"] = None                                                         # the usual checks with the flag set
+    assert call(ssm.SSM_BWD_CHECKPOINTS) == 1
