@@ -487,10 +487,15 @@ SSM_API const char* ssm_status_string(ssm_status_t status);
  * context usable. Codes: 0 no error; 1 a TMA load never completed; 2 the consumers never
  * released a staging buffer; 3 a converted B/C tile was never published; 4 a tensor-core
  * MMA never signalled completion.
- * The forward pass's bounded waits last about one second by default; the environment
- * variable SSM_B300_WAIT_LIMIT_CYCLES sets another limit (in SM clock cycles), and
- * SSM_B300_FAULT_INJECT=skip_loads makes the staging warp issue no copies, so that every
- * wait for data runs out (used by the failure-detection tests only).
+ * The bounded waits of the forward pass's channel kernel and of the streamed decode kernel
+ * last about one second by default; the environment variable SSM_B300_WAIT_LIMIT_CYCLES
+ * sets another limit (in SM clock cycles), and SSM_B300_FAULT_INJECT=skip_loads makes their
+ * staging thread issue no copies, so that every wait for data runs out (used by the
+ * failure-detection tests only).
+ *
+ * Kernel selection switches (each path computes the same results; tests compare them):
+ * SSM_B300_FORWARD_KERNEL=generic|chan|auto (the forward pass's kernel), SSM_B300_SEGMENTS=0
+ * (no segmented schedule), SSM_B300_DECODE=plain (the per-thread decode kernel).
  */
 SSM_API ssm_status_t ssm_device_error(void* stream, int32_t* code);
 
