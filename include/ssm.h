@@ -407,8 +407,11 @@ SSM_API ssm_status_t ssm_selective_scan_fwd_train(const ssm_tensor_t* u, const s
  * the workspace's checkpoint region already holds the checkpoints of this step's forward
  * pass (ssm_selective_scan_fwd_train reported checkpoints_written = 1 for the same inputs,
  * h0 and workspace, and nothing wrote the workspace since), so the checkpoint pass is
- * skipped. Results are identical to ssm_selective_scan_bwd. Other flag bits:
+ * skipped. Other flag bits:
  * SSM_ERR_UNSUPPORTED. ssm_selective_scan_bwd(...) is ssm_selective_scan_bwd_ex(..., 0, ...).
+ * The gradients equal those of ssm_selective_scan_bwd bit for bit when the forward pass ran
+ * as one segment, and to rounding when it ran the segmented schedule (long sequences over
+ * few channels), whose carried states reassociate the recurrence.
  */
 SSM_API ssm_status_t ssm_selective_scan_bwd_ex(const ssm_tensor_t* u, const ssm_tensor_t* delta,
                                                const ssm_tensor_t* A, const ssm_tensor_t* B,
