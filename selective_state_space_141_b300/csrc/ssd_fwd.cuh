@@ -893,15 +893,48 @@ __global__ void __launch_bounds__(kTcThreads)
 struct SsdItem {
   int64_t b, c, h, g, t0;
 };
-__device__ __forceinline__ SsdItem ssd_item(const SsdParams& p, int64_t it) {
-  SsdItem r;
-  r.h = it % p.H;
-  r.c = (it / p.H) % p.nc;
-  r.b = it / (p.H * p.nc);
-  r.g = r.h / (p.H / p.G);
-  r.t0 = r.c * kSsdQ;
-  return r;
-}
+
+// The items first, first + step, first + 2 step, ... of a persistent CTA, decoded as
+// (b, c, h) counters that advance with carries: a few integer operations per item where
+// dividing each item index costs several 64-bit divisions per thread (items < 2^31, checked
+// on the host).
+struct SsdItemWalk {
+  uint32_t H, nc, hpg, h, c, b, sh, sq;
+  __device__ __forceinline__ void init(const SsdParams& p, uint32_t first, uint32_t step) {
+    H = (uint32_t)p.H;
+    nc = (uint32_t)p.nc;
+    hpg = (uint32_t)(p.H / p.G);
+    const uint32_t q = first / H;
+    h = first - q * H;
+    c = q % nc;
+    b = q / nc;
+    sq = step / H;
+    sh = step - sq * H;
+  }
+  __device__ __forceinline__ void advance() {
+    h += sh;
+    uint32_t cq = sq;
+    if (h >= H) {
+      h -= H;
+      ++cq;
+    }
+    c += cq;
+    if (c >= nc) {
+      const uint32_t w = c / nc;
+      b += w;
+      c -= w * nc;
+    }
+  }
+  __device__ __forceinline__ SsdItem item() const {
+    SsdItem r;
+    r.h = h;
+    r.c = c;
+    r.b = b;
+    r.g = hpg == H ? 0 : h / hpg;
+    r.t0 = (int64_t)c * kSsdQ;
+    return r;
+  }
+};
 
 // Pass 2. Per item the inputs arrive by TMA and bulk copies on one mbarrier (one thread
 // issues them): X and C as 64 x 64 boxes with the 128-byte swizzle (rows of 128 bytes; the
@@ -963,10 +996,12 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
   const int mp = warp & 1, pc0 = (warp >> 1) * (P / 4);
   const int mrow[2] = {mp, 3 - mp};
   bool ok = true;
-  for (int k = 0;; ++k) {
+  SsdItemWalk wk;
+  wk.init(p, blockIdx.x, gridDim.x);
+  for (int k = 0;; ++k, wk.advance()) {
     const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
     if (it >= items) break;
-    const SsdItem m = ssd_item(p, it);
+    const SsdItem m = wk.item();
     if (tid == 0) {
       const int32_t row = (int32_t)(m.b * p.L + m.t0);
       mbar_arrive_expect_tx(bar, Sm::kTx);
@@ -1171,14 +1206,16 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
 
   if (warp == 17) {  // ---------------- copier ----------------
     if (lane == 0) {
-      for (int k = 0;; ++k) {
+      SsdItemWalk wk;
+      wk.init(p, blockIdx.x, gridDim.x);
+      for (int k = 0;; ++k, wk.advance()) {
         const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
         if (it >= items) break;
         const int s = k & 1;
         // stage s last held item k - 2: wait until its MMAs have read it
         if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort)) break;
         unsigned char* st = sm + s * L::kStage;
-        const SsdItem m = ssd_item(p, it);
+        const SsdItem m = wk.item();
         const int32_t row = (int32_t)(m.b * p.L + m.t0);
         mbar_arrive_expect_tx(&loaded[s], L::kTx);
         tma_load_3d_bar(st + L::kX, &tm_x, 0, (int32_t)m.h, row, &loaded[s]);
@@ -1224,9 +1261,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     const int q = warp & 3, th = warp >> 2;  // TMEM lane quarter, quarter of the steps
     const int prow = 32 * q + lane;          // head row of this thread in the epilogue (TMEM lane)
     // item k's outputs (y rows of its chunk; the MMA results in TMEM buffer k % 2)
-    auto epilogue = [&](int k) {
-      const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
-      const SsdItem m = ssd_item(p, it);
+    auto epilogue = [&](int k, const SsdItem& m) {
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
       const int bsel = k & 1;
       if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort)) return false;
@@ -1251,12 +1286,15 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     };
     bool ok = true;
     int k = 0;
-    for (;; ++k) {
+    SsdItemWalk wk;
+    wk.init(p, blockIdx.x, gridDim.x);
+    SsdItem mprev{};  // the previous item, whose outputs this iteration writes
+    for (;; ++k, wk.advance()) {
       const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
       if (it >= items) break;
       const int s = k & 1;
       unsigned char* st = sm + s * L::kStage;
-      const SsdItem m = ssd_item(p, it);
+      const SsdItem m = wk.item();
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
       if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort)) ok = false;
       if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
@@ -1312,9 +1350,10 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       }
       fence_smem_to_async();
       mbar_arrive(&full[s]);
-      if (k >= 1 && !epilogue(k - 1)) ok = false;
+      if (k >= 1 && !epilogue(k - 1, mprev)) ok = false;
+      mprev = m;
     }
-    if (ok && k >= 1) epilogue(k - 1);
+    if (ok && k >= 1) epilogue(k - 1, mprev);
   }
   tc_fence_before();
   __syncthreads();

@@ -1313,7 +1313,9 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
   }
   if (last_state && overlaps(last_state, y)) return SSM_ERR_LAYOUT;
   const SsdPlan plan = ssd_plan(batch, L, H, groups, P, N);
-  const bool chunked = workspace && workspace_bytes >= plan.bytes && plan.bytes > 0 && H <= 65535;
+  // (the chunk-parallel read-out walks its items with 32-bit counters: fewer than 2^31 items)
+  const bool chunked = workspace && workspace_bytes >= plan.bytes && plan.bytes > 0 && H <= 65535 &&
+                       batch * ((L + ssm::kSsdQ - 1) / ssm::kSsdQ) * H < ((int64_t)1 << 31);
   if (chunked) {
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SSM_ERR_LAYOUT;
     ssm_tensor_t w{};
