@@ -45,6 +45,8 @@ struct alignas(16) DecStage {
   float cw[kDecTile * 4];                // kConv: conv weights, 4 per channel
   float cb[kDecTile];                    // kConv with conv_b
   __nv_bfloat16 cs[kDecTile * 3 + 8];    // kConv: conv state, 3 per channel (+ pad to 16 B)
+  int64_t d0;                            // the tile's first channel index d (written by the producer)
+  int64_t pad;
 };
 static_assert(sizeof(DecStage) % 16 == 0, "stage members start 16-byte aligned");
 
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
         if (i >= kDecStages && !mbar_wait(&empty[s], ((i / kDecStages) - 1) & 1, kErrWaitEmpty, lim)) break;
         DecStage& sg = stg[s];
         const int64_t c0 = tile * kDecTile, b = c0 / D, d0 = c0 - b * D;
-        mbar_arrive_expect_tx(&full[s], tx);
+        mbar_expect_tx(&full[s], tx);  // the copies first; the arrive after the tile's d0 below
         bulk_load(sg.state, p.state + c0 * N, kDecTile * N * 4, &full[s]);
         bulk_load(sg.A, p.A + d0 * N, kDecTile * N * 4, &full[s]);
         bulk_load(sg.x, x + c0, kDecTile * 2, &full[s]);
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
           bulk_load(sg.cs, static_cast<const __nv_bfloat16*>(p.conv_state) + c0 * 3, kDecTile * 3 * 2, &full[s]);
           if (cbias) bulk_load(sg.cb, p.conv_b + d0, kDecTile * 4, &full[s]);
         }
+        sg.d0 = d0;             // the tile's first channel index, for the consumers
+        mbar_arrive(&full[s]);  // releases d0; the phase completes when the copies have landed
       }
       // Wait (bounded) for the copies still in flight before leaving.
       const int issued = i;
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     const int s = i % kDecStages;
     if (!mbar_wait(&full[s], (i / kDecStages) & 1, kErrWaitFull, lim)) break;
     const DecStage& sg = stg[s];
-    const int64_t c0 = tile * kDecTile, bd = c0 + j, d = (c0 - (c0 / D) * D) + j;
+    const int64_t bd = tile * kDecTile + j;
     const __nv_bfloat16 xraw = sg.x[j];
     float x = __bfloat162float(xraw);
     __nv_bfloat16 cs1, cs2;
@@ -152,6 +156,9 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     if (kMap && p.delta_bias) dt += sg.bias[j];
     if (kMap && p.delta_softplus) dt = softplus_precise(dt);
     const float zz = p.z ? __bfloat162float(sg.z[j]) : 0.f;
+    // d: from the producer's tile offset with the conv prologue (measured faster there), by
+    // division otherwise (it can be computed before the barrier wait: measured faster there)
+    const int64_t d = kConv ? sg.d0 + j : (tile * kDecTile) % D + j;
     const float dx = dt * x;
     const float4* sp = reinterpret_cast<const float4*>(sg.state + j * N + g * 8);
     const float4* ap = reinterpret_cast<const float4*>(sg.A + j * N + g * 8);
