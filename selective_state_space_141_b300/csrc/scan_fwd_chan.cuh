@@ -114,13 +114,27 @@ __device__ __forceinline__ float2 chan_u2(ConvLane& c, float xa, float xb) {
   return silu2_fast(acc);
 }
 
+// Zero-order hold: B-bar u = phi(z) (dt u) B with z = dt A and phi(z) = (e^z - 1) / z, from
+// x = z log2(e) and a = 2^x already computed for the decay: (a - 1) / z where |z| >= 1/64
+// (the cancellation in a - 1 then costs at most ~2e-5 of phi), the series 1 + z/2 + z^2/6
+// below (remainder under 2e-7; exact at z = 0). phi times the pair of dt u values.
+__device__ __forceinline__ float2 zoh_scale2(float2 x, float2 a, float2 dup) {
+  const float2 z = __fmul2_rn(x, make_float2(kLn2, kLn2));
+  const float2 ser = __ffma2_rn(z, __ffma2_rn(z, make_float2(1.f / 6.f, 1.f / 6.f), make_float2(0.5f, 0.5f)),
+                                make_float2(1.f, 1.f));
+  const float2 em1 = __fadd2_rn(a, make_float2(-1.f, -1.f));
+  const float phx = fabsf(z.x) < 0.015625f ? ser.x : __fdividef(em1.x, z.x);
+  const float phy = fabsf(z.y) < 0.015625f ? ser.y : __fdividef(em1.y, z.y);
+  return __fmul2_rn(dup, make_float2(phx, phy));
+}
+
 // kChanSub steps of one lane (one channel, all N states), in three phases so that one
 // warp per SM sub-partition finds independent work: (1) step sizes (independent
 // softplus chains, two steps per packed op), (2) the recurrence (only h carries from
 // step to step), (3) D skip, gate and y staging (two steps per packed op).
 // kTail: steps at or past tc get dt = 0 and no input, so exp(0) = 1 exactly leaves h
 // bit-for-bit unchanged (selects, not multiplies; those rows hold zero fill).
-template <typename TY, int N, bool kSoftplus, bool kGate, bool kTail, bool kConv>
+template <typename TY, int N, bool kSoftplus, bool kGate, bool kTail, bool kConv, bool kZoh = false>
 __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __nv_bfloat16* sd,
                                               const __nv_bfloat16* sz, const float* bc, TY* yt, int t0, int tc,
                                               float bias, float Dk, const float2 (&A2)[N / 2], float2 (&h)[N / 2],
@@ -154,8 +168,8 @@ __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __n
       const float2 x1 = __fmul2_rn(dtp, A2[2 * q + 1]);
       const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));           // A-bar = exp(dt A)
       const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
-      const float2 b0 = __fmul2_rn(dup, make_float2(bq.x, bq.y));     // (dt u) B
-      const float2 b1 = __fmul2_rn(dup, make_float2(bq.z, bq.w));
+      const float2 b0 = __fmul2_rn(kZoh ? zoh_scale2(x0, a0, dup) : dup, make_float2(bq.x, bq.y));  // (dt u) B
+      const float2 b1 = __fmul2_rn(kZoh ? zoh_scale2(x1, a1, dup) : dup, make_float2(bq.z, bq.w));
       h[2 * q] = __ffma2_rn(a0, h[2 * q], b0);                        // h = A-bar h + B-bar u
       h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], b1);
       acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q], acc0);    // C . h
@@ -179,7 +193,7 @@ __device__ __forceinline__ void chan_subchunk(const __nv_bfloat16* su, const __n
 // Aggregate pass over kChanSub steps: the recurrence from the given state without the
 // read-out (no C, no y), plus the running sum of dt, from which the decay product of a
 // whole segment is exp(A * sum dt). Same tail rule as chan_subchunk.
-template <int N, bool kSoftplus, bool kTail, bool kConv>
+template <int N, bool kSoftplus, bool kTail, bool kConv, bool kZoh = false>
 __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const __nv_bfloat16* sd, const float* bc,
                                                   int t0, int tc, float bias, const float2 (&A2)[N / 2],
                                                   float2 (&h)[N / 2], float& sdt, ConvLane& cv) {
@@ -210,8 +224,9 @@ __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const
       const float2 x1 = __fmul2_rn(dtp, A2[2 * q + 1]);
       const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));
       const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
-      h[2 * q] = __ffma2_rn(a0, h[2 * q], __fmul2_rn(dup, make_float2(bq.x, bq.y)));
-      h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], __fmul2_rn(dup, make_float2(bq.z, bq.w)));
+      h[2 * q] = __ffma2_rn(a0, h[2 * q], __fmul2_rn(kZoh ? zoh_scale2(x0, a0, dup) : dup, make_float2(bq.x, bq.y)));
+      h[2 * q + 1] =
+          __ffma2_rn(a1, h[2 * q + 1], __fmul2_rn(kZoh ? zoh_scale2(x1, a1, dup) : dup, make_float2(bq.z, bq.w)));
     }
   }
 }
@@ -222,7 +237,8 @@ __device__ __forceinline__ void chan_subchunk_agg(const __nv_bfloat16* su, const
 //               segment writing the checkpoints only.
 // blockIdx = (channel block of 128, batch row, sequence segment).
 // kConv: the u tensor holds the conv input x; u is its causal conv + SiLU (ConvLane).
-template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg, bool kConv, bool kCk = false>
+template <typename TY, int N, int TC, int S, bool kSoftplus, bool kGate, bool kAgg, bool kConv, bool kCk = false,
+          bool kZoh = false>
 __global__ void __launch_bounds__(kChanThreads, 1)
 scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -380,12 +396,12 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
       if (tc == TC) {
         for (int t0 = 0; t0 < TC; t0 += kChanSub) {
           checkpoint(t0);
-          chan_subchunk_agg<N, kSoftplus, false, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+          chan_subchunk_agg<N, kSoftplus, false, kConv, kZoh>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
         }
       } else {
         for (int t0 = 0; t0 < tc; t0 += kChanSub) {
           checkpoint(t0);
-          chan_subchunk_agg<N, kSoftplus, true, kConv>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
+          chan_subchunk_agg<N, kSoftplus, true, kConv, kZoh>(su, sd, bc, t0, tc, bias, A2, h, sdt, cv);
         }
       }
       __syncwarp();
@@ -402,12 +418,12 @@ scan_fwd_chan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ 
     if (tc == TC) {
       for (int t0 = 0; t0 < TC; t0 += kChanSub) {
         checkpoint(t0);
-        chan_subchunk<TY, N, kSoftplus, kGate, false, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
+        chan_subchunk<TY, N, kSoftplus, kGate, false, kConv, kZoh>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
       }
     } else {
       for (int t0 = 0; t0 < tc; t0 += kChanSub) {
         checkpoint(t0);
-        chan_subchunk<TY, N, kSoftplus, kGate, true, kConv>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
+        chan_subchunk<TY, N, kSoftplus, kGate, true, kConv, kZoh>(su, sd, sz, bc, yt, t0, tc, bias, Dk, A2, h, cv);
       }
     }
     // Release the input stage, then send this chunk's y tile (rows past L and columns

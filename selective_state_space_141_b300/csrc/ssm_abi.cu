@@ -138,15 +138,15 @@ constexpr int kChanTC = 32, kChanStages = 4;
 bool chan_eligible(const FwdParams& p, int64_t N) {
   // TMA needs 16-byte aligned bases and row pitches (D % 8 == 0 covers bf16 and fp32
   // y) and int32 coordinates; last_state is written with 16-byte vector stores.
-  // The zero-order-hold B-bar is a general-kernel option.
-  return !p.zoh && (N == 8 || N == 16) && p.D % 8 == 0 && p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
+  // The zero-order-hold B-bar runs here too, except with the conv prologue.
+  return !(p.zoh && p.conv_w) && (N == 8 || N == 16) && p.D % 8 == 0 && p.L < (int64_t)INT32_MAX && aligned16(p.u) &&
          aligned16(p.delta) && aligned16(p.z) && aligned16(p.B) && aligned16(p.C) && aligned16(p.y) &&
          aligned16(p.last_state) && encode_fn() != nullptr;
 }
 
-template <typename TY, int N, bool kSP, bool kZ, bool kAgg, bool kConv, bool kCk = false>
+template <typename TY, int N, bool kSP, bool kZ, bool kAgg, bool kConv, bool kCk = false, bool kZoh = false>
 cudaError_t launch_chan_k(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st) {
-  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg, kConv, kCk>;
+  auto kern = &ssm::scan_fwd_chan<TY, N, kChanTC, kChanStages, kSP, kZ, kAgg, kConv, kCk, kZoh>;
   constexpr int smem = ssm::chan_smem_bytes<TY, N, kChanTC, kChanStages>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -245,6 +245,14 @@ cudaError_t launch_carry(const ssm::SegY& sy, const float* E, const float* P, co
 template <typename TY, int N, bool kAgg, bool kConv>
 cudaError_t launch_chan_sz(const FwdParams& p, const CUtensorMap* maps, int nseg, cudaStream_t st, bool sp, bool z) {
   if (kAgg) z = false;
+  if constexpr (!kConv) {
+    if (p.zoh) {  // the zero-order-hold B-bar (not with checkpoints: the training pair is the Delta B form)
+      if (sp && z) return launch_chan_k<TY, N, true, !kAgg, kAgg, false, false, true>(p, maps, nseg, st);
+      if (sp) return launch_chan_k<TY, N, true, false, kAgg, false, false, true>(p, maps, nseg, st);
+      if (z) return launch_chan_k<TY, N, false, !kAgg, kAgg, false, false, true>(p, maps, nseg, st);
+      return launch_chan_k<TY, N, false, false, kAgg, false, false, true>(p, maps, nseg, st);
+    }
+  }
   if constexpr (!kAgg && !kConv) {
     if (p.ck) {  // the full pass of a training forward: y and the backward's checkpoints
       if (sp && z) return launch_chan_k<TY, N, true, true, false, false, true>(p, maps, nseg, st);

@@ -226,3 +226,35 @@ def test_decode_zoh_vs_oracle(dtype):
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
     check(y, yr, tol, dtype == torch.bfloat16, "y")
     check(st, sr, tol, False, "state")
+
+
+@pytest.mark.parametrize("case", ["long-segmented", "tiny-dt"])
+def test_fwd_zoh_channel_kernel(case, monkeypatch):
+    """The zero-order hold on the channel kernel (bf16, N = 16): phi(z) = (e^z - 1) / z from
+    the step's own 2^x where |z| >= 1/64, the series below. A long sequence over few channels
+    (the segmented schedule) and step sizes tiny enough that every z falls in the series
+    branch (some exactly 0), each against the oracle and against the generic kernel."""
+    if case == "long-segmented":
+        b, L, D, N = 1, 6001, 64, 16
+        d = inputs.random_fwd(b, L, D, N, torch.bfloat16, DEV, seed=63)
+    else:
+        b, L, D, N = 2, 333, 128, 16
+        d = inputs.random_fwd(b, L, D, N, torch.bfloat16, DEV, seed=64, delta_softplus=False)
+        g = torch.Generator(device="cpu").manual_seed(65)
+        dl = torch.rand(b, L, D, generator=g) * 2e-3                    # |dt A| <= 2e-3 * 16 < 1/64
+        dl[:, ::7] = 0.0                                                 # and z = 0 exactly
+        d["delta"] = dl.to(torch.bfloat16).to(DEV)
+        d["delta_bias"] = None
+    kw = dict(D=d["D"], z=d["z"], delta_bias=d["delta_bias"], delta_softplus=d["delta_softplus"], zoh=True)
+    yr, lr = oracle.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], **kw)
+    y, last = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], y_dtype=torch.float32,
+                                     use_workspace=False, **kw)
+    monkeypatch.setenv("SSM_B300_FORWARD_KERNEL", "generic")
+    yg, lg = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], y_dtype=torch.float32,
+                                    use_workspace=False, **kw)
+    monkeypatch.delenv("SSM_B300_FORWARD_KERNEL")
+    torch.cuda.synchronize()
+    assert ssm.device_error() == 0
+    check(y, yr, TOL_BF16, False, "y (channel kernel)")
+    check(last, lr, TOL_BF16, False, "last_state (channel kernel)")
+    check(yg, yr, TOL_BF16, False, "y (generic kernel)")
