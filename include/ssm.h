@@ -490,8 +490,8 @@ SSM_API const char* ssm_status_string(ssm_status_t status);
  * context usable. Codes: 0 no error; 1 a TMA load never completed; 2 the consumers never
  * released a staging buffer; 3 a converted B/C tile was never published; 4 a tensor-core
  * MMA never signalled completion.
- * The bounded waits of the forward pass's channel kernel and of the streamed decode kernel
- * last about one second by default; the environment variable SSM_B300_WAIT_LIMIT_CYCLES
+ * The bounded waits of the forward pass's channel kernel, the streamed decode kernel and the
+ * tensor-core SSD kernels last about one second by default; the environment variable SSM_B300_WAIT_LIMIT_CYCLES
  * sets another limit (in SM clock cycles), and SSM_B300_FAULT_INJECT=skip_loads makes their
  * staging thread issue no copies, so that every wait for data runs out (used by the
  * failure-detection tests only).

@@ -51,6 +51,11 @@ struct SsdParams {
   float* ws_cs;
   float* ws_CB;
   int nc;
+  // Failure detection (tcgen05 kernels): the limit of every bounded wait in cycles (0: the
+  // default of about one second), and a test-only switch that stops the copier issuing
+  // copies, so that every wait for data runs out.
+  long long wait_cycles;
+  int fault_skip_loads;
 };
 
 constexpr int kSsdQ = 64;
@@ -667,13 +672,14 @@ struct SsdTcWalk {
 // Bounded wait on a barrier phase that also gives up once another role has aborted.
 // Suspended between checks (up to 2 us a try), so that waiting warps leave the issue
 // slots to the warps with work.
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit,
+                                        int err = kErrWaitMma) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   while (!mbar_try_wait_suspend(bar, parity, 2000u)) {
     if (*abort) return false;
-    if (clock64() - start > kWaitCycles) {
-      atomicCAS(&g_ssm_error, 0, (int)kErrWaitMma);
+    if (clock64() - start > limit) {
+      atomicCAS(&g_ssm_error, 0, err);
       *abort = 1;
       return false;
     }
@@ -708,6 +714,7 @@ __global__ void __launch_bounds__(kTcThreads)
   uint64_t* loaded = full + 8;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem_raw + L::kSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem_raw + L::kAbort);
+  const long long lim = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb0 = blockIdx.x * NB;
   const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G);
@@ -747,10 +754,10 @@ __global__ void __launch_bounds__(kTcThreads)
   };
 
   if (warp == 5) {  // ---------------- copier ----------------
-    if (lane == 0) {
+    if (lane == 0 && !p.fault_skip_loads) {
       for (int c = 0; c < nc; ++c) {
         // stage c % 2 last held chunk c - 2: wait until its MMA has read it
-        if (c >= 2 && !tc_wait(&empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1), abort)) break;
+        if (c >= 2 && !tc_wait(&empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1), abort, lim)) break;
         load(c & 1, c);
       }
     }
@@ -758,8 +765,8 @@ __global__ void __launch_bounds__(kTcThreads)
     if (lane == 0) {
       for (int c = 0; c < nc; ++c) {
         const int s = c & 1;
-        if (!tc_wait(&full[s], (uint32_t)((c >> 1) & 1), abort)) break;
-        if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort)) break;
+        if (!tc_wait(&full[s], (uint32_t)((c >> 1) & 1), abort, lim)) break;
+        if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort, lim)) break;
         tc_fence_after();
         const unsigned char* st = smem_raw + s * L::kStage;
         const uint32_t xa = umma_saddr(st + L::kX), wa = umma_saddr(st + L::kW);
@@ -791,7 +798,7 @@ __global__ void __launch_bounds__(kTcThreads)
     // releases its TMEM buffer
     auto epilogue = [&](int c, float dec) {
       const int s = c & 1;
-      if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort)) return false;
+      if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort, lim)) return false;
       tc_fence_after();
       float Sc[NB];
       {  // the high part's 32 columns, then the low part's
@@ -827,7 +834,7 @@ __global__ void __launch_bounds__(kTcThreads)
     float dec_prev = 0.f;  // exp(cs_end) of chunk c - 1
     for (int c = 0; c < nc; ++c) {
       const int s = c & 1;
-      if (ok && !tc_wait(&loaded[s], (uint32_t)((c >> 1) & 1), abort)) ok = false;
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((c >> 1) & 1), abort, lim, kErrWaitFull)) ok = false;
       const int rv = (int)((p.L - (int64_t)c * Q) < Q ? (p.L - (int64_t)c * Q) : Q);
       if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
         unsigned char* st = smem_raw + s * L::kStage;
@@ -1181,6 +1188,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
   uint64_t* tempty = loaded + 8;                                  // [2]
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L::kSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const long long lim = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
   float* ecs = reinterpret_cast<float*>(sm + L::kEcs);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t items = p.batch * p.nc * p.H;
@@ -1205,7 +1213,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
   const uint32_t tmem = *slot;
 
   if (warp == 17) {  // ---------------- copier ----------------
-    if (lane == 0) {
+    if (lane == 0 && !p.fault_skip_loads) {
       SsdItemWalk wk;
       wk.init(p, blockIdx.x, gridDim.x);
       for (int k = 0;; ++k, wk.advance()) {
@@ -1213,7 +1221,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         if (it >= items) break;
         const int s = k & 1;
         // stage s last held item k - 2: wait until its MMAs have read it
-        if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort)) break;
+        if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, lim)) break;
         unsigned char* st = sm + s * L::kStage;
         const SsdItem m = wk.item();
         const int32_t row = (int32_t)(m.b * p.L + m.t0);
@@ -1236,8 +1244,8 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
         if (it >= items) break;
         const int s = k & 1;
-        if (!tc_wait(&full[s], (uint32_t)((k >> 1) & 1), abort)) break;
-        if (k >= 2 && !tc_wait(&tempty[s], (uint32_t)(((k - 2) >> 1) & 1), abort)) break;
+        if (!tc_wait(&full[s], (uint32_t)((k >> 1) & 1), abort, lim)) break;
+        if (k >= 2 && !tc_wait(&tempty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, lim)) break;
         tc_fence_after();
         const unsigned char* st = sm + s * L::kStage;
         const uint32_t xa = umma_saddr(st + L::kX), ca = umma_saddr(st + L::kC), ha = umma_saddr(st + L::kH);
@@ -1264,7 +1272,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     auto epilogue = [&](int k, const SsdItem& m) {
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
       const int bsel = k & 1;
-      if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort)) return false;
+      if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort, lim)) return false;
       tc_fence_after();
       uint32_t v1[16], v2[16];
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)bsel + 16u * (uint32_t)th;
@@ -1296,7 +1304,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       unsigned char* st = sm + s * L::kStage;
       const SsdItem m = wk.item();
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
-      if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort)) ok = false;
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort, lim, kErrWaitFull)) ok = false;
       if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
         for (int i = tid; i < (Q - rv) * (P / 8); i += kTcScanWorkers) {
           const int t = rv + i / (P / 8), c = i % (P / 8);

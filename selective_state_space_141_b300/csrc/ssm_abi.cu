@@ -1362,6 +1362,8 @@ ssm_status_t ssm_ssd_fwd(int64_t groups, const ssm_tensor_t* x, const ssm_tensor
   p.G = groups;
   const bool yf = y->dtype == SSM_F32;
   p.nc = (int)((L + ssm::kSsdQ - 1) / ssm::kSsdQ);
+  p.wait_cycles = wait_limit_cycles();
+  p.fault_skip_loads = fault_skip_loads();
   p.ws_H = nullptr;
   p.ws_dt = nullptr;
   p.ws_cs = nullptr;

@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-The channel kernel's and the streamed decode kernel's waits on their mbarriers are
-bounded; a wait that runs out records an error code in the library's device error word and
+The channel kernel's, the streamed decode kernel's and the tensor-core SSD kernels' waits
+on their mbarriers are bounded; a wait that runs out records an error code in the library's device error word and
 the kernel returns (no trap, no hang). Here the staging thread is told to issue no copies
 (SSM_B300_FAULT_INJECT=skip_loads) and the wait limit is cut to 2e5 cycles (about 0.1
 ms), so every wait for data runs out. The tests check that the call returns, that
@@ -76,3 +76,26 @@ def test_decode_wait_runs_out_and_context_recovers(monkeypatch):
     yr, sr = oracle.state_update(s0, *args, D=d["D"], z=d["z"][0])
     check(y, yr, TOL_BF16, True, "y after recovery")
     check(state, sr, TOL_BF16, False, "state after recovery")
+
+
+def test_ssd_waits_run_out_and_context_recovers(monkeypatch):
+    """The tensor-core SSD kernels' waits (state walk and read-out, P = 128): with no copies
+    issued, the workers' waits for data run out, every role leaves through the shared
+    abort flag (the TMEM it holds released), the call returns with an error code, and a
+    following normal call on the same context matches the oracle."""
+    d = inputs.ssd_inputs(inputs.SsdWorkload("t", 1, 200, 3, 128, 128, 1, 75), DEV)
+    kw = dict(D=d["D"], dt_bias=d["dt_bias"], dt_softplus=d["dt_softplus"], y_dtype=torch.float32)
+    assert ssm.device_error() == 0
+    monkeypatch.setenv("SSM_B300_FAULT_INJECT", "skip_loads")
+    monkeypatch.setenv("SSM_B300_WAIT_LIMIT_CYCLES", "200000")
+    ssm.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], **kw)
+    code = ssm.device_error()
+    assert code in (1, 4), f"expected a wait-ran-out code, got {code}"
+    monkeypatch.delenv("SSM_B300_FAULT_INJECT")
+    monkeypatch.delenv("SSM_B300_WAIT_LIMIT_CYCLES")
+    y, last = ssm.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], **kw)
+    assert ssm.device_error() == 0
+    yr, lr = oracle.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], dt_bias=d["dt_bias"],
+                            dt_softplus=d["dt_softplus"])
+    check(y, yr, TOL_BF16, False, "y after recovery")
+    check(last, lr, TOL_BF16, False, "last_state after recovery")
