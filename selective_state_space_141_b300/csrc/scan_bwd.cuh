@@ -23,8 +23,8 @@
 // with the previous chunk at once, the chunk's states are recomputed into shared memory
 // from its checkpoint, and the chunk is walked backwards; the read-out C.h + D u that the
 // gate's gradient needs is recomputed in that walk. dB and dC are sums over channels:
-// each warp reduces its 16 channels with one transpose-reduce (shuffles) per step and
-// writes one partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over
+// each warp sums its 16 channels once per step (column sums in shared memory for N = 16,
+// a shuffle transpose-reduce below) and writes one partial per (b, t, warp, n); scan_bwd_reduce then sums the partials over
 // warps, and dA, dD, dbias over batch rows, in a fixed order (deterministic, no atomics).
 #pragma once
 
@@ -207,7 +207,7 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
 
 // grid (W = ceil(D / 16), batch), block 32 (one warp: 16 channels x two halves of the
 // states); dynamic shared memory:
-//   hs  [kBwdK + 1][N/4][32] f32x2 each lane's state pairs h_{t0-1} .. h_{t0+K-1} of the chunk
+//   hs  [kBwdK][N/4][32]     f32x2 each lane's state pairs h_{t0-1} .. h_{t0+K-2} of the chunk
 //   bc  [kBwdK][2N]          f32  the chunk's B | C rows
 //   sc  [kBwdK][16]          f32x4 per (step, channel): dt, dt u, dv, u
 //   sx  [kBwdK][16]          f32x2 per (step, channel): d(dt)/d(delta), dy silu'(z)
@@ -215,7 +215,7 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
 //   stage                         raw inputs of one chunk (refilled as soon as they are read)
 template <typename T, typename TG, int N>
 constexpr int bwd_smem_bytes() {
-  return ((kBwdK + 1) * (N / 2) * 32 + kBwdK * 2 * N + kBwdK * kBwdCh * 6 + (N == 16 ? kBwdCh * 32 : 0)) * 4 +
+  return (kBwdK * (N / 2) * 32 + kBwdK * 2 * N + kBwdK * kBwdCh * 6 + (N == 16 ? kBwdCh * 32 : 0)) * 4 +
          (int)sizeof(BwdStage<T, TG, N>);
 }
 
@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   constexpr int P2 = NH / 2;  // packed pairs per lane
   constexpr int kItems = kBwdK * kBwdCh / 32;  // (step, channel) items per lane in a chunk
   extern __shared__ __align__(16) float sm[];
-  float2* hs2 = reinterpret_cast<float2*>(sm);  // [kBwdK + 1][P2][32]
-  float* bc = sm + (kBwdK + 1) * NH * 32;
+  float2* hs2 = reinterpret_cast<float2*>(sm);  // [kBwdK][P2][32]
+  float* bc = sm + kBwdK * NH * 32;
   float4* sc = reinterpret_cast<float4*>(bc + kBwdK * 2 * N);  // [kBwdK][16]
   float2* sx = reinterpret_cast<float2*>(sc + kBwdK * kBwdCh);  // [kBwdK][16]
   float* red = reinterpret_cast<float*>(sx + kBwdK * kBwdCh);  // [16][32] when N = 16
@@ -367,14 +367,13 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     {
       const float2* ckp = reinterpret_cast<const float2*>(p.ck + (((int64_t)b * p.nc + c) * D + d) * N + nb);
 #pragma unroll
-      for (int q = 0; q < P2; ++q) {
-        h[q] = vd ? ckp[q] : make_float2(0.f, 0.f);
-        hs2[q * 32 + lane] = h[q];
-      }
+      for (int q = 0; q < P2; ++q) h[q] = vd ? ckp[q] : make_float2(0.f, 0.f);
+      // (the state after the last step stays in h: the reverse walk starts from it)
+#pragma unroll 4
       for (int k = 0; k < kc; ++k) {
-        fwd_step(k);
 #pragma unroll
-        for (int q = 0; q < P2; ++q) hs2[((k + 1) * P2 + q) * 32 + lane] = h[q];
+        for (int q = 0; q < P2; ++q) hs2[(k * P2 + q) * 32 + lane] = h[q];  // the state before step k
+        fwd_step(k);
       }
     }
     // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
@@ -387,7 +386,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
     const float2* sxp = sx + (kc - 1) * kBwdCh + ch;
     const float* bcp = bc + (kc - 1) * 2 * N + nb;
     const float2* hsp = hs2 + (kc - 1) * P2 * 32 + lane;
-#pragma unroll 2
+#pragma unroll 4
     for (int k = kc - 1; k >= 0; --k) {
       const float4 s = *scp;  // dt, dt u, dv, u
       const float2 sxv = *sxp;
