@@ -196,6 +196,47 @@ __device__ __forceinline__ void load_pairs(const float* row, float2 (&v)[P2]) {
   }
 }
 
+// 16 bytes of T (8 bf16 or 4 fp32) from shared memory to fp32 in shared memory.
+template <typename T>
+__device__ __forceinline__ void vec_to_f32(float* dst, const T* src) {
+  const uint4 v = *reinterpret_cast<const uint4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  if constexpr (sizeof(T) == 4) {
+    d4[0] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+  } else {
+    // bf16 -> fp32 is the 16 bits moved to the top half
+    d4[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u), __uint_as_float(v.y << 16),
+                        __uint_as_float(v.y & 0xffff0000u));
+    d4[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u), __uint_as_float(v.w << 16),
+                        __uint_as_float(v.w & 0xffff0000u));
+  }
+}
+
+// Two adjacent elements of T (bf16 or fp32) from shared memory as floats.
+template <typename T>
+__device__ __forceinline__ float2 ld_pair(const T* src) {
+  if constexpr (sizeof(T) == 4) {
+    return *reinterpret_cast<const float2*>(src);
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  }
+}
+// Softplus and sigmoid of two values on the bf16 path (2^x, log2 and the reciprocal on the
+// SFU, the rest as packed f32x2 ops): max(r, 0) + ln2 log2(1 + 2^(-|r| log2 e)), and
+// 1 / (1 + 2^(-x log2 e)).
+__device__ __forceinline__ float2 softplus2_bwd(float2 r) {
+  const float2 a = __fmul2_rn(make_float2(fabsf(r.x), fabsf(r.y)), make_float2(-kLog2e, -kLog2e));
+  const float2 op = __fadd2_rn(make_float2(ex2(a.x), ex2(a.y)), make_float2(1.f, 1.f));
+  return __ffma2_rn(make_float2(lg2(op.x), lg2(op.y)), make_float2(kLn2, kLn2),
+                    make_float2(fmaxf(r.x, 0.f), fmaxf(r.y, 0.f)));
+}
+__device__ __forceinline__ float2 sigmoid2_bwd(float2 x) {
+  const float2 a = __fmul2_rn(x, make_float2(-kLog2e, -kLog2e));
+  const float2 den = __fadd2_rn(make_float2(ex2(a.x), ex2(a.y)), make_float2(1.f, 1.f));
+  return make_float2(__fdividef(1.f, den.x), __fdividef(1.f, den.y));
+}
+
 // Decay factors of two states: 2^(dt A log2 e) on the SFU, or exp in double on the
 // fp32 I/O path (as the forward kernels).
 template <bool kAccurate>
@@ -241,6 +282,10 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   // the prologue's items all belong to channel lane & 15
   const int pch = lane & 15;
   const float pbias = (d0 + pch < D && p.delta_bias) ? p.delta_bias[d0 + pch] : 0.f;
+  const int pc0 = 2 * (lane & 7);  // the bf16 prologue's channel pair
+  const float2 pbias2 = p.delta_bias ? make_float2(d0 + pc0 < D ? p.delta_bias[d0 + pc0] : 0.f,
+                                                   d0 + pc0 + 1 < D ? p.delta_bias[d0 + pc0 + 1] : 0.f)
+                                     : make_float2(0.f, 0.f);
 
   float2 Av[P2], A2[P2], h[P2];  // A, A log2(e) (Av: the fp32 path's exact decay and sums)
 #pragma unroll
@@ -259,10 +304,53 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   // (not once per lane of the channel and per sweep). full = false: the forward sweep's
   // dt and dt u only (dy and z are not staged there).
   auto prologue = [&](bool full) {
-    for (int i = lane; i < kBwdK * N; i += 32) {
-      const int k = i / N, n = i % N;
-      bc[k * 2 * N + n] = to_f32(sg.B[i]);
-      if (full) bc[k * 2 * N + N + n] = to_f32(sg.C[i]);
+    constexpr int kV = 16 / (int)sizeof(T);  // elements per 16-byte piece
+    if constexpr (N % kV == 0) {
+      for (int pc = lane; pc < kBwdK * N / kV; pc += 32) {
+        const int e0 = pc * kV, k = e0 / N, n0 = e0 % N;
+        vec_to_f32<T>(bc + k * 2 * N + n0, &sg.B[e0]);
+        if (full) vec_to_f32<T>(bc + k * 2 * N + N + n0, &sg.C[e0]);
+      }
+    } else {
+      for (int i = lane; i < kBwdK * N; i += 32) {
+        const int k = i / N, n = i % N;
+        bc[k * 2 * N + n] = to_f32(sg.B[i]);
+        if (full) bc[k * 2 * N + N + n] = to_f32(sg.C[i]);
+      }
+    }
+    if constexpr (!kAccurate) {
+      // bf16 path: two adjacent channels per lane (c0, c0 + 1; the same for every j),
+      // steps 4 j + lane / 8, with packed ops
+      const int c0 = 2 * (lane & 7);
+#pragma unroll
+      for (int j = 0; j < kItems / 2; ++j) {
+        const int k = 4 * j + (lane >> 3);
+        const float2 r = __fadd2_rn(ld_pair(&sg.dl[k][c0]), pbias2);
+        float2 dt = r, sr = make_float2(1.f, 1.f);
+        if (p.delta_softplus) {
+          dt = softplus2_bwd(r);
+          if (full) sr = sigmoid2_bwd(r);
+        }
+        const float2 x = ld_pair(&sg.u[k][c0]);
+        float2 dv = make_float2(0.f, 0.f), dyz = make_float2(0.f, 0.f);
+        if (full) {
+          const float2 dyv = ld_pair(&sg.dy[k][c0]);
+          dv = dyv;
+          if (p.z) {
+            const float2 zz = ld_pair(&sg.z[k][c0]);
+            const float2 sz = sigmoid2_bwd(zz);
+            dv = __fmul2_rn(__fmul2_rn(dyv, zz), sz);  // dy silu(z)
+            const float2 oms = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-sz.x, -sz.y));
+            dyz = __fmul2_rn(dyv, __fmul2_rn(sz, __ffma2_rn(zz, oms, make_float2(1.f, 1.f))));  // dy silu'(z)
+          }
+        }
+        const float2 dtx = __fmul2_rn(dt, x);
+        sc[k * kBwdCh + c0] = make_float4(dt.x, dtx.x, dv.x, x.x);
+        sc[k * kBwdCh + c0 + 1] = make_float4(dt.y, dtx.y, dv.y, x.y);
+        *reinterpret_cast<float4*>(&sx[k * kBwdCh + c0]) = make_float4(sr.x, dyz.x, sr.y, dyz.y);
+      }
+      __syncwarp();
+      return;
     }
 #pragma unroll
     for (int j = 0; j < kItems; ++j) {
