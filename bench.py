@@ -583,7 +583,8 @@ def backward_bench(args, ssm, torch, w, d, dev, fwd_launch_ms):
 
 
 def ssd_bench(args, ssm, torch, inputs, dev, peaks):
-    """The Mamba-2 SSD workload (chunked, tensor cores): CUDA events around back-to-back calls."""
+    """The Mamba-2 SSD workload (chunked, tensor cores): CUDA events around one replay of a
+    CUDA graph of back-to-back calls."""
     w = inputs.SSD_M2
     d = inputs.ssd_inputs(w, dev)
     y = torch.empty_like(d["x"])
@@ -595,17 +596,28 @@ def ssd_bench(args, ssm, torch, inputs, dev, peaks):
         ssm.ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], dt_bias=d["dt_bias"], dt_softplus=True,
                     y=y, last_state=ls, workspace=ws)
 
-    for _ in range(3):
-        call()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    # calls back to back between two events (the host enqueues faster than the GPU runs,
-    # so the binding's own host time stays off the device timeline)
+    # the calls captured in one CUDA graph, so that the binding's host work per call (about
+    # as long as the call's device time here) stays off the device timeline
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(args.ssd_steps):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.ssd_steps):
-        call()
+    g.replay()
     e1.record()
     torch.cuda.synchronize()
+    if ssm.device_error() != 0:
+        raise RuntimeError("device error word set during the SSD calls")
     m = e0.elapsed_time(e1) / args.ssd_steps
     tf = w.flops() / (m / 1e3) / 1e12
     tpk = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -618,7 +630,8 @@ def ssd_bench(args, ssm, torch, inputs, dev, peaks):
                                     "mma_sync_peak": MMA_SYNC_TFLOPS, "frac_of_mma_sync": tf / MMA_SYNC_TFLOPS},
                          "hbm": {"achieved_gbs": gbs, "peak_gbs": hpk, "frac": gbs / hpk,
                                  "algorithmic_bytes": w.compulsory_bytes()}},
-            "calls": args.ssd_steps, "workspace_bytes": nbytes, "launches_per_call": 3,
+            "calls": args.ssd_steps, "timing": "one CUDA graph of the calls", "workspace_bytes": nbytes,
+            "launches_per_call": 3,
             "kernel": "step sizes + C B^T per chunk (mma.sync); state walk and persistent read-out on tcgen05 "
                       "(TMEM accumulators, TMA operands, warp-specialised copier / MMA / worker warps); bf16 "
                       "operands (hi/lo pairs for products of inputs), fp32 accumulate"}

@@ -671,10 +671,12 @@ struct SsdTcWalk {
 
 // Bounded wait on a barrier phase that also gives up once another role has aborted.
 // Suspended between checks (up to 2 us a try), so that waiting warps leave the issue
-// slots to the warps with work.
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit,
+// slots to the warps with work. The limit is read from the parameters only once the first
+// try has failed, so no role keeps it in registers (the state walk needs three CTAs per SM).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const SsdParams& p,
                                         int err = kErrWaitMma) {
   if (mbar_try_wait(bar, parity)) return true;
+  const long long limit = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
   const long long start = clock64();
   while (!mbar_try_wait_suspend(bar, parity, 2000u)) {
     if (*abort) return false;
@@ -699,7 +701,7 @@ __device__ __forceinline__ bool bar_and(bool v, int bar_id, int n) {
 }
 
 template <int N>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kTcThreads, 3)
     ssd_state_walk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                              const SsdParams p) {
   using L = SsdTcWalk<N>;
@@ -714,7 +716,6 @@ __global__ void __launch_bounds__(kTcThreads)
   uint64_t* loaded = full + 8;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem_raw + L::kSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem_raw + L::kAbort);
-  const long long lim = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb0 = blockIdx.x * NB;
   const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (p.H / p.G);
@@ -757,7 +758,7 @@ __global__ void __launch_bounds__(kTcThreads)
     if (lane == 0 && !p.fault_skip_loads) {
       for (int c = 0; c < nc; ++c) {
         // stage c % 2 last held chunk c - 2: wait until its MMA has read it
-        if (c >= 2 && !tc_wait(&empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1), abort, lim)) break;
+        if (c >= 2 && !tc_wait(&empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1), abort, p)) break;
         load(c & 1, c);
       }
     }
@@ -765,8 +766,8 @@ __global__ void __launch_bounds__(kTcThreads)
     if (lane == 0) {
       for (int c = 0; c < nc; ++c) {
         const int s = c & 1;
-        if (!tc_wait(&full[s], (uint32_t)((c >> 1) & 1), abort, lim)) break;
-        if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort, lim)) break;
+        if (!tc_wait(&full[s], (uint32_t)((c >> 1) & 1), abort, p)) break;
+        if (c >= 2 && !tc_wait(&tempty[s], (uint32_t)(((c - 2) >> 1) & 1), abort, p)) break;
         tc_fence_after();
         const unsigned char* st = smem_raw + s * L::kStage;
         const uint32_t xa = umma_saddr(st + L::kX), wa = umma_saddr(st + L::kW);
@@ -798,7 +799,7 @@ __global__ void __launch_bounds__(kTcThreads)
     // releases its TMEM buffer
     auto epilogue = [&](int c, float dec) {
       const int s = c & 1;
-      if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort, lim)) return false;
+      if (!tc_wait(&tfull[s], (uint32_t)((c >> 1) & 1), abort, p)) return false;
       tc_fence_after();
       float Sc[NB];
       {  // the high part's 32 columns, then the low part's
@@ -834,7 +835,7 @@ __global__ void __launch_bounds__(kTcThreads)
     float dec_prev = 0.f;  // exp(cs_end) of chunk c - 1
     for (int c = 0; c < nc; ++c) {
       const int s = c & 1;
-      if (ok && !tc_wait(&loaded[s], (uint32_t)((c >> 1) & 1), abort, lim, kErrWaitFull)) ok = false;
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((c >> 1) & 1), abort, p, kErrWaitFull)) ok = false;
       const int rv = (int)((p.L - (int64_t)c * Q) < Q ? (p.L - (int64_t)c * Q) : Q);
       if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
         unsigned char* st = smem_raw + s * L::kStage;
@@ -1188,7 +1189,6 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
   uint64_t* tempty = loaded + 8;                                  // [2]
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L::kSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
-  const long long lim = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
   float* ecs = reinterpret_cast<float*>(sm + L::kEcs);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t items = p.batch * p.nc * p.H;
@@ -1221,7 +1221,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         if (it >= items) break;
         const int s = k & 1;
         // stage s last held item k - 2: wait until its MMAs have read it
-        if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, lim)) break;
+        if (k >= 2 && !tc_wait(&empty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, p)) break;
         unsigned char* st = sm + s * L::kStage;
         const SsdItem m = wk.item();
         const int32_t row = (int32_t)(m.b * p.L + m.t0);
@@ -1244,8 +1244,8 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         const int64_t it = blockIdx.x + (int64_t)k * gridDim.x;
         if (it >= items) break;
         const int s = k & 1;
-        if (!tc_wait(&full[s], (uint32_t)((k >> 1) & 1), abort, lim)) break;
-        if (k >= 2 && !tc_wait(&tempty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, lim)) break;
+        if (!tc_wait(&full[s], (uint32_t)((k >> 1) & 1), abort, p)) break;
+        if (k >= 2 && !tc_wait(&tempty[s], (uint32_t)(((k - 2) >> 1) & 1), abort, p)) break;
         tc_fence_after();
         const unsigned char* st = sm + s * L::kStage;
         const uint32_t xa = umma_saddr(st + L::kX), ca = umma_saddr(st + L::kC), ha = umma_saddr(st + L::kH);
@@ -1272,7 +1272,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     auto epilogue = [&](int k, const SsdItem& m) {
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
       const int bsel = k & 1;
-      if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort, lim)) return false;
+      if (!tc_wait(&tfull[bsel], (uint32_t)((k >> 1) & 1), abort, p)) return false;
       tc_fence_after();
       uint32_t v1[16], v2[16];
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)bsel + 16u * (uint32_t)th;
@@ -1304,7 +1304,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       unsigned char* st = sm + s * L::kStage;
       const SsdItem m = wk.item();
       const int rv = (int)((p.L - m.t0) < Q ? (p.L - m.t0) : Q);
-      if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort, lim, kErrWaitFull)) ok = false;
+      if (ok && !tc_wait(&loaded[s], (uint32_t)((k >> 1) & 1), abort, p, kErrWaitFull)) ok = false;
       if (ok && rv < Q) {  // steps past L: zero rows of X (another batch row's data or fill)
         for (int i = tid; i < (Q - rv) * (P / 8); i += kTcScanWorkers) {
           const int t = rv + i / (P / 8), c = i % (P / 8);
