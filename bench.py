@@ -212,11 +212,25 @@ def oracle_sample(w, seconds, seed=0):
     return k * L, t, k, threads
 
 
+def cpu_model():
+    """The host CPU's model name (Linux /proc/cpuinfo), or the platform's processor string."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline_obj(w, seconds):
     elems, t, k, threads = oracle_sample(w, seconds)
     frac = elems / w.elems
     gbs = w.compulsory_bytes() * frac / t / 1e9
     return {"value": gbs, "unit": "GB/s", "elem_per_s": elems / t, "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
             "sample": f"{k} whole-sequence channels (L={w.L}, N={w.N}) of batch row 0, fp64, "
                       f"{threads} threads, {t:.1f} s; GB/s scaled by the sample's share of compulsory bytes"}
 
@@ -245,6 +259,7 @@ def run_reference(args, w, ws, rank):
                        "sample_per_step": f"~{statistics.median(ks)} whole-sequence channels"},
             "elem_per_s": elems / total,
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
                              "sample": f"each step: whole-sequence channels of one batch row, ~{per_step:.1f} s"},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
