@@ -176,8 +176,9 @@ def max_over_ranks(x, ws):
 
 
 # ---- CPU oracle timing -----------------------------------------------------------------
-def oracle_sample(w, seconds, seed=0):
-    """Time the oracle on whole-sequence channels of batch row 0, sized to ~``seconds``.
+def oracle_sample(w, seconds, seed=0, threads=None):
+    """Time the oracle on whole-sequence channels of batch row 0, sized to ~``seconds``, on
+    ``threads`` host threads (all CPUs by default).
     Returns (elements (B*L*D units) processed, wall seconds, channels, threads)."""
     import numpy as np
     import torch
@@ -185,7 +186,7 @@ def oracle_sample(w, seconds, seed=0):
     import oracle
     from selective_state_space_141_b300 import inputs
 
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     g = torch.Generator().manual_seed(seed)
     L, N = w.L, w.N
 
@@ -227,10 +228,13 @@ def cpu_model():
 
 def cpu_baseline_obj(w, seconds):
     elems, t, k, threads = oracle_sample(w, seconds)
+    e1, t1, k1, _ = oracle_sample(w, min(2.0, seconds), threads=1)
     frac = elems / w.elems
     gbs = w.compulsory_bytes() * frac / t / 1e9
     return {"value": gbs, "unit": "GB/s", "elem_per_s": elems / t, "cores": threads, "kind": "oracle",
             "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "single_thread": {"elem_per_s": e1 / t1, "GB/s": w.compulsory_bytes() * (e1 / w.elems) / t1 / 1e9,
+                              "sample": f"{k1} whole-sequence channels, 1 thread, {t1:.1f} s"},
             "sample": f"{k} whole-sequence channels (L={w.L}, N={w.N}) of batch row 0, fp64, "
                       f"{threads} threads, {t:.1f} s; GB/s scaled by the sample's share of compulsory bytes"}
 
