@@ -426,7 +426,6 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   // N = 16 leave sum j in lane j)
   const int n_red = N == 16 ? lane : (vidx / NH) * N + nb + (vidx % NH);
   const bool writer = (lane & ((1 << (5 - kLog)) - 2)) == 0;
-  const bool lead = half == 0 && vd;  // writes the channel's per-step outputs
   TG* du = static_cast<TG*>(p.du) + b * L * D + d;
   TG* ddl = static_cast<TG*>(p.ddelta) + b * L * D + d;
   TG* dzp = p.dz ? static_cast<TG*>(p.dz) + b * L * D + d : nullptr;
@@ -513,7 +512,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       const float dr = ddt * sxv.x;
       dD_acc = fmaf(s.z, s.w, dD_acc);
       dbias_acc += dr;
-      if (lead) {
+      if (vd) {  // both lanes of the channel hold the same sums and write the same values
         *pdu = from_f32<TG>(dux);
         *pddl = from_f32<TG>(dr);
         if (dzp) *pdz = from_f32<TG>(sxv.y * v);  // dz = dy v silu'(z)
