@@ -166,6 +166,24 @@ template <typename T, typename TG, int N>
 __device__ __forceinline__ void stage_chunk(BwdStage<T, TG, N>& sg, const BwdParams& p, int64_t b, int c, int64_t d0,
                                             bool reverse, int lane) {
   const int64_t t0 = (int64_t)c * kBwdK;
+  if constexpr (sizeof(T) == 2 && sizeof(TG) == 2 && N == 16) {
+    // a whole chunk of a whole channel block: no clamping; lane l copies the 16 bytes at row
+    // l / 2, half l % 2 of each (step x channel) tile, and piece l of the B and C blocks
+    if (p.async_ok && t0 + kBwdK <= p.L && d0 + kBwdCh <= p.D) {
+      const int64_t off = (b * p.L + t0 + (lane >> 1)) * p.D + d0 + (lane & 1) * 8;
+      const int64_t offbc = (b * p.L + t0) * N + lane * 8;
+      cp_async16(&sg.u[0][0] + lane * 8, static_cast<const T*>(p.u) + off, 16);
+      cp_async16(&sg.dl[0][0] + lane * 8, static_cast<const T*>(p.delta) + off, 16);
+      cp_async16(&sg.B[0] + lane * 8, static_cast<const T*>(p.B) + offbc, 16);
+      if (reverse) {
+        cp_async16(&sg.dy[0][0] + lane * 8, static_cast<const TG*>(p.dy) + off, 16);
+        if (p.z) cp_async16(&sg.z[0][0] + lane * 8, static_cast<const T*>(p.z) + off, 16);
+        cp_async16(&sg.C[0] + lane * 8, static_cast<const T*>(p.C) + offbc, 16);
+      }
+      cp_async_commit();
+      return;
+    }
+  }
   stage_rows<T>(sg.u, static_cast<const T*>(p.u), b, t0, p.L, p.D, d0, p.async_ok, lane);
   stage_rows<T>(sg.dl, static_cast<const T*>(p.delta), b, t0, p.L, p.D, d0, p.async_ok, lane);
   stage_bc<T, N>(sg.B, static_cast<const T*>(p.B), b, t0, p.L, p.async_ok, lane);
