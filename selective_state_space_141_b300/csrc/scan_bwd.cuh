@@ -474,11 +474,23 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
       for (int q = 0; q < P2; ++q) h[q] = vd ? ckp[q] : make_float2(0.f, 0.f);
       // (the state after the last step stays in h: the reverse walk starts from it)
+      // walked by pointer, as the reverse sweep below
+      const float4* rsc = sc + ch;
+      const float* rbc = bc + nb;
+      float2* rhs = hs2 + lane;
 #pragma unroll 4
       for (int k = 0; k < kc; ++k) {
 #pragma unroll
-        for (int q = 0; q < P2; ++q) hs2[(k * P2 + q) * 32 + lane] = h[q];  // the state before step k
-        fwd_step(k);
+        for (int q = 0; q < P2; ++q) rhs[q * 32] = h[q];  // the state before step k
+        const float4 s = *rsc;
+        const float2 dt2 = make_float2(s.x, s.x), du2 = make_float2(s.y, s.y);
+        float2 b2[P2];
+        load_pairs<P2>(rbc, b2);
+#pragma unroll
+        for (int q = 0; q < P2; ++q) h[q] = __ffma2_rn(decay2<kAccurate>(dt2, Av[q], A2[q]), h[q], __fmul2_rn(du2, b2[q]));
+        rsc += kBwdCh;
+        rbc += 2 * N;
+        rhs += P2 * 32;
       }
     }
     // walk it backwards; h[] holds h_t of the current step (the chunk's last state first)
