@@ -1285,10 +1285,16 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       const int64_t ystride = p.H * P;
       TY* yb = static_cast<TY*>(p.y) + ((m.b * p.L + m.t0 + 16 * th) * p.H + m.h) * P + prow;
       const int tn = rv - 16 * th;  // steps of this quarter inside the sequence
+      if (tn >= 16) {  // a whole quarter: no per-step bounds
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        if (c < tn) *yb = from_f32<TY>(fmaf(e[c], __uint_as_float(v2[c]), __uint_as_float(v1[c])));
-        yb += ystride;
+        for (int c = 0; c < 16; ++c)
+          yb[c * ystride] = from_f32<TY>(fmaf(e[c], __uint_as_float(v2[c]), __uint_as_float(v1[c])));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < tn) *yb = from_f32<TY>(fmaf(e[c], __uint_as_float(v2[c]), __uint_as_float(v1[c])));
+          yb += ystride;
+        }
       }
       return true;
     };
