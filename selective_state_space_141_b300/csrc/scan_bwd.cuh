@@ -242,7 +242,8 @@ __device__ __forceinline__ float2 ld_pair(const T* src) {
 }
 // Softplus and sigmoid of two values on the bf16 path (2^x, log2 and the reciprocal on the
 // SFU, the rest as packed f32x2 ops): max(r, 0) + ln2 log2(1 + 2^(-|r| log2 e)), and
-// 1 / (1 + 2^(-x log2 e)).
+// 1 / (1 + 2^(-x log2 e)) (the denominator is at least 1, so the SFU's reciprocal is used
+// as it stands).
 __device__ __forceinline__ float2 softplus2_bwd(float2 r) {
   const float2 a = __fmul2_rn(make_float2(fabsf(r.x), fabsf(r.y)), make_float2(-kLog2e, -kLog2e));
   const float2 op = __fadd2_rn(make_float2(ex2(a.x), ex2(a.y)), make_float2(1.f, 1.f));
@@ -252,7 +253,10 @@ __device__ __forceinline__ float2 softplus2_bwd(float2 r) {
 __device__ __forceinline__ float2 sigmoid2_bwd(float2 x) {
   const float2 a = __fmul2_rn(x, make_float2(-kLog2e, -kLog2e));
   const float2 den = __fadd2_rn(make_float2(ex2(a.x), ex2(a.y)), make_float2(1.f, 1.f));
-  return make_float2(__fdividef(1.f, den.x), __fdividef(1.f, den.y));
+  float rx, ry;  // den >= 1: the approximate reciprocal needs no range handling
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rx) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ry) : "f"(den.y));
+  return make_float2(rx, ry);
 }
 
 // Decay factors of two states: 2^(dt A log2 e) on the SFU, or exp in double on the
