@@ -274,11 +274,13 @@ __device__ __forceinline__ float2 decay2(float2 dt2, float2 A, float2 A2) {
 //   bc  [kBwdK][2N]          f32  the chunk's B | C rows
 //   sc  [kBwdK][16]          f32x4 per (step, channel): dt, dt u, dv, u
 //   sx  [kBwdK][16]          f32x2 per (step, channel): d(dt)/d(delta), dy silu'(z)
-//   red [16][32]             f32  (N = 16) one step's dB | dC values per channel, for the channel sums
+//   red [2][16][32]          f32  (N = 16) a step's dB | dC values per channel, for the channel
+//                                 sums; two tiles, used by alternate steps
+// (N = 16, bf16: 31 KB, so that seven CTAs fit in an SM's 228 KB with their 1 KB reserve)
 //   stage                         raw inputs of one chunk (refilled as soon as they are read)
 template <typename T, typename TG, int N>
 constexpr int bwd_smem_bytes() {
-  return (kBwdK * (N / 2) * 32 + kBwdK * 2 * N + kBwdK * kBwdCh * 6 + (N == 16 ? kBwdCh * 32 : 0)) * 4 +
+  return (kBwdK * (N / 2) * 32 + kBwdK * 2 * N + kBwdK * kBwdCh * 6 + (N == 16 ? 2 * kBwdCh * 32 : 0)) * 4 +
          (int)sizeof(BwdStage<T, TG, N>);
 }
 
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   float4* sc = reinterpret_cast<float4*>(bc + kBwdK * 2 * N);  // [kBwdK][16]
   float2* sx = reinterpret_cast<float2*>(sc + kBwdK * kBwdCh);  // [kBwdK][16]
   float* red = reinterpret_cast<float*>(sx + kBwdK * kBwdCh);  // [16][32] when N = 16
-  BwdStage<T, TG, N>& sg = *reinterpret_cast<BwdStage<T, TG, N>*>(red + (N == 16 ? kBwdCh * 32 : 0));
+  BwdStage<T, TG, N>& sg = *reinterpret_cast<BwdStage<T, TG, N>*>(red + (N == 16 ? 2 * kBwdCh * 32 : 0));
   const int lane = threadIdx.x, ch = lane >> 1, half = lane & 1, nb = half * NH;
   const int w = blockIdx.x;
   const int64_t b = blockIdx.y;
@@ -460,6 +462,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
   // per phase) and the column reads each touch 32 distinct banks.
   const int fch = (ch & 1) | ((ch & 2) << 1);
   float4* red_w = reinterpret_cast<float4*>(red + ch * 32);
+  int rbuf = 0;  // float offset of this step's tile: 0 or kBwdCh * 32, alternating
   int rd_off[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) rd_off[c] = ((((lane >> 2) ^ ((c & 1) | ((c & 2) << 1))) << 2) | (lane & 3));
@@ -560,15 +563,18 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdParams p) {
       hsp -= P2 * 32;
       float sr;
       if constexpr (N == 16) {
-        red_w[(2 * half) ^ fch] = make_float4(vr[0], vr[1], vr[2], vr[3]);
-        red_w[(2 * half + 1) ^ fch] = make_float4(vr[4], vr[5], vr[6], vr[7]);
-        red_w[(4 + 2 * half) ^ fch] = make_float4(vr[8], vr[9], vr[10], vr[11]);
-        red_w[(5 + 2 * half) ^ fch] = make_float4(vr[12], vr[13], vr[14], vr[15]);
+        float4* rw = red_w + rbuf / 4;
+        const float* rr = red + rbuf;
+        rw[(2 * half) ^ fch] = make_float4(vr[0], vr[1], vr[2], vr[3]);
+        rw[(2 * half + 1) ^ fch] = make_float4(vr[4], vr[5], vr[6], vr[7]);
+        rw[(4 + 2 * half) ^ fch] = make_float4(vr[8], vr[9], vr[10], vr[11]);
+        rw[(5 + 2 * half) ^ fch] = make_float4(vr[12], vr[13], vr[14], vr[15]);
         __syncwarp();
-        sr = red[rd_off[0]];
+        sr = rr[rd_off[0]];
 #pragma unroll
-        for (int c = 1; c < kBwdCh; ++c) sr += red[c * 32 + rd_off[c & 3]];
-        __syncwarp();  // every lane has read before the next step's stores
+        for (int c = 1; c < kBwdCh; ++c) sr += rr[c * 32 + rd_off[c & 3]];
+        rbuf ^= kBwdCh * 32;  // the next step writes the other tile; this one is rewritten two
+                              // steps on, after the next step's barrier
       } else {
         sr = bwd_transpose_reduce<NV>(vr, lane);
       }
