@@ -52,3 +52,26 @@ def test_reference_arm_prints_only_on_rank_zero(capsys):
     args = types.SimpleNamespace(steps=1, warmup=0, gpus=2)
     bench.run_reference(args, inputs.TINY, 2, rank=1)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line(capsys):
+    """Rank 0 prints one JSON line with the bench contract's keys, the oracle as the timed
+    program (cpu_baseline kind "oracle", its thread count and CPU), and an e2e object with no
+    host-device bytes."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    from selective_state_space_141_b300 import inputs
+    args = types.SimpleNamespace(steps=1, warmup=0, gpus=1)
+    bench.run_reference(args, inputs.TINY, 1, rank=0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["steps"] == 1
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["cpu_model"]
+    e = line["e2e"]
+    assert e["value"] == line["value"] and e["unit"] == line["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
