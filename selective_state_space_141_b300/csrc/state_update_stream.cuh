@@ -131,6 +131,10 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
 
   // ---------------- consumers: thread = (channel j of the tile, state half g) ----------------
   const int j = tid >> 1, g = tid & 1, lane = tid & 31;
+  // the step-size-map variant advances the tile's first channel, (tile * kDecTile) mod D, by a
+  // fixed step per tile (measured faster there; the plain variant keeps the division)
+  int64_t dt0 = ((int64_t)blockIdx.x * kDecTile) % D;
+  const int64_t dstep = ((int64_t)gridDim.x * kDecTile) % D;
   int i = 0;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
     const int s = i % kDecStages;
@@ -156,9 +160,13 @@ __global__ void __launch_bounds__(kDecConsumers + 32) state_update_stream(const 
     if (kMap && p.delta_bias) dt += sg.bias[j];
     if (kMap && p.delta_softplus) dt = softplus_precise(dt);
     const float zz = p.z ? __bfloat162float(sg.z[j]) : 0.f;
-    // d: from the producer's tile offset with the conv prologue (measured faster there), by
-    // division otherwise (it can be computed before the barrier wait: measured faster there)
-    const int64_t d = kConv ? sg.d0 + j : (tile * kDecTile) % D + j;
+    // d: from the producer's tile offset with the conv prologue, by the running offset with
+    // the step-size map, by division in the plain step (each measured fastest for its variant)
+    const int64_t d = kConv ? sg.d0 + j : (kMap ? dt0 : (tile * kDecTile) % D) + j;
+    if (kMap && !kConv) {
+      dt0 += dstep;
+      if (dt0 >= D) dt0 -= D;
+    }
     const float dx = dt * x;
     const float4* sp = reinterpret_cast<const float4*>(sg.state + j * N + g * 8);
     const float4* ap = reinterpret_cast<const float4*>(sg.A + j * N + g * 8);
