@@ -1317,6 +1317,8 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
           *reinterpret_cast<uint4*>(st + L::kX + (c >> 3) * 8192 + t * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
+      // the item's cs in log2 units, so that W's decays are one ex2 each
+      if (ok && tid < Q) reinterpret_cast<float*>(st + L::kCs)[tid] *= kLog2e;
       if (!bar_and(ok, 1, kTcScanWorkers)) {
         ok = false;
         break;
@@ -1348,7 +1350,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int i = 8 * i8 + e;
-              w[e] = t >= i ? cbv[e] * __expf(ct - civ[e]) * div[e] : 0.f;
+              w[e] = t >= i ? cbv[e] * ex2(ct - civ[e]) * div[e] : 0.f;
               if (t == i) w[e] += Dh;
             }
             uint32_t hi[4], lo[4];
@@ -1359,7 +1361,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
           }
           *reinterpret_cast<uint4*>(st + L::kW + off) = hv;
           *reinterpret_cast<uint4*>(st + L::kW + Q * Q * 2 + off) = lv;
-          if (i8 == 0) ecs[s * Q + t] = __expf(ct);
+          if (i8 == 0) ecs[s * Q + t] = ex2(ct);
         }
       }
       fence_smem_to_async();
